@@ -1,0 +1,489 @@
+"""Benchmark: EAGLE-3 tree verify step at B = 64, Llama-3-8B shape, on one GB300.
+
+One step = the whole hot path over one batch of 64 sequences:
+  EAGLE-2 expansion, 8 levels (draft LM-head GEMM 4096 -> 128256 on the tcgen05
+  tensor cores for 1 + 7 x 10 frontier rows per sequence, softmax + top-10 per
+  row, per-level select), rerank to 60 nodes, tree attention for one layer
+  (32 q / 8 kv heads, d = 128, committed KV length 4096), verify-and-accept
+  (V = 128256, T = 1), and KV compaction over 32 layers.
+Metric: tree-verify steps/s (value) and accepted tokens/s; the dominant kernel's
+roofline fraction against the measured peaks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: the path shards by sequence with no exchange, so N ranks run N
+independent batches (weak scaling); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "tree-verify steps/sec & accepted tokens/s at B=64; HBM GB/s vs roofline"
+CFG = W.CONFIGS["eagle3_b64"]
+SEED = 0
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+class Step:
+    """Resident inputs and the call sequence of one verify step (all library calls)."""
+
+    def __init__(self, dev, seed=SEED):
+        import torch
+
+        import eagle_tree_speculative_gb300 as E
+        self.E, self.torch, self.dev = E, torch, dev
+        c = CFG
+        B, k, D, n, V, H = c.B, c.top_k, c.depth, c.n, c.V, c.H
+        self.B, self.k, self.D, self.n, self.V, self.H, self.R = B, k, D, n, V, H, c.R
+        # draft LM head, hidden states per level (host-generated, uploaded once)
+        self.w = W.lm_head(V, H, c.w_std, seed).to(dev)
+        self.hidden = [W.hidden_states(B, 1 if l == 1 else k, H, l, seed).to(dev)
+                       for l in range(1, D + 1)]
+        self.logits = torch.empty(B, c.R, V, device=dev)          # draft-logit storage
+        self.state = torch.empty(E.tree_state_size(B, k, D), dtype=torch.uint8, device=dev)
+        self.tokens = torch.empty(B, n, dtype=torch.int32, device=dev)
+        self.parent = torch.empty_like(self.tokens)
+        self.draft_row = torch.empty_like(self.tokens)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # attention inputs: queries of the tree nodes, one layer of the 32-layer cache
+        g = torch.Generator(device=dev).manual_seed(seed + 1)
+        self.q = torch.randn(B, n, c.Hq, c.head_dim, device=dev, generator=g).to(torch.bfloat16)
+        shape = (c.n_layers, B, c.Hkv, c.Lmax, c.head_dim)
+        self.kc = torch.randn(shape, device=dev, generator=g, dtype=torch.bfloat16)
+        self.vc = torch.randn(shape, device=dev, generator=g, dtype=torch.bfloat16)
+        self.kv_len0 = torch.full((B,), c.L, dtype=torch.int32, device=dev)
+        self.kv_len = self.kv_len0.clone()
+        self.attn_out = torch.empty_like(self.q)
+        ws = E.tree_attn_workspace_size(B, n, c.Hq, c.Hkv, c.head_dim, c.Lmax)
+        self.attn_ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        self.accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+        self.path = torch.empty(B, D + 1, dtype=torch.int32, device=dev)
+        self.emit = torch.empty(B, D + 1, dtype=torch.int32, device=dev)
+        # one expansion to fix the tree, then the synthetic target logits: the draft row of
+        # each expanded node plus N(0, sigma^2) noise, a fresh N(0, s^2) row for leaves
+        self.expand()
+        torch.cuda.synchronize()
+        s = float(c.w_std * np.sqrt(H))
+        rows = self.draft_row.long()
+        self.target = torch.empty(B, n, V, device=dev)
+        for b in range(B):
+            r = rows[b]
+            has = r >= 0
+            noise = torch.randn(n, V, device=dev, generator=g) * c.sigma
+            self.target[b] = torch.where(has[:, None], self.logits[b, r.clamp(min=0)] + noise,
+                                         torch.randn(n, V, device=dev, generator=g) * s)
+        torch.cuda.synchronize()
+        self.gemm_events = []
+
+    def expand(self, time_gemm=False):
+        E, torch = self.E, self.torch
+        for lvl in range(1, self.D + 1):
+            k_in = 1 if lvl == 1 else self.k
+            off = 0 if lvl == 1 else 1 + (lvl - 2) * self.k
+            if time_gemm:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            E.eagle_lmhead_gemm(self.hidden[lvl - 1].view(self.B * k_in, self.H), self.w,
+                                out=self.logits, ldo=self.V, rows_per_group=k_in,
+                                group_stride=self.R, row_offset=off, dev_status=self.status)
+            if time_gemm:
+                e1.record()
+                self.gemm_events.append((e0, e1, self.B * k_in))
+            E.eagle2_expand(lvl, lvl == self.D, self.logits, self.k, self.D, self.n, self.state,
+                            out_tokens=self.tokens, out_parent=self.parent,
+                            out_draft_row=self.draft_row, dev_status=self.status)
+
+    def run(self, seed, time_gemm=False):
+        E = self.E
+        self.expand(time_gemm)
+        E.eagle_tree_attn(self.q, self.kc[0], self.vc[0], self.kv_len, self.parent,
+                          out=self.attn_out, workspace=self.attn_ws, dev_status=self.status)
+        E.eagle_verify_accept(self.target, self.logits, self.tokens, self.parent, self.D, 1.0, seed,
+                              draft_row=self.draft_row, accept_len=self.accept_len, path=self.path,
+                              emit=self.emit, dev_status=self.status)
+        E.eagle_kv_compact(self.kc, self.vc, self.kv_len, self.path, self.accept_len, self.D,
+                           dev_status=self.status)
+        self.kv_len.copy_(self.kv_len0)      # keep the committed length fixed across steps
+
+    # kernels launched per step: per level GEMM + top-k + select (+ rerank at the last),
+    # attention (+ combine when split), verify, compaction
+    def launches_per_step(self):
+        c = CFG
+        ws = self.E.tree_attn_workspace_size(self.B, self.n, c.Hq, c.Hkv, c.head_dim, c.Lmax)
+        return self.D * 3 + 1 + (2 if ws else 1) + 1 + 1
+
+
+def time_region(fn, steps, torch):
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = measured_peaks()
+    st = Step(dev)
+    for i in range(args.warmup):
+        st.run(1000 + i)
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise RuntimeError(f"device status {int(st.status.item())} during warm-up")
+
+    # -------- device-resident timed region --------
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    accepted = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def body(i):
+        st.run(i, time_gemm=True)
+        accepted.add_(st.accept_len.sum() + st.B)
+
+    ms = time_region(body, args.steps, torch)
+    clk = clocks.stop()
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tok_per_step = float(accepted.item()) / args.steps
+    # dominant kernel: the LM-head GEMM, timed per launch inside the region
+    gemm_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in st.gemm_events)
+    gemm_rows = sum(m for _, _, m in st.gemm_events)
+    gemm_flops = 2.0 * gemm_rows * st.H * st.V
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+
+    # -------- per-call breakdown (separate short timing) --------
+    br = breakdown(st, torch)
+
+    # -------- end to end through the public API with host buffers --------
+    e2e = run_e2e(st, torch, max(5, min(args.steps, 20)))
+    if int(st.status.item()) != 0:
+        raise RuntimeError(f"device status {int(st.status.item())}")
+
+    out = {
+        "metric": METRIC,
+        "value": round(world * 1000.0 / ms_per_step, 3),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 GEMM/attention (fp32 accumulate), f32 logits",
+        "data": "synthetic (seeded normals; random-init LM head; no datasets or trained weights)",
+        "config": {"workload": "EAGLE-3 tree verify step, B=64, Llama-3-8B shape: EAGLE-2 "
+                               "expansion 8 levels x top-10 (LM head 4096->128256), rerank to 60 "
+                               "nodes, tree attention 1 layer (32q/8kv heads, d=128, KV 4096), "
+                               "verify V=128256 T=1 sigma=0.3, KV compaction 32 layers",
+                   "B": CFG.B, "nodes": CFG.n, "depth": CFG.depth, "top_k": CFG.top_k,
+                   "vocab": CFG.V, "hidden": CFG.H, "kv_len": CFG.L, "attn_layers": 1,
+                   "compact_layers": CFG.n_layers, "temperature": 1.0,
+                   "l2": "inputs larger than L2 (LM head 1.05 GB, logits 2.3 GB, KV 1.1 GB/layer)",
+                   "parallelism": f"replicas x{world} (sequence-sharded, no collective)"},
+        "accepted_tokens_per_s": round(world * tok_per_step * 1000.0 / ms_per_step, 1),
+        "mean_accept_len_plus_1": round(tok_per_step / st.B, 4),
+        "roofline": {"kernel": "lmhead_gemm_kernel (tcgen05)", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / peak, 4), "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained",
+                     "flops_per_step": gemm_flops / args.steps,
+                     "ms_per_step_in_kernel": round(gemm_ms / args.steps, 4)},
+        "breakdown_ms": br,
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    return out
+
+
+def breakdown(st, torch, reps=20):
+    """Per-call device time (ms) with its HBM figure, each call timed alone."""
+    E = st.E
+    c = CFG
+    res = {}
+
+    def t(fn):
+        for _ in range(3):
+            fn()
+        return time_region(lambda i: fn(), reps, torch) / reps
+
+    res["expand_8_levels"] = round(t(lambda: st.expand()), 4)
+    a = t(lambda: E.eagle_tree_attn(st.q, st.kc[0], st.vc[0], st.kv_len0, st.parent,
+                                    out=st.attn_out, workspace=st.attn_ws))
+    kv_bytes = 2 * c.B * c.Hkv * (c.L + c.n) * c.head_dim * 2
+    flops = 4.0 * c.B * c.n * c.Hq * c.head_dim * (c.L + c.n)
+    res["tree_attn_1_layer"] = round(a, 4)
+    res["tree_attn_GBps"] = round(kv_bytes / (a * 1e-3) / 1e9, 1)
+    res["tree_attn_TFLOPs"] = round(flops / (a * 1e-3) / 1e12, 1)
+    v = t(lambda: E.eagle_verify_accept(st.target, st.logits, st.tokens, st.parent, st.D, 1.0, 7,
+                                        draft_row=st.draft_row, accept_len=st.accept_len,
+                                        path=st.path, emit=st.emit))
+    res["verify_accept"] = round(v, 4)
+    rows_visited = float(st.accept_len.sum().item() + st.B)
+    res["verify_visited_row_GBps"] = round(2 * rows_visited * c.V * 4 / (v * 1e-3) / 1e9, 1)
+
+    def comp():
+        E.eagle_kv_compact(st.kc, st.vc, st.kv_len, st.path, st.accept_len, st.D)
+        st.kv_len.copy_(st.kv_len0)
+    res["kv_compact_32_layers"] = round(t(comp), 4)
+    s = t(lambda: E.eagle_softmax_stats(st.target, 1.0))
+    res["softmax_stats_all_rows_standalone"] = round(s, 4)
+    res["softmax_stats_GBps"] = round(st.target.numel() * 4 / (s * 1e-3) / 1e9, 1)
+    return res
+
+
+def run_e2e(st, torch, steps):
+    """The same step through the public API with the step's inputs in pinned host memory:
+    H2D of the hidden states, queries and target logits, D2H of the emitted tokens."""
+    host_hidden = [h.cpu().pin_memory() for h in st.hidden]
+    host_target = st.target.cpu().pin_memory()
+    host_q = st.q.cpu().pin_memory()
+    out_acc = torch.empty(st.B, dtype=torch.int32).pin_memory()
+    out_emit = torch.empty(st.B, st.D + 1, dtype=torch.int32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h in host_hidden) + \
+        host_target.numel() * 4 + host_q.numel() * 2
+    d2h = out_acc.numel() * 4 + out_emit.numel() * 4
+
+    def body(i):
+        for dst, src in zip(st.hidden, host_hidden):
+            dst.copy_(src, non_blocking=True)
+        st.target.copy_(host_target, non_blocking=True)
+        st.q.copy_(host_q, non_blocking=True)
+        st.run(5000 + i)
+        out_acc.copy_(st.accept_len, non_blocking=True)
+        out_emit.copy_(st.emit, non_blocking=True)
+
+    body(0)
+    ms = time_region(body, steps, torch)
+    return {"value": round(1000.0 * steps / ms, 3), "unit": "steps/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+class OracleSample:
+    """A bounded sample of one step, run by the CPU oracle as it stands.
+
+    Per sample: one sequence's expansion from its 71 draft-logit rows (top-10 /
+    select / rerank), its verify walk, its 32-layer compaction, its tree attention
+    restricted to one of the 8 kv heads (4 query heads), and ONE row of the LM-head
+    GEMM.  The step estimate scales each part to the full step: attention x8 heads
+    x64 sequences, GEMM x4544 rows, the rest x64 sequences.
+    """
+
+    def __init__(self, seed=SEED):
+        import oracle
+        self.o = oracle
+        c = CFG
+        self.c = c
+        trow, drows = W.tree_draft_rows(c, seed, B=1)
+        self.drows = drows
+        self.tree = oracle.eagle2_from_logits(drows, c.top_k, c.depth, c.n)
+        self.tgt = W.assemble_target(trow, self.tree["draft_row"], self.tree["cand"],
+                                     c.target_std, seed)
+        G = c.Hq // c.Hkv
+        self.q, self.k, self.v, self.kv_len = W.attn_inputs(1, c.n, G, 1, c.head_dim, c.L, c.Lmax, seed)
+        self.h = W.to_bf16(W.normal((1, c.H), 1.0, seed, 99))
+        self.w = W.lm_head(c.V, c.H, c.w_std, seed)
+        kc, vc = W.kv_cache(1, 1, c.Hkv, c.Lmax, c.head_dim, seed)
+        import torch
+        self.kb = kc.view(torch.int16).numpy().view(np.uint16)
+        self.vb = vc.view(torch.int16).numpy().view(np.uint16)
+        self.gemm_rows = c.B * c.R - c.B * (c.top_k - 1)    # 64 + 7 * 640 = 4544
+
+    def run(self):
+        o, c = self.o, self.c
+        t = {}
+        t0 = time.perf_counter()
+        o.eagle2_from_logits(self.drows, c.top_k, c.depth, c.n)
+        t["expand"] = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        r = o.verify_accept(self.tgt, self.drows, self.tree["tokens"], self.tree["parent"], c.depth,
+                            1.0, 0, draft_row=self.tree["draft_row"])
+        t["verify"] = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        o.tree_attn(self.q, self.k, self.v, self.kv_len, self.tree["parent"], c.head_dim ** -0.5)
+        t["attn_1head"] = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        o.lmhead_rows(self.h, self.w, np.zeros(1, np.int32))
+        t["gemm_1row"] = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        kl = np.full(1, c.L, np.int32)
+        for _ in range(c.n_layers):
+            kl[0] = c.L
+            o.kv_compact(self.kb, self.vb, kl, r["path"], r["accept_len"], c.depth)
+        t["compact"] = time.perf_counter() - t0
+        est = (c.B * (t["expand"] + t["verify"] + t["compact"] + c.Hkv * t["attn_1head"])
+               + self.gemm_rows * t["gemm_1row"])
+        return est, t
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+SAMPLE_DESC = ("one sequence per sample: expansion from 71 draft-logit rows, verify walk, "
+               "32-layer compaction, tree attention for 1 of 8 kv heads, 1 of 4544 LM-head "
+               "rows; scaled to the full B=64 step (x64 sequences, x8 heads, x4544 rows)")
+
+
+def cpu_baseline(budget_s=15.0):
+    s = OracleSample()
+    ests = []
+    t_start = time.perf_counter()
+    while not ests or time.perf_counter() - t_start < budget_s:
+        est, _ = s.run()
+        ests.append(est)
+    est = float(np.median(ests))
+    return {"value": round(1.0 / est, 6), "unit": "steps/s", "cores": cpu_threads(),
+            "kind": "oracle", "sample": SAMPLE_DESC + f"; {len(ests)} samples"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    s = OracleSample()
+    for _ in range(args.warmup):
+        s.run()
+    ests = [s.run()[0] for _ in range(args.steps)]
+    est = float(np.median(ests))
+    value = 1.0 / est
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (CPU oracle)", "data": "synthetic",
+            "config": {"workload": "EAGLE-3 tree verify step, B=64, Llama-3-8B shape "
+                                   "(same workload as the GPU arm; bounded CPU sample, scaled)"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cpu_threads(),
+                             "kind": "oracle", "sample": SAMPLE_DESC},
+            "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    out = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""GB300 (sm_103a) draft-tree verify-and-accept for EAGLE-style speculative decoding.
+
+Thin binding over the C ABI of include/eagle.h: every function marshals torch
+CUDA tensors into device pointers plus the current CUDA stream and calls the
+library entry point of the same name; all arithmetic runs in the library's
+kernels.  PyTorch only provides device memory and streams.  Functions raise
+EagleError on a non-OK status; errors found in device data are reported through
+the optional ``dev_status`` int32 tensor (bits EAGLE_DEV_*).
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+EAGLE_DEV_BAD_TREE = 0x01
+EAGLE_DEV_BAD_TOKEN = 0x02
+EAGLE_DEV_NONFINITE = 0x04
+EAGLE_DEV_DEPTH = 0x08
+EAGLE_DEV_CAPACITY = 0x10
+EAGLE_DEV_TIMEOUT = 0x20
+
+
+class EagleError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {_lib.load().eagle_status_str(code).decode()} ({code})")
+
+
+def lib():
+    return _lib.load()
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise EagleError(fn, code)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _status(dev_status, device):
+    if dev_status is None:
+        return None
+    return _dev(dev_status, "dev_status", torch.int32)
+
+
+# ---------------------------------------------------------------- workspace sizes
+def tree_attn_workspace_size(B, n, Hq, Hkv, head_dim, Lmax) -> int:
+    return int(lib().eagle_tree_attn_workspace_size(B, n, Hq, Hkv, head_dim, Lmax))
+
+
+def tree_state_size(B, top_k, depth) -> int:
+    return int(lib().eagle2_tree_state_size(B, top_k, depth))
+
+
+# ---------------------------------------------------------------- calls
+def eagle_tree_attn(q, k_cache, v_cache, kv_len, parent, scale=None, out=None, workspace=None,
+                    dev_status=None, stream=None):
+    """q [B,n,Hq,d], k/v cache [B,Hkv,Lmax,d] bf16; kv_len [B], parent [B,n] int32."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache", torch.bfloat16)
+    _dev(v_cache, "v_cache", torch.bfloat16)
+    _dev(kv_len, "kv_len", torch.int32)
+    _dev(parent, "parent", torch.int32)
+    B, n, Hq, d = q.shape
+    Hkv, Lmax = k_cache.shape[-3], k_cache.shape[-2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.bfloat16)
+    need = tree_attn_workspace_size(B, n, Hq, Hkv, d, Lmax)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("eagle_tree_attn", lib().eagle_tree_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(parent), _ptr(out),
+        B, n, Hq, Hkv, d, Lmax, float(scale), _ptr(workspace), ws_bytes,
+        _ptr(_status(dev_status, q.device)), _stream(stream)))
+    return out
+
+
+def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, temperature, seed,
+                        draft_row=None, accept_len=None, path=None, emit=None, row_stats=None,
+                        dev_status=None, stream=None):
+    """Returns (accept_len [B], path [B,D+1], emit [B,D+1]) int32 tensors."""
+    _dev(target_logits, "target_logits", torch.float32)
+    B, n, V = target_logits.shape
+    R = n
+    if draft_logits is not None:
+        _dev(draft_logits, "draft_logits", torch.float32)
+        R = draft_logits.shape[1]
+    _dev(tokens, "tokens", torch.int32)
+    _dev(parent, "parent", torch.int32)
+    if draft_row is not None:
+        _dev(draft_row, "draft_row", torch.int32)
+    dev = target_logits.device
+    D = int(max_depth)
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
+    path = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if path is None else path
+    emit = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if emit is None else emit
+    if row_stats is not None:
+        _dev(row_stats, "row_stats", torch.float32)
+    _check("eagle_verify_accept", lib().eagle_verify_accept(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_row), _ptr(tokens), _ptr(parent),
+        B, n, V, R, D, float(temperature), int(seed) & (2**64 - 1),
+        _ptr(accept_len), _ptr(path), _ptr(emit), _ptr(row_stats),
+        _ptr(_status(dev_status, dev)), _stream(stream)))
+    return accept_len, path, emit
+
+
+def eagle_kv_compact(k_cache, v_cache, kv_len, path, accept_len, max_depth, dev_status=None,
+                     stream=None):
+    """k/v cache [n_layers,B,Hkv,Lmax,d] bf16 (in place); kv_len updated in place."""
+    _dev(k_cache, "k_cache", torch.bfloat16)
+    _dev(v_cache, "v_cache", torch.bfloat16)
+    _dev(kv_len, "kv_len", torch.int32)
+    _dev(path, "path", torch.int32)
+    _dev(accept_len, "accept_len", torch.int32)
+    nl, B, Hkv, Lmax, d = k_cache.shape
+    _check("eagle_kv_compact", lib().eagle_kv_compact(
+        _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(path), _ptr(accept_len),
+        nl, B, Hkv, d, Lmax, int(max_depth), _ptr(_status(dev_status, k_cache.device)),
+        _stream(stream)))
+
+
+def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=None,
+                  lm_head_w=None, out_tokens=None, out_parent=None, out_draft_row=None,
+                  frontier_tokens=None, dev_status=None, stream=None):
+    """One EAGLE-2 level over draft-logit storage logits [B, R, V] (f32)."""
+    _dev(logits, "logits", torch.float32)
+    _dev(tree_state, "tree_state")
+    B, R, V = logits.shape
+    H = 0
+    if hidden is not None:
+        _dev(hidden, "hidden", torch.bfloat16)
+        _dev(lm_head_w, "lm_head_w", torch.bfloat16)
+        H = hidden.shape[-1]
+    for name, t in (("out_tokens", out_tokens), ("out_parent", out_parent),
+                    ("out_draft_row", out_draft_row), ("frontier_tokens", frontier_tokens)):
+        if t is not None:
+            _dev(t, name, torch.int32)
+    nbytes = tree_state.numel() * tree_state.element_size()
+    _check("eagle2_expand", lib().eagle2_expand(
+        int(level), int(final), _ptr(hidden), _ptr(lm_head_w), _ptr(logits), B, H, V, top_k, depth,
+        n_out, _ptr(tree_state), nbytes, _ptr(out_tokens), _ptr(out_parent), _ptr(out_draft_row),
+        _ptr(frontier_tokens), _ptr(_status(dev_status, logits.device)), _stream(stream)))
+
+
+def eagle_softmax_stats(logits, temperature, row_max=None, row_sum=None, row_argmax=None,
+                        dev_status=None, stream=None):
+    _dev(logits, "logits", torch.float32)
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    dev = logits.device
+    shp = logits.shape[:-1]
+    if temperature > 0:
+        row_max = torch.empty(shp, dtype=torch.float32, device=dev) if row_max is None else row_max
+        row_sum = torch.empty(shp, dtype=torch.float32, device=dev) if row_sum is None else row_sum
+    if row_argmax is None:
+        row_argmax = torch.empty(shp, dtype=torch.int32, device=dev)
+    _check("eagle_softmax_stats", lib().eagle_softmax_stats(
+        _ptr(logits), rows, V, float(temperature), _ptr(row_max), _ptr(row_sum), _ptr(row_argmax),
+        _ptr(_status(dev_status, dev)), _stream(stream)))
+    return row_max, row_sum, row_argmax
+
+
+def eagle_lmhead_gemm(hidden, w, out=None, ldo=None, rows_per_group=None, group_stride=0,
+                      row_offset=0, dev_status=None, stream=None):
+    """out[row(m)] = hidden[m] . W^T, hidden [M,K], w [N,K] bf16, out f32."""
+    _dev(hidden, "hidden", torch.bfloat16)
+    _dev(w, "w", torch.bfloat16)
+    M, K = hidden.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=hidden.device)
+    _dev(out, "out", torch.float32)
+    ldo = N if ldo is None else ldo
+    rpg = M if rows_per_group is None else rows_per_group
+    _check("eagle_lmhead_gemm", lib().eagle_lmhead_gemm(
+        _ptr(hidden), _ptr(w), _ptr(out), M, K, N, int(ldo), int(rpg), int(group_stride),
+        int(row_offset), _ptr(_status(dev_status, hidden.device)), _stream(stream)))
+    return out

@@ -1,0 +1,229 @@
+/*
+ * eagle.h -- C ABI of the GB300 (sm_103a) draft-tree verify-and-accept library.
+ *
+ * One step of EAGLE-style speculative decoding, split into the calls below:
+ *   eagle2_expand        EAGLE-2 draft-tree expansion and reranking, fed by the
+ *                        draft LM-head GEMM (tcgen05 tensor cores)
+ *   eagle_tree_attn      tree-masked GQA attention of the tree nodes over the
+ *                        committed KV cache plus their own ancestors
+ *   eagle_verify_accept  temperature softmax + Leviathan rejection walk over the
+ *                        tree, residual / bonus sampling, greedy mode at T = 0
+ *   eagle_kv_compact     move the accepted path's K/V rows behind the committed
+ *                        prefix and advance the logical length
+ * plus two building blocks exposed for measurement and testing
+ * (eagle_softmax_stats, eagle_lmhead_gemm).
+ *
+ * Pages (cited by title and section):
+ *   Lesson: "推测解码与 EAGLE-3" -- "不变量：Leviathan 拒绝采样", "KV cache 回滚",
+ *           "动手构建" steps 1-4.
+ *   Guide:  "EAGLE-1/2/3 拆解：推测解码省的是大模型前向次数，赚不赚看草稿准确率" --
+ *           "无损性的来源与它的证明位置", "EAGLE-2：草稿树的 Expansion 与 Reranking",
+ *           "EAGLE-3：取消特征约束..." (the draft head's own lm_head),
+ *           "一次 eagenerate 调用的完整流转".
+ *   TTT:    "EAGLE-3 完全拆解：Training-Time Test ..." -- "EAGLE-3 和 EAGLE-2 动态树如何拼在一起".
+ *
+ * Conventions shared by every call
+ *   - Every pointer is caller-owned DEVICE memory unless stated otherwise; the
+ *     library never allocates, frees, synchronises or prints.  Arrays are dense
+ *     row-major in the shapes given.  bf16 data is passed as raw 16-bit words.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work; results are ready when the stream is.
+ *   - Host-checkable errors (bad sizes, NULL pointers, unsupported shapes) return
+ *     a non-zero eagle_status and launch nothing.
+ *   - Errors only visible in device data never trap: the kernel skips the
+ *     affected sequence (accept_len = -1 where there is one), and ORs an
+ *     EAGLE_DEV_* bit into *dev_status (an int32 in device memory the caller
+ *     zeroes and reads when it synchronises).  dev_status may be NULL.
+ *   - No global mutable state; calls on different streams are independent
+ *     unless they share output buffers.
+ *   - Shapes: n (tree nodes, root included) <= 64; head_dim == 128;
+ *     Hq % Hkv == 0; temperature == 0 selects greedy decoding.
+ */
+#ifndef EAGLE_GB300_H
+#define EAGLE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EAGLE_OK = 0,
+    EAGLE_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, T < 0 ...      */
+    EAGLE_ERR_SHAPE = 2,        /* unsupported shape (n > 64, head_dim != 128) */
+    EAGLE_ERR_CAPACITY = 3,     /* a buffer or workspace is too small          */
+    EAGLE_ERR_CUDA = 4,         /* a CUDA launch / runtime call failed         */
+    EAGLE_ERR_DEVICE_DATA = 5,  /* reserved for callers mapping dev_status     */
+    EAGLE_ERR_TIMEOUT = 6       /* a bounded device wait expired               */
+} eagle_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define EAGLE_DEV_BAD_TREE  0x01  /* parent[0] != -1 or parent[i] not in [0, i) */
+#define EAGLE_DEV_BAD_TOKEN 0x02  /* token or draft row index out of range      */
+#define EAGLE_DEV_NONFINITE 0x04  /* NaN / +inf logit, or an all -inf row        */
+#define EAGLE_DEV_DEPTH     0x08  /* tree deeper than max_depth                  */
+#define EAGLE_DEV_CAPACITY  0x10  /* kv_len[b] + n > Lmax                        */
+#define EAGLE_DEV_TIMEOUT   0x20  /* a bounded pipeline wait gave up             */
+
+typedef void* eagle_stream_t;
+
+/* ---------------------------------------------------------------------------
+ * eagle_tree_attn -- tree attention for one layer.
+ * Lesson "KV cache 回滚" (the verifier attends with a non-causal mask that
+ * follows the tree; one flash-attention call with a custom mask) and Guide
+ * "EAGLE-2" (tree attention lets all tree tokens go through one forward).
+ * For sequence b, node i, query head h (kv head h / (Hq/Hkv)):
+ *   keys   = committed rows 0 .. L_b-1  plus tree rows L_b + j for every j that
+ *            is i or an ancestor of i (L_b = kv_len[b]);
+ *   out    = softmax(scale * q . k) . v, fp32 accumulation, bf16 result.
+ *   q        bf16 [B, n, Hq, head_dim]
+ *   k_cache  bf16 [B, Hkv, Lmax, head_dim]  (tree K already written at rows L_b + j)
+ *   v_cache  bf16 [B, Hkv, Lmax, head_dim]
+ *   kv_len   int32 [B]      parent int32 [B, n]  (parent[0] = -1, parent[i] < i)
+ *   out      bf16 [B, n, Hq, head_dim]
+ *   workspace / ws_bytes: device scratch of at least
+ *            eagle_tree_attn_workspace_size(B, n, Hq, Hkv, head_dim, Lmax) bytes
+ *            (may be NULL when that size is 0); contents need no initialisation.
+ * Device errors: an invalid tree or kv_len[b] + n > Lmax sets a dev_status bit
+ * and writes zeros for that sequence.
+ * ------------------------------------------------------------------------- */
+size_t eagle_tree_attn_workspace_size(int B, int n, int Hq, int Hkv, int head_dim, int Lmax);
+eagle_status eagle_tree_attn(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* kv_len, const int32_t* parent, void* out,
+                             int B, int n, int Hq, int Hkv, int head_dim, int Lmax, float scale,
+                             void* workspace, size_t ws_bytes, int32_t* dev_status,
+                             eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle_verify_accept -- the Leviathan walk over the draft tree.
+ * Lesson "不变量" and steps 1-3; Guide "无损性的来源" and "EAGLE-2" (a node is
+ * accepted only if all its prefixes are).  q = softmax(target/T), p =
+ * softmax(draft/T).  From the root, the children of the current node v are
+ * tried in increasing index; child c with token x is accepted iff p(x) <= 0
+ * or u_c < q_cur(x) / p(x), u_c = Philox(seed; 0, c, b, 0) word 0 >> 8 times
+ * 2^-24.  A rejected child replaces q_cur by norm(max(0, q_cur - p)) (kept if
+ * that sums to 0).  An accepted child becomes v with q_cur = q(child).  When
+ * no child is accepted, the final token is drawn from q_cur (residual, or the
+ * bonus token from q(v)) by the exponential race argmax_t q_cur(t) / E_t,
+ * E_t = -ln u'_t, u'_t = (2 (w >> 9) + 1) 2^-24 with w = word (t & 3) of
+ * Philox(seed; t >> 2, 0, b, 1).  At temperature 0 a child is accepted iff
+ * its token is the argmax of target row v (lowest index on ties) and the
+ * final token is that argmax.
+ *   target_logits f32 [B, n, V]  row i: target logits after node i
+ *   draft_logits  f32 [B, R, V]  draft logits rows (only rows of nodes with
+ *                 children are read; unused at T = 0, may then be NULL)
+ *   draft_row     int32 [B, n] or NULL: row of draft_logits holding the draft
+ *                 distribution after node i (NULL: row i, and R must equal n)
+ *   tokens        int32 [B, n]  token of node i (node 0 ignored)
+ *   parent        int32 [B, n]
+ *   max_depth     D: the tree depth bound; sizes path and emit
+ *   temperature   T >= 0      seed: Philox key (low word, high word)
+ *   accept_len    int32 [B]       accepted drafts (root excluded), -1 on error
+ *   path          int32 [B, D+1]  node ids of the accepted path, root first, -1 padded
+ *   emit          int32 [B, D+1]  accepted draft tokens then the final token, -1 padded
+ *   row_stats     f32 [2, B, n, 2] or NULL: (max z, sum exp(z - max)) of the
+ *                 target (slot 0) and draft (slot 1) rows the walk visited;
+ *                 rows it did not visit are left untouched.
+ * No workspace.  Device errors: invalid tree / token / draft row, non-finite
+ * rows -> accept_len[b] = -1, path/emit = -1, dev_status bit.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_verify_accept(const float* target_logits, const float* draft_logits,
+                                 const int32_t* draft_row, const int32_t* tokens,
+                                 const int32_t* parent, int B, int n, int V, int R,
+                                 int max_depth, float temperature, uint64_t seed,
+                                 int32_t* accept_len, int32_t* path, int32_t* emit,
+                                 float* row_stats, int32_t* dev_status, eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle_kv_compact -- commit the accepted path into the KV cache.
+ * Lesson "KV cache 回滚" and "第 4 步" (one physical cache plus a logical
+ * length).  For t = 0 .. a (a = accept_len[b]): row L_b + path[b][t] moves to
+ * row L_b + t in every layer and kv head, for K and V (all source rows are read
+ * before any is written); then kv_len[b] = L_b + a + 1.
+ *   k_cache, v_cache bf16 [n_layers, B, Hkv, Lmax, head_dim], in place
+ *   kv_len int32 [B] (read and updated)   path int32 [B, D+1]   accept_len int32 [B]
+ * Sequences with accept_len < 0 are skipped.  L_b + path[a] >= Lmax or a > D
+ * sets EAGLE_DEV_CAPACITY and skips the sequence.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, const int32_t* path,
+                              const int32_t* accept_len, int n_layers, int B, int Hkv,
+                              int head_dim, int Lmax, int max_depth, int32_t* dev_status,
+                              eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle2_expand -- one level of EAGLE-2 expansion; optionally the rerank.
+ * Guide "EAGLE-2：草稿树的 Expansion 与 Reranking" and TTT "EAGLE-3 和 EAGLE-2
+ * 动态树如何拼在一起": node value V_i = product of draft confidences on the
+ * root path; each level runs the draft forward only on the top_k nodes of the
+ * previous level with the largest V; the rerank keeps the global top-n by V.
+ * Confidences c = softmax(draft logits) at temperature 1; each frontier row
+ * contributes its top_k tokens (larger logit first, lower token on ties);
+ * products are float32.  Level 1 expands the root row into top_k candidates;
+ * level l >= 2 expands the top_k frontier rows into top_k^2 candidates and keeps
+ * the top_k by V (lower candidate id on ties) as the next frontier.
+ * Candidate ids: root 0; level 1: 1 + j; level l: 1 + k + (l-2)k^2 + s k + j.
+ * Draft rows: root 0; frontier slot s chosen at level l < depth: 1 + (l-1)k + s.
+ *   level         1 .. depth (call in order; level 1 initialises tree_state)
+ *   final         non-zero: after this level, rerank and write the out_* arrays
+ *   hidden        bf16 [B, k_in, H] or NULL (k_in = 1 at level 1, top_k after):
+ *                 the draft model's output for the current frontier rows.  When
+ *                 given, logits rows of this level are computed as hidden . W^T.
+ *   lm_head_w     bf16 [V, H] (needed when hidden != NULL)
+ *   logits        f32 [B, R, V], R = 1 + (depth-1) top_k: draft-logit storage.
+ *                 This level's rows are written (hidden != NULL) or read.
+ *   tree_state    scratch of eagle2_tree_state_size(B, top_k, depth) bytes that
+ *                 persists across the levels of one tree
+ *   out_tokens, out_parent, out_draft_row  int32 [B, n_out] (final only):
+ *                 nodes in topological order (depth asc, V desc, id asc), root
+ *                 first with token -1 and draft row 0; out_draft_row = -1 for
+ *                 nodes that were never expanded.
+ *   frontier_tokens int32 [B, top_k] or NULL: tokens of the new frontier.
+ * Constraints: 1 <= top_k <= 16, top_k <= V, 2 <= n_out <= min(64, candidates+1),
+ * depth <= 16.  Device errors: non-finite logit rows set EAGLE_DEV_NONFINITE.
+ * ------------------------------------------------------------------------- */
+size_t eagle2_tree_state_size(int B, int top_k, int depth);
+eagle_status eagle2_expand(int level, int final, const void* hidden, const void* lm_head_w,
+                           float* logits, int B, int H, int V, int top_k, int depth, int n_out,
+                           void* tree_state, size_t state_bytes, int32_t* out_tokens,
+                           int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
+                           int32_t* dev_status, eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle_softmax_stats -- per-row temperature softmax statistics.
+ * z = logits / T; row_max = max z; row_sum = sum exp(z - row_max) (T > 0).
+ * At T = 0 only row_argmax is written (lowest index on ties).
+ *   logits f32 [rows, V]; row_max, row_sum f32 [rows] (may be NULL at T = 0);
+ *   row_argmax int32 [rows] or NULL.
+ * Non-finite rows set EAGLE_DEV_NONFINITE.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_softmax_stats(const float* logits, int64_t rows, int V, float temperature,
+                                 float* row_max, float* row_sum, int32_t* row_argmax,
+                                 int32_t* dev_status, eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle_lmhead_gemm -- the draft LM head, logits = hidden . W^T.
+ * Guide "EAGLE-3" code changes: the draft head's own lm_head = Linear(hidden,
+ * draft_vocab, bias=False).  bf16 inputs, fp32 accumulation and output, on the
+ * tcgen05 tensor cores.
+ *   hidden bf16 [M, K]   w bf16 [N, K]   (K % 64 == 0, 16-byte aligned bases)
+ *   out    f32: row m of the product is stored at
+ *          out + ((m / rows_per_group) * group_stride + row_offset + m % rows_per_group) * ldo
+ *          (rows_per_group = M, group_stride = 0, row_offset = 0: a plain [M, ldo] matrix)
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_lmhead_gemm(const void* hidden, const void* w, float* out, int M, int K, int N,
+                               int64_t ldo, int rows_per_group, int64_t group_stride,
+                               int64_t row_offset, int32_t* dev_status, eagle_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* eagle_status_str(eagle_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int eagle_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EAGLE_GB300_H */

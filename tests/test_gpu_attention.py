@@ -1,0 +1,94 @@
+"""GPU parity of eagle_tree_attn against the double-precision oracle.
+
+Tolerance: per (sequence, node, head) row, max|O_gpu - O_ref| / max|O_ref| <= 1e-2
+(bf16 inputs and output, fp32 accumulation, P rounded to bf16 for the PV product).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.helpers import attn_row_rel_err
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def _run(q, k, v, kv_len, parent, scale, status=None):
+    import eagle_tree_speculative_gb300 as E
+    st = torch.zeros(1, dtype=torch.int32, device="cuda") if status is None else status
+    out = E.eagle_tree_attn(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(kv_len).cuda(),
+                            torch.from_numpy(np.ascontiguousarray(parent)).cuda(), scale=scale,
+                            dev_status=st)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), int(st.item())
+
+
+def _check(B, n, Hq, Hkv, kv_len, Lmax, seed, parent=None, sample=None):
+    d = 128
+    q, k, v, kv_len = W.attn_inputs(B, n, Hq, Hkv, d, kv_len, Lmax, seed)
+    if parent is None:
+        parent = np.stack([W.random_tree(n, 8, seed, b) for b in range(B)])
+    scale = d ** -0.5
+    got, st = _run(q, k, v, kv_len, parent, scale)
+    assert st == 0
+    bs = range(B) if sample is None else sample
+    for b in bs:
+        ref = oracle.tree_attn(q[b:b + 1], k[b:b + 1], v[b:b + 1], kv_len[b:b + 1],
+                               parent[b:b + 1], scale)
+        err = attn_row_rel_err(got[b:b + 1], ref)
+        assert err.max() <= TOL, (b, err.max())
+    return got
+
+
+def test_small_ragged_lengths_several_tiles():
+    _check(B=3, n=13, Hq=8, Hkv=2, kv_len=[0, 37, 200], Lmax=230, seed=1)
+
+
+def test_gqa_groups_and_row_blocks():
+    # n * G = 21 * 8 = 168 rows: two 128-row blocks, ragged tail
+    _check(B=2, n=21, Hq=16, Hkv=2, kv_len=[300, 129], Lmax=330, seed=2)
+
+
+def test_lone_root_with_empty_cache_returns_value_row():
+    q, k, v, kv_len = W.attn_inputs(2, 1, 4, 2, 128, 0, 8, seed=3)
+    got, st = _run(q, k, v, kv_len, np.full((2, 1), -1, np.int32), 0.1)
+    assert st == 0
+    for b in range(2):
+        for h in range(4):
+            np.testing.assert_array_equal(got[b, 0, h], v[b, h // 2, 0].float().numpy())
+
+
+def test_chain_tree_matches_oracle_causal_case():
+    _check(B=2, n=20, Hq=4, Hkv=4, kv_len=[64, 100], Lmax=128, seed=4,
+           parent=np.stack([W.chain_tree(20)] * 2))
+
+
+def test_vicuna13b_shape_b1_split_kv():
+    """B=1, 60 nodes, 40 heads, L=2048: the split-KV path; every row checked."""
+    cfg = W.CONFIGS["eagle2_b1"]
+    _check(B=1, n=cfg.n, Hq=cfg.Hq, Hkv=cfg.Hkv, kv_len=cfg.L, Lmax=cfg.Lmax, seed=5)
+
+
+def test_llama3_8b_shape_b64_full_size_sampled():
+    """B=64, 60 nodes, 32/8 heads, L=4096 (the benchmark launch); 3 sequences checked."""
+    cfg = W.CONFIGS["eagle3_b64"]
+    _check(B=cfg.B, n=cfg.n, Hq=cfg.Hq, Hkv=cfg.Hkv, kv_len=cfg.L, Lmax=cfg.Lmax, seed=6,
+           sample=[0, 31, 63])
+
+
+@pytest.mark.parametrize("B,L", [(8, 512), (1, 8192)])
+def test_llama70b_shape_sweep_points(B, L):
+    cfg = W.CONFIGS["sweep_70b"]
+    _check(B=B, n=cfg.n, Hq=cfg.Hq, Hkv=cfg.Hkv, kv_len=L, Lmax=L + cfg.n, seed=7 + B,
+           sample=[0, B - 1] if B > 1 else None)
+
+
+def test_capacity_and_tree_errors_set_status_and_zero_output():
+    import eagle_tree_speculative_gb300 as E
+    q, k, v, kv_len = W.attn_inputs(2, 4, 2, 1, 128, [10, 3], 14, seed=8)
+    parent = np.array([[-1, 0, 1, 2], [-1, 2, 0, 1]], np.int32)     # second tree invalid
+    got, st = _run(q, k, v, kv_len, parent, 0.1)
+    assert st & E.EAGLE_DEV_CAPACITY and st & E.EAGLE_DEV_BAD_TREE   # 10 + 4 > 14 in seq 0
+    assert np.all(got == 0)

@@ -1,0 +1,192 @@
+"""GPU parity of eagle_verify_accept and eagle_softmax_stats against the oracle.
+
+Same seeded inputs on both sides (workloads/), element-by-element comparison:
+bit-exact at temperature 0; at temperature 1 identical except counted
+near-ties (see tests/helpers.py for the tolerances).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests.helpers import assert_tie_budget, compare_walks
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu():
+    import eagle_tree_speculative_gb300 as E
+    return E
+
+
+def _cuda(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _run_gpu(tgt, drf, tok, par, D, T, seed, draft_row=None, row_stats=False):
+    E = _gpu()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs = None
+    if row_stats:
+        B, n, _ = tgt.shape
+        rs = torch.full((2, B, n, 2), float("nan"), device="cuda")
+    acc, path, emit = E.eagle_verify_accept(
+        _cuda(tgt), None if drf is None else _cuda(drf), _cuda(tok), _cuda(par), D, T, seed,
+        draft_row=None if draft_row is None else _cuda(draft_row), row_stats=rs, dev_status=status)
+    torch.cuda.synchronize()
+    out = (acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(), int(status.item()))
+    return out + ((rs.cpu().numpy(),) if row_stats else ())
+
+
+# ---------------------------------------------------------------- chain (1000 steps)
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_chain_1000_steps_match_oracle(T):
+    cfg = W.CONFIGS["chain"]
+    B, n, V, D = 1000, cfg.n, cfg.V, cfg.depth
+    tgt, drf = W.chain_logits(B, n, V, cfg.sigma, cfg.target_std, seed=0)
+    tok = np.full((B, n), -1, np.int32)
+    tok[:, 1:] = oracle.sample_rows(drf[:, :n - 1], T, seed=0)    # draft i+1 ~ p(after node i)
+    par = np.broadcast_to(W.chain_tree(n), (B, n)).copy()
+    ref = oracle.verify_accept(tgt, drf, tok, par, D, T, seed=0)
+    acc, path, emit, st, rs = _run_gpu(tgt, drf, tok, par, D, T, 0, row_stats=True)
+    assert st == 0 and (ref["status"] == 0).all()
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+    assert_tie_budget(dec, ties)
+    if T > 0:
+        # softmax statistics of every visited row, 1e-5 relative
+        m, Z, _, _ = oracle.softmax_rows(tgt, T)
+        seen = ~np.isnan(rs[0, :, :, 0])
+        assert seen.sum() >= B
+        np.testing.assert_allclose(rs[0][..., 0][seen], m[seen], rtol=1e-6)
+        np.testing.assert_allclose(rs[0][..., 1][seen], Z[seen], rtol=1e-5)
+        mp, Zp, _, _ = oracle.softmax_rows(drf, T)
+        seen = ~np.isnan(rs[1, :, :, 0])
+        np.testing.assert_allclose(rs[1][..., 1][seen], Zp[seen], rtol=1e-5)
+
+
+# ---------------------------------------------------------------- EAGLE-2 trees
+def _tree_case(cfg, B, seed, V=None, sigma=None):
+    V = cfg.V if V is None else V
+    trow, drows = W.tree_draft_rows(cfg, seed, B=B, V=V, sigma=sigma)
+    tree = oracle.eagle2_from_logits(drows, cfg.top_k, cfg.depth, cfg.n)
+    tgt = W.assemble_target(trow, tree["draft_row"], tree["cand"], cfg.target_std, seed)
+    return tgt, drows, tree
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_eagle2_tree_b1_shape_matches_oracle(T):
+    cfg = W.CONFIGS["eagle2_b1"]
+    B = 40                                     # 40 independent B=1 problems in one launch
+    tgt, drows, tree = _tree_case(cfg, B, seed=1)
+    ref = oracle.verify_accept(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, T, seed=5,
+                               draft_row=tree["draft_row"])
+    acc, path, emit, st = _run_gpu(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, T, 5,
+                                   draft_row=tree["draft_row"])
+    assert st == 0
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+    assert_tie_budget(dec, ties)
+    assert ref["accept_len"].mean() > 0.5     # the synthetic draft is informative
+
+
+def test_eagle3_tree_b64_full_size_matches_oracle():
+    """Full B=64, n=60, depth 8, V=128256 verify (sigma 0.3, T=1)."""
+    cfg = W.CONFIGS["eagle3_b64"]
+    tgt, drows, tree = _tree_case(cfg, cfg.B, seed=2)
+    ref = oracle.verify_accept(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, 1.0, seed=9,
+                               draft_row=tree["draft_row"])
+    acc, path, emit, st = _run_gpu(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, 1.0, 9,
+                                   draft_row=tree["draft_row"])
+    assert st == 0
+    dec, ties = compare_walks(ref, acc, path, emit)
+    assert_tie_budget(dec, ties)
+
+
+@pytest.mark.parametrize("V", [1001, 7])
+def test_unaligned_vocab_and_tiny_vocab(V):
+    """V not a multiple of 4 takes the scalar path; V=7 leaves some CTAs of a cluster empty."""
+    B, n = 33, 9
+    tgt = W.per_seq_normal(B, (n, V), 2.0, 4, W.TAG_TARGET)
+    drf = tgt + W.per_seq_normal(B, (n, V), 0.7, 4, W.TAG_DRAFT_NOISE)
+    par = np.stack([W.random_tree(n, 4, 4, b) for b in range(B)])
+    tok = W.rng(4, 5).integers(0, V, size=(B, n), dtype=np.int32)
+    for T in (1.0, 0.0):
+        ref = oracle.verify_accept(tgt, drf, tok, par, 4, T, seed=3)
+        acc, path, emit, st = _run_gpu(tgt, drf, tok, par, 4, T, 3)
+        assert st == 0
+        dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+        assert_tie_budget(dec, ties)
+
+
+def test_root_only_tree_emits_one_bonus_token():
+    B, V = 50, 500
+    tgt = W.per_seq_normal(B, (1, V), 2.0, 6, W.TAG_TARGET)
+    par = np.full((B, 1), -1, np.int32)
+    tok = np.full((B, 1), -1, np.int32)
+    ref = oracle.verify_accept(tgt, tgt, tok, par, 0, 1.0, seed=8)
+    acc, path, emit, st = _run_gpu(tgt, tgt, tok, par, 0, 1.0, 8)
+    assert st == 0 and (acc == 0).all() and (path[:, 0] == 0).all()
+    compare_walks(ref, acc, path, emit)
+
+
+def test_device_errors_flag_and_skip_without_trapping():
+    E = _gpu()
+    V, n = 64, 4
+    tgt = W.per_seq_normal(4, (n, V), 1.0, 7, W.TAG_TARGET)
+    tgt[3, 0, 5] = np.nan
+    par = np.array([[-1, 0, 1, 2], [-1, 0, 3, 1], [0, 0, 1, 2], [-1, 0, 0, 1]], np.int32)
+    tok = np.array([[-1, 1, 2, 3], [-1, 1, 2, 3], [-1, 1, 2, 3], [-1, 1, 2, 3]], np.int32)
+    tok[0, 2] = V                                             # token out of range
+    acc, path, emit, st = _run_gpu(tgt, tgt, tok, par, 3, 1.0, 0)
+    assert list(acc) == [-1, -1, -1, -1]
+    assert st & E.EAGLE_DEV_BAD_TREE and st & E.EAGLE_DEV_BAD_TOKEN and st & E.EAGLE_DEV_NONFINITE
+    assert (path == -1).all() and (emit == -1).all()
+    # the context is healthy afterwards
+    tok[0, 2] = 2
+    par[1], par[2] = par[0], par[0]
+    tgt[3, 0, 5] = 0.0
+    acc, path, emit, st = _run_gpu(tgt, tgt, tok, par, 3, 1.0, 0)
+    assert st == 0 and (acc >= 0).all()
+
+
+def test_host_side_validation_returns_status_without_launch():
+    E = _gpu()
+    t = torch.zeros(1, 65, 8, device="cuda")
+    i = torch.zeros(1, 65, dtype=torch.int32, device="cuda")
+    with pytest.raises(E.EagleError) as ex:
+        E.eagle_verify_accept(t, t, i, i, 3, 1.0, 0)
+    assert ex.value.code == 2                                 # n > 64 -> EAGLE_ERR_SHAPE
+    with pytest.raises(E.EagleError) as ex:
+        E.eagle_verify_accept(t[:, :4], t[:, :4], i[:, :4], i[:, :4], 3, -1.0, 0)
+    assert ex.value.code == 1                                 # T < 0
+
+
+# ---------------------------------------------------------------- softmax statistics
+@pytest.mark.parametrize("V,T", [(32000, 1.0), (1001, 0.7), (32000, 0.0)])
+def test_softmax_stats_match_oracle(V, T):
+    E = _gpu()
+    x = W.per_seq_normal(3, (37, V), 2.0, 10, W.TAG_TARGET).reshape(111, V)
+    x[5, 17] = x[5].max() + 1.0
+    x[6, 3] = x[6, 9] = x[6].max() + 1.0                     # tie: lowest index wins
+    m, Z, am, st = oracle.softmax_rows(x, T)
+    gm, gz, ga = E.eagle_softmax_stats(_cuda(x), T)
+    torch.cuda.synchronize()
+    assert np.array_equal(ga.cpu().numpy(), am)
+    if T > 0:
+        np.testing.assert_allclose(gm.cpu().numpy(), m, rtol=1e-6)
+        np.testing.assert_allclose(gz.cpu().numpy(), Z, rtol=1e-5)
+
+
+def test_softmax_stats_full_size_sampled_rows():
+    """B*n = 3840 rows of V = 128256 on the GPU; 64 sampled rows checked by the oracle."""
+    E = _gpu()
+    B, n, V = 64, 60, 128256
+    x = W.per_seq_normal(B, (n, V), 2.0, 11, W.TAG_TARGET)
+    gm, gz, ga = E.eagle_softmax_stats(_cuda(x), 1.0)
+    torch.cuda.synchronize()
+    rows = W.rng(11, 1).choice(B * n, size=64, replace=False)
+    flat = x.reshape(B * n, V)[rows]
+    m, Z, am, _ = oracle.softmax_rows(flat, 1.0)
+    np.testing.assert_allclose(gm.reshape(-1).cpu().numpy()[rows], m, rtol=1e-6)
+    np.testing.assert_allclose(gz.reshape(-1).cpu().numpy()[rows], Z, rtol=1e-5)
+    assert np.array_equal(ga.reshape(-1).cpu().numpy()[rows], am)

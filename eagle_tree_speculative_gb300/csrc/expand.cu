@@ -79,38 +79,36 @@ __device__ __forceinline__ bool topk_better(float v, int i, float w, int j) {
     return v > w || (v == w && i < j);
 }
 
-// Lanes hold descending lists tv/ti (k valid entries, the rest sentinels).
-// Writes the warp's k best, in order, to out_v/out_i (lane 0 writes).
-__device__ __forceinline__ void warp_merge_topk(float (&tv)[kKMax], int (&ti)[kKMax], int k,
-                                                float* out_v, int* out_i) {
+// ---------------------------------------------------------------------------
+// Row softmax statistics + top-k in one pass over the vocabulary.
+// Statistics: each thread keeps an online (max, sum) with sum = sum
+// 2^((l - max) log2 e).  Top-k: each warp keeps ONE sorted list distributed
+// over its lanes (lane j holds the j-th best, order: logit desc, token asc).
+// A chunk of 4 logits per lane is filtered against the warp's current k-th
+// best (a ballot); the rare survivors are inserted one at a time with a
+// shuffle shift.  The block then merges the per-warp lists the same way.
+constexpr int kTopkThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Insert (v, i) into the warp list (lv, li) sorted desc; all lanes call with the
+// same (v, i).  Returns nothing; the list keeps its 32 best entries.
+__device__ __forceinline__ void warp_list_insert(float& lv, int& li, float v, int i) {
     const int lane = threadIdx.x & 31;
-    for (int j = 0; j < k; ++j) {
-        float bv = tv[0];
-        int bi = ti[0];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (topk_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
-        if (tv[0] == bv && ti[0] == bi) {       // ids are unique: exactly one winner lane
-#pragma unroll
-            for (int e = 0; e < kKMax - 1; ++e) { tv[e] = tv[e + 1]; ti[e] = ti[e + 1]; }
-            tv[kKMax - 1] = -INFINITY;
-            ti[kKMax - 1] = 0x7fffffff;
-        }
-        if (lane == 0) { out_v[j] = bv; out_i[j] = bi; }
+    const bool gt = topk_better(v, i, lv, li);            // candidate beats my entry
+    const float pv = __shfl_up_sync(0xffffffffu, lv, 1);
+    const int pi = __shfl_up_sync(0xffffffffu, li, 1);
+    const bool pgt = __shfl_up_sync(0xffffffffu, gt ? 1 : 0, 1) != 0;
+    if (gt) {
+        if (lane == 0 || !pgt) { lv = v; li = i; }
+        else { lv = pv; li = pi; }
     }
 }
-
-// ---------------------------------------------------------------------------
-constexpr int kTopkThreads = 256;
 
 __global__ void __launch_bounds__(kTopkThreads)
 row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int V, int k, int D,
                 void* state, int32_t* dev_status) {
-    __shared__ float s_v[(kTopkThreads / 32) * kKMax];
-    __shared__ int s_i[(kTopkThreads / 32) * kKMax];
+    __shared__ float s_v[kTopkThreads / 32][kKMax];
+    __shared__ int s_i[kTopkThreads / 32][kKMax];
     __shared__ float s_red[kTopkThreads / 32][2];
     __shared__ int s_bad[kTopkThreads / 32];
     __shared__ float s_pick_v[kKMax];
@@ -119,79 +117,133 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
     const int b = blockIdx.x / k_in, s = blockIdx.x % k_in;
     const float* x = logits + ((int64_t)b * R + off + s) * (int64_t)V;
 
-    float tv[kKMax];
-    int ti[kKMax];
-#pragma unroll
-    for (int j = 0; j < kKMax; ++j) { tv[j] = -INFINITY; ti[j] = 0x7fffffff; }
-    float thr_v = -INFINITY;
-    int thr_i = 0x7fffffff;
-    MaxSum ms{-INFINITY, 0.f};
+    float lv = -INFINITY;            // warp list entry of this lane
+    int li = 0x7fffffff;
+    float tv = -INFINITY;            // the warp's current k-th best (broadcast)
+    int ti = 0x7fffffff;
+    float m = -INFINITY, sum = 0.f;
     int bad = 0;
 
-    auto push = [&](float l, int t) {
-        bad |= isnan(l) || l == INFINITY;
-        if (l != -INFINITY) {
-            if (l > ms.m) { ms.s = (ms.m == -INFINITY) ? 0.f : ms.s * expf(ms.m - l); ms.m = l; }
-            ms.s += expf(l - ms.m);
-        }
-        if (topk_better(l, t, thr_v, thr_i)) {
-            float cv = l;
-            int ci = t;
-#pragma unroll
-            for (int j = 0; j < kKMax; ++j) {
-                if (j < k && topk_better(cv, ci, tv[j], ti[j])) {
-                    float fv = tv[j]; int fi = ti[j];
-                    tv[j] = cv; ti[j] = ci;
-                    cv = fv; ci = fi;
-                }
+    auto offer = [&](float v, int i, bool mine) {
+        // lanes with a surviving candidate insert it, one lane at a time
+        unsigned ball = __ballot_sync(0xffffffffu, mine && topk_better(v, i, tv, ti));
+        while (ball) {
+            const int src = __ffs(ball) - 1;
+            ball &= ball - 1;
+            const float cv = __shfl_sync(0xffffffffu, v, src);
+            const int ci = __shfl_sync(0xffffffffu, i, src);
+            if (topk_better(cv, ci, tv, ti)) {
+                warp_list_insert(lv, li, cv, ci);
+                tv = __shfl_sync(0xffffffffu, lv, k - 1);
+                ti = __shfl_sync(0xffffffffu, li, k - 1);
             }
-#pragma unroll
-            for (int j = 0; j < kKMax; ++j)
-                if (j == k - 1) { thr_v = tv[j]; thr_i = ti[j]; }
         }
+    };
+    auto chunk4 = [&](float4 l4, int t, bool valid) {
+        if (valid) {
+            bad |= isnan(l4.x) | isnan(l4.y) | isnan(l4.z) | isnan(l4.w) | (l4.x == INFINITY) |
+                   (l4.y == INFINITY) | (l4.z == INFINITY) | (l4.w == INFINITY);
+            const float mx = fmaxf(fmaxf(l4.x, l4.y), fmaxf(l4.z, l4.w));
+            if (mx > m) {
+                sum = (m == -INFINITY) ? 0.f : sum * exp2f((m - mx) * kLog2e);
+                m = mx;
+            }
+            if (m != -INFINITY)
+                sum += exp2f((l4.x - m) * kLog2e) + exp2f((l4.y - m) * kLog2e) +
+                       exp2f((l4.z - m) * kLog2e) + exp2f((l4.w - m) * kLog2e);
+        }
+        offer(l4.x, t, valid);
+        offer(l4.y, t + 1, valid);
+        offer(l4.z, t + 2, valid);
+        offer(l4.w, t + 3, valid);
     };
 
     if (((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0)) {
-#pragma unroll 2
-        for (int t = 4 * tid; t < V; t += 4 * kTopkThreads) {
-            float4 l4 = __ldg(reinterpret_cast<const float4*>(x + t));
-            push(l4.x, t); push(l4.y, t + 1); push(l4.z, t + 2); push(l4.w, t + 3);
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        const int n4 = V >> 2;
+        // warp-uniform trip counts: every lane of a warp runs the same iterations
+        int base = warp * 32;
+        for (; base + 3 * kTopkThreads < n4; base += 4 * kTopkThreads) {
+            const int t = base + lane;
+            const float4 a0 = __ldg(x4 + t), a1 = __ldg(x4 + t + kTopkThreads);
+            const float4 a2 = __ldg(x4 + t + 2 * kTopkThreads), a3 = __ldg(x4 + t + 3 * kTopkThreads);
+            chunk4(a0, 4 * t, true);
+            chunk4(a1, 4 * (t + kTopkThreads), true);
+            chunk4(a2, 4 * (t + 2 * kTopkThreads), true);
+            chunk4(a3, 4 * (t + 3 * kTopkThreads), true);
+        }
+        for (; base < n4; base += kTopkThreads) {
+            const int t = base + lane;
+            const bool ok = t < n4;
+            chunk4(ok ? __ldg(x4 + t) : make_float4(0.f, 0.f, 0.f, 0.f), 4 * t, ok);
         }
     } else {
-        for (int t = tid; t < V; t += kTopkThreads) push(x[t], t);
+        for (int base = warp * 32; base < V; base += kTopkThreads) {
+            const int t = base + lane;
+            const bool ok = t < V;
+            const float l = ok ? x[t] : 0.f;
+            if (ok) {
+                bad |= isnan(l) | (l == INFINITY);
+                if (l > m) { sum = (m == -INFINITY) ? 0.f : sum * exp2f((m - l) * kLog2e); m = l; }
+                if (m != -INFINITY) sum += exp2f((l - m) * kLog2e);
+            }
+            offer(l, t, ok);
+        }
     }
-    ms = warp_ms(ms);
+    // combine (max, sum) across the warp in the exp2 domain
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, o);
+        const float os = __shfl_xor_sync(0xffffffffu, sum, o);
+        if (om != -INFINITY) {
+            if (m == -INFINITY) { m = om; sum = os; }
+            else {
+                const float nm = fmaxf(m, om);
+                sum = sum * exp2f((m - nm) * kLog2e) + os * exp2f((om - nm) * kLog2e);
+                m = nm;
+            }
+        }
+    }
     bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) { s_red[warp][0] = ms.m; s_red[warp][1] = ms.s; s_bad[warp] = bad; }
-    // Each lane holds its k best, sorted.  Warp merge: k rounds of "warp-best
-    // head, winner pops"; then warp 0 merges the per-warp lists the same way.
-    warp_merge_topk(tv, ti, k, &s_v[warp * kKMax], &s_i[warp * kKMax]);
+    if (lane == 0) { s_red[warp][0] = m; s_red[warp][1] = sum; s_bad[warp] = bad; }
+    if (lane < kKMax) { s_v[warp][lane] = lv; s_i[warp][lane] = li; }
     __syncthreads();
     if (warp == 0) {
-#pragma unroll
-        for (int j = 0; j < kKMax; ++j) {
-            const bool mine = lane < kTopkThreads / 32 && j < k;
-            tv[j] = mine ? s_v[lane * kKMax + j] : -INFINITY;
-            ti[j] = mine ? s_i[lane * kKMax + j] : 0x7fffffff;
-        }
-        warp_merge_topk(tv, ti, k, s_pick_v, s_pick_i);
+        lv = -INFINITY; li = 0x7fffffff;
+        tv = -INFINITY; ti = 0x7fffffff;
+        for (int w = 0; w < kTopkThreads / 32; ++w)
+            for (int j = 0; j < k; ++j) {
+                const float cv = s_v[w][j];
+                const int ci = s_i[w][j];
+                if (ci != 0x7fffffff && topk_better(cv, ci, tv, ti)) {
+                    warp_list_insert(lv, li, cv, ci);
+                    tv = __shfl_sync(0xffffffffu, lv, k - 1);
+                    ti = __shfl_sync(0xffffffffu, li, k - 1);
+                }
+            }
+        if (lane < k) { s_pick_v[lane] = lv; s_pick_i[lane] = li; }
     }
     __syncthreads();
     if (tid == 0) {
-        MaxSum m{-INFINITY, 0.f};
+        float M = -INFINITY, S = 0.f;
         int bd = 0;
         for (int w = 0; w < kTopkThreads / 32; ++w) {
-            m = ms_combine(m, MaxSum{s_red[w][0], s_red[w][1]});
+            const float wm = s_red[w][0], ws = s_red[w][1];
             bd |= s_bad[w];
+            if (wm == -INFINITY) continue;
+            if (M == -INFINITY) { M = wm; S = ws; continue; }
+            const float nm = fmaxf(M, wm);
+            S = S * exp2f((M - nm) * kLog2e) + ws * exp2f((wm - nm) * kLog2e);
+            M = nm;
         }
         SeqState st = seq_state(state, b, k, D);
-        if (bd || m.m == -INFINITY) {
+        if (bd || M == -INFINITY) {
             st.hdr[0] = 1;
             flag_error(dev_status, EAGLE_DEV_NONFINITE);
         }
         for (int j = 0; j < k; ++j) {
             st.row_tok[s * kKMax + j] = s_pick_i[j];
-            st.row_conf[s * kKMax + j] = expf(s_pick_v[j] - m.m) / m.s;
+            st.row_conf[s * kKMax + j] = exp2f((s_pick_v[j] - M) * kLog2e) / S;
         }
     }
 }

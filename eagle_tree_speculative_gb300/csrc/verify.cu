@@ -23,8 +23,7 @@
 namespace eagle {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct VerifyArgs {
     const float* target;
@@ -34,6 +33,7 @@ struct VerifyArgs {
     const int32_t* parent;
     int B, n, V, R, D;
     float T;
+    float c;          // log2(e) / T
     uint64_t seed;
     int32_t* accept_len;
     int32_t* path;
@@ -42,37 +42,188 @@ struct VerifyArgs {
     int32_t* dev_status;
 };
 
+// Softmax statistics of a row at temperature T, kept over the raw logits:
+// lmax = max l, S = sum 2^((l - lmax) c) with c = log2(e) / T, so that
+// softmax(l / T)(x) = 2^((l_x - lmax) c) / S.  (max z = lmax / T, Z = S.)
+struct RowStat {
+    float lmax, S;
+};
+
+__device__ __forceinline__ RowStat rs_combine(RowStat a, RowStat b, float c) {
+    if (b.lmax == -INFINITY) return a;
+    if (a.lmax == -INFINITY) return b;
+    const float M = fmaxf(a.lmax, b.lmax);
+    return RowStat{M, a.S * exp2f((a.lmax - M) * c) + b.S * exp2f((b.lmax - M) * c)};
+}
+
+__device__ __forceinline__ void rs_push4(RowStat& a, float4 l, float c) {
+    const float mx = fmaxf(fmaxf(l.x, l.y), fmaxf(l.z, l.w));
+    if (mx == -INFINITY) return;
+    if (mx > a.lmax) {
+        a.S = (a.lmax == -INFINITY) ? 0.f : a.S * exp2f((a.lmax - mx) * c);
+        a.lmax = mx;
+    }
+    a.S += exp2f((l.x - a.lmax) * c) + exp2f((l.y - a.lmax) * c) + exp2f((l.z - a.lmax) * c) +
+           exp2f((l.w - a.lmax) * c);
+}
+
+__device__ __forceinline__ void rs_push1(RowStat& a, float l, float c) {
+    if (l == -INFINITY) return;
+    if (l > a.lmax) {
+        a.S = (a.lmax == -INFINITY) ? 0.f : a.S * exp2f((a.lmax - l) * c);
+        a.lmax = l;
+    }
+    a.S += exp2f((l - a.lmax) * c);
+}
+
+__device__ __forceinline__ int bad4(float4 l) {
+    return isnan(l.x) | isnan(l.y) | isnan(l.z) | isnan(l.w) | (l.x == INFINITY) |
+           (l.y == INFINITY) | (l.z == INFINITY) | (l.w == INFINITY);
+}
+
+// Probability of a token from its logit: 2^((l - lmax) c) / S, the division
+// taken as a product with the precomputed reciprocal inv = 1 / S.
+__device__ __forceinline__ float prob_of(float l, float lmax, float inv, float c) {
+    return exp2f((l - lmax) * c) * inv;
+}
+
+// Weight of token t in q_cur after j rejections at the current node:
+// r_0 = q(t); r_i = max(0, r_{i-1} - p(t)) / S_i (unchanged when S_i == 0);
+// invS[i] = 1 / S_i (0 marks S_i == 0).
+__device__ __forceinline__ float residual_at(float lq, float lp, RowStat Q, float iq, RowStat P,
+                                             float ip, float c, const float* invS, int j) {
+    float r = prob_of(lq, Q.lmax, iq, c);
+    if (j == 0) return r;
+    const float pp = prob_of(lp, P.lmax, ip, c);
+    for (int i = 1; i <= j; ++i) {
+        const float is = invS[i];
+        if (is > 0.f) r = fmaxf(0.f, r - pp) * is;
+    }
+    return r;
+}
+
 struct Slot {
     float f[4];
     int i;
     int bad;
 };
 
-// Per-CTA scratch and the cluster exchange slots.
+template <int NT>
 struct VerifySmem {
     int parent[kMaxNodes];
     int tok[kMaxNodes];
     int row[kMaxNodes];
     int nkids[kMaxNodes];
-    float S[kMaxNodes + 1];          // residual normalisers S_1..S_j of the current node
+    int lastkid[kMaxNodes];
+    float invS[kMaxNodes + 1];       // 1 / S_i of the residual normalisers at the current node
     int path[kMaxNodes + 1];
     int emit[kMaxNodes + 1];
-    float red[kWarps][4];
-    int redi[kWarps];
-    int redbad[kWarps];
+    float red[NT / 32][4];
+    int redi[NT / 32];
+    int redbad[NT / 32];
     Slot x[2];                       // double-buffered exchange slot
     int err;
 };
 
-template <int CS>
-struct Sync {
-    __device__ static void all() {
+template <int CS, int NT>
+struct Cluster {
+    using Smem = VerifySmem<NT>;
+    __device__ static void sync() {
         if constexpr (CS > 1) cg::this_cluster().sync();
         else __syncthreads();
     }
-    __device__ static const Slot* slot(VerifySmem& sm, int buf, int rank) {
+    __device__ static const Slot* slot(Smem& sm, int buf, int rank) {
         if constexpr (CS > 1) return cg::this_cluster().map_shared_rank(&sm.x[buf], rank);
         else return &sm.x[buf];
+    }
+    // Block reduction to thread 0's slot, one cluster barrier, then every thread
+    // reads all CS slots in rank order (identical results in every thread).
+    __device__ static void stats(Smem& sm, int& buf, RowStat& q, RowStat& p, int& bad, float c) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            q = rs_combine(q, RowStat{__shfl_xor_sync(~0u, q.lmax, o), __shfl_xor_sync(~0u, q.S, o)}, c);
+            p = rs_combine(p, RowStat{__shfl_xor_sync(~0u, p.lmax, o), __shfl_xor_sync(~0u, p.S, o)}, c);
+        }
+        bad = __any_sync(~0u, bad);
+        if (lane == 0) {
+            sm.red[warp][0] = q.lmax; sm.red[warp][1] = q.S;
+            sm.red[warp][2] = p.lmax; sm.red[warp][3] = p.S;
+            sm.redbad[warp] = bad;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            RowStat a{-INFINITY, 0.f}, b{-INFINITY, 0.f};
+            int bd = 0;
+            for (int w = 0; w < NT / 32; ++w) {
+                a = rs_combine(a, RowStat{sm.red[w][0], sm.red[w][1]}, c);
+                b = rs_combine(b, RowStat{sm.red[w][2], sm.red[w][3]}, c);
+                bd |= sm.redbad[w];
+            }
+            sm.x[buf].f[0] = a.lmax; sm.x[buf].f[1] = a.S;
+            sm.x[buf].f[2] = b.lmax; sm.x[buf].f[3] = b.S;
+            sm.x[buf].bad = bd;
+        }
+        sync();
+        q = RowStat{-INFINITY, 0.f};
+        p = RowStat{-INFINITY, 0.f};
+        bad = 0;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) {
+            const Slot* s = slot(sm, buf, r);
+            q = rs_combine(q, RowStat{s->f[0], s->f[1]}, c);
+            p = rs_combine(p, RowStat{s->f[2], s->f[3]}, c);
+            bad |= s->bad;
+        }
+        buf ^= 1;
+    }
+    __device__ static float sum(Smem& sm, int& buf, float v) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        v = warp_sum(v);
+        if (lane == 0) sm.red[warp][0] = v;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float t = 0.f;
+            for (int w = 0; w < NT / 32; ++w) t += sm.red[w][0];
+            sm.x[buf].f[0] = t;
+        }
+        sync();
+        float S = 0.f;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) S += slot(sm, buf, r)->f[0];
+        buf ^= 1;
+        return S;
+    }
+    __device__ static KeyIdx argmax(Smem& sm, int& buf, KeyIdx v, int& bad) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        v = warp_argmax(v);
+        bad = __any_sync(~0u, bad);
+        if (lane == 0) { sm.red[warp][0] = v.k; sm.redi[warp] = v.i; sm.redbad[warp] = bad; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            KeyIdx b{-INFINITY, 0x7fffffff};
+            int bd = 0;
+            for (int w = 0; w < NT / 32; ++w) {
+                KeyIdx c{sm.red[w][0], sm.redi[w]};
+                if (ki_better(c, b)) b = c;
+                bd |= sm.redbad[w];
+            }
+            sm.x[buf].f[0] = b.k;
+            sm.x[buf].i = b.i;
+            sm.x[buf].bad = bd;
+        }
+        sync();
+        KeyIdx b{-INFINITY, 0x7fffffff};
+        bad = 0;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) {
+            const Slot* s = slot(sm, buf, r);
+            KeyIdx c{s->f[0], s->i};
+            if (ki_better(c, b)) b = c;
+            bad |= s->bad;
+        }
+        buf ^= 1;
+        return b;
     }
 };
 
@@ -81,41 +232,54 @@ __device__ __forceinline__ int cta_rank_in_cluster(int cs) {
     return 0;
 }
 
-// ----- element-wise helpers (z = l / T, IEEE division) ---------------------
-__device__ __forceinline__ void ms_push(MaxSum& a, float z) {
-    if (z == -INFINITY) return;
-    if (z > a.m) {
-        a.s = (a.m == -INFINITY) ? 0.f : a.s * expf(a.m - z);
-        a.m = z;
+// Exponential race over the weights w_t (any positive scale): argmax_t w_t / E_t,
+// E_t = -ln u'_t.  `weight(lq, lp)` gives w_t from the two logits of token t.
+template <int NT, class Weight>
+__device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* prow, int lo, int hi,
+                                             bool vec4, uint32_t b, uint32_t k0, uint32_t k1,
+                                             Weight weight) {
+    KeyIdx best{-1.f, 0x7fffffff};
+    if (vec4) {
+        for (int t = lo + 4 * (int)threadIdx.x; t < hi; t += 4 * NT) {
+            const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
+            const float4 b4 = prow ? __ldg(reinterpret_cast<const float4*>(prow + t))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
+            const float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
+            const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float rr = weight(ax[e], bx[e]);
+                if (rr > 0.f) {
+                    const KeyIdx cand{rr / -logf(unit_open(wx[e])), t + e};
+                    if (ki_better(cand, best)) best = cand;
+                }
+            }
+        }
+    } else {
+        for (int t = lo + (int)threadIdx.x; t < hi; t += NT) {
+            const float rr = weight(qrow[t], prow ? prow[t] : 0.f);
+            if (rr > 0.f) {
+                const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
+                const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
+                const KeyIdx cand{rr / -logf(unit_open(wx[t & 3])), t};
+                if (ki_better(cand, best)) best = cand;
+            }
+        }
     }
-    a.s += expf(z - a.m);
-}
-
-__device__ __forceinline__ bool not_finite_logit(float l) { return isnan(l) || l == INFINITY; }
-
-// Residual weight of token t after j rejections at the current node:
-// r_0 = q(t); r_i = max(0, r_{i-1} - p(t)) / S_i  (unchanged when S_i == 0).
-__device__ __forceinline__ float residual_at(float lq, float lp, float T, float mq, float Zq,
-                                             float mp, float Zp, const float* S, int j) {
-    float r = expf(lq / T - mq) / Zq;
-    if (j == 0) return r;
-    float pp = expf(lp / T - mp) / Zp;
-    for (int i = 1; i <= j; ++i) {
-        float s = S[i];
-        if (s > 0.f) r = fmaxf(0.f, r - pp) / s;
-    }
-    return r;
+    return best;
 }
 
 // ---------------------------------------------------------------------------
-template <int CS>
-__global__ void __launch_bounds__(kThreads) verify_walk_kernel(VerifyArgs a) {
-    __shared__ VerifySmem sm;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+template <int CS, int NT>
+__global__ void __launch_bounds__(NT) verify_walk_kernel(VerifyArgs a) {
+    using C = Cluster<CS, NT>;
+    __shared__ VerifySmem<NT> sm;
+    const int tid = threadIdx.x;
     const int rank = cta_rank_in_cluster(CS);
     const int b = blockIdx.x / CS;
     const int n = a.n, V = a.V;
-    const float T = a.T;
+    const float c = a.c;
     const int64_t Vl = V;
 
     // ---- load and validate the tree (identically in every CTA) ----
@@ -124,22 +288,24 @@ __global__ void __launch_bounds__(kThreads) verify_walk_kernel(VerifyArgs a) {
         sm.tok[tid] = a.tokens[(int64_t)b * n + tid];
         sm.row[tid] = a.draft_row ? a.draft_row[(int64_t)b * n + tid] : tid;
         sm.nkids[tid] = 0;
+        sm.lastkid[tid] = -1;
     }
     __syncthreads();
     if (tid == 0) {
         int err = 0;
-        int depth[kMaxNodes];
+        unsigned char depth[kMaxNodes];
         if (sm.parent[0] != -1) err |= EAGLE_DEV_BAD_TREE;
         depth[0] = 0;
         for (int i = 1; i < n && !err; ++i) {
-            int p = sm.parent[i];
+            const int p = sm.parent[i];
             if (p < 0 || p >= i) { err |= EAGLE_DEV_BAD_TREE; break; }
-            depth[i] = depth[p] + 1;
+            depth[i] = (unsigned char)(depth[p] + 1);
             if (depth[i] > a.D) err |= EAGLE_DEV_DEPTH;
             if (sm.tok[i] < 0 || sm.tok[i] >= V) err |= EAGLE_DEV_BAD_TOKEN;
             sm.nkids[p] += 1;
+            sm.lastkid[p] = i;
         }
-        if (!err && T > 0.f)
+        if (!err && a.T > 0.f)
             for (int i = 0; i < n; ++i)
                 if (sm.nkids[i] && (sm.row[i] < 0 || sm.row[i] >= a.R)) err |= EAGLE_DEV_BAD_TOKEN;
         sm.err = err;
@@ -163,258 +329,181 @@ __global__ void __launch_bounds__(kThreads) verify_walk_kernel(VerifyArgs a) {
     while (!err) {
         const float* qrow = tgt_b + (int64_t)v * Vl;
         const bool kids = sm.nkids[v] > 0;
-        int moved = 0;
-        if (T > 0.f) {
+        if (a.T > 0.f) {
             const float* prow = kids ? drf_b + (int64_t)sm.row[v] * Vl : nullptr;
-            // ---------- pass: row statistics of q(v) and p(v) ----------
-            MaxSum Q{-INFINITY, 0.f}, P{-INFINITY, 0.f};
+            // ---------- pass: statistics of q(v) and p(v) ----------
+            RowStat Q{-INFINITY, 0.f}, P{-INFINITY, 0.f};
             int bad = 0;
             if (vec4) {
-#pragma unroll 2
-                for (int t = lo + 4 * tid; t < hi; t += 4 * kThreads) {
-                    float4 lq = __ldg(reinterpret_cast<const float4*>(qrow + t));
-                    float4 lp = prow ? __ldg(reinterpret_cast<const float4*>(prow + t))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                    bad |= not_finite_logit(lq.x) | not_finite_logit(lq.y) |
-                           not_finite_logit(lq.z) | not_finite_logit(lq.w);
-                    ms_push(Q, lq.x / T); ms_push(Q, lq.y / T);
-                    ms_push(Q, lq.z / T); ms_push(Q, lq.w / T);
+                int t = lo + 4 * tid;
+                for (; t + 4 * NT < hi; t += 8 * NT) {
+                    const float4 q0 = __ldg(reinterpret_cast<const float4*>(qrow + t));
+                    const float4 q1 = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * NT));
+                    float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
                     if (prow) {
-                        bad |= not_finite_logit(lp.x) | not_finite_logit(lp.y) |
-                               not_finite_logit(lp.z) | not_finite_logit(lp.w);
-                        ms_push(P, lp.x / T); ms_push(P, lp.y / T);
-                        ms_push(P, lp.z / T); ms_push(P, lp.w / T);
+                        p0 = __ldg(reinterpret_cast<const float4*>(prow + t));
+                        p1 = __ldg(reinterpret_cast<const float4*>(prow + t + 4 * NT));
+                        bad |= bad4(p0) | bad4(p1);
+                        rs_push4(P, p0, c);
+                        rs_push4(P, p1, c);
+                    }
+                    bad |= bad4(q0) | bad4(q1);
+                    rs_push4(Q, q0, c);
+                    rs_push4(Q, q1, c);
+                }
+                for (; t < hi; t += 4 * NT) {
+                    const float4 q0 = __ldg(reinterpret_cast<const float4*>(qrow + t));
+                    bad |= bad4(q0);
+                    rs_push4(Q, q0, c);
+                    if (prow) {
+                        const float4 p0 = __ldg(reinterpret_cast<const float4*>(prow + t));
+                        bad |= bad4(p0);
+                        rs_push4(P, p0, c);
                     }
                 }
             } else {
-                for (int t = lo + tid; t < hi; t += kThreads) {
-                    float lq = qrow[t];
-                    bad |= not_finite_logit(lq);
-                    ms_push(Q, lq / T);
+                for (int t = lo + tid; t < hi; t += NT) {
+                    const float lq = qrow[t];
+                    bad |= isnan(lq) | (lq == INFINITY);
+                    rs_push1(Q, lq, c);
                     if (prow) {
-                        float lp = prow[t];
-                        bad |= not_finite_logit(lp);
-                        ms_push(P, lp / T);
+                        const float lp = prow[t];
+                        bad |= isnan(lp) | (lp == INFINITY);
+                        rs_push1(P, lp, c);
                     }
                 }
             }
-            Q = warp_ms(Q);
-            P = warp_ms(P);
-            bad = __any_sync(0xffffffffu, bad);
-            if (lane == 0) {
-                sm.red[warp][0] = Q.m; sm.red[warp][1] = Q.s;
-                sm.red[warp][2] = P.m; sm.red[warp][3] = P.s;
-                sm.redbad[warp] = bad;
-            }
-            __syncthreads();
-            if (tid == 0) {
-                MaxSum q{-INFINITY, 0.f}, p{-INFINITY, 0.f};
-                int bd = 0;
-                for (int w = 0; w < kWarps; ++w) {
-                    q = ms_combine(q, MaxSum{sm.red[w][0], sm.red[w][1]});
-                    p = ms_combine(p, MaxSum{sm.red[w][2], sm.red[w][3]});
-                    bd |= sm.redbad[w];
-                }
-                sm.x[buf].f[0] = q.m; sm.x[buf].f[1] = q.s;
-                sm.x[buf].f[2] = p.m; sm.x[buf].f[3] = p.s;
-                sm.x[buf].bad = bd;
-            }
-            Sync<CS>::all();
-            MaxSum q{-INFINITY, 0.f}, p{-INFINITY, 0.f};
-            bad = 0;
-#pragma unroll
-            for (int r = 0; r < CS; ++r) {
-                const Slot* s = Sync<CS>::slot(sm, buf, r);
-                q = ms_combine(q, MaxSum{s->f[0], s->f[1]});
-                p = ms_combine(p, MaxSum{s->f[2], s->f[3]});
-                bad |= s->bad;
-            }
-            buf ^= 1;
-            if (bad || q.m == -INFINITY || (prow && p.m == -INFINITY)) {
+            C::stats(sm, buf, Q, P, bad, c);
+            if (bad || Q.lmax == -INFINITY || (prow && P.lmax == -INFINITY)) {
                 err = EAGLE_DEV_NONFINITE;
                 break;
             }
-            const float mq = q.m, Zq = q.s, mp = p.m, Zp = p.s;
             if (a.row_stats && rank == 0 && tid == 0) {
                 float* rs = a.row_stats;
-                rs[(((int64_t)0 * a.B + b) * n + v) * 2 + 0] = mq;
-                rs[(((int64_t)0 * a.B + b) * n + v) * 2 + 1] = Zq;
+                rs[(((int64_t)0 * a.B + b) * n + v) * 2 + 0] = Q.lmax / a.T;
+                rs[(((int64_t)0 * a.B + b) * n + v) * 2 + 1] = Q.S;
                 if (prow) {
-                    rs[(((int64_t)1 * a.B + b) * n + v) * 2 + 0] = mp;
-                    rs[(((int64_t)1 * a.B + b) * n + v) * 2 + 1] = Zp;
+                    rs[(((int64_t)1 * a.B + b) * n + v) * 2 + 0] = P.lmax / a.T;
+                    rs[(((int64_t)1 * a.B + b) * n + v) * 2 + 1] = P.S;
                 }
             }
+            const float iq = 1.f / Q.S, ip = prow ? 1.f / P.S : 0.f;
             // ---------- children in index order ----------
             int j = 0;
-            for (int c = v + 1; c < n && kids; ++c) {
-                if (sm.parent[c] != v) continue;
-                const int x = sm.tok[c];
+            bool moved = false, fused = false;
+            for (int ch = v + 1; ch < n && kids; ++ch) {
+                if (sm.parent[ch] != v) continue;
+                const int x = sm.tok[ch];
                 const float lq = qrow[x], lp = prow[x];
-                const float px = expf(lp / T - mp) / Zp;
-                const float r = residual_at(lq, lp, T, mq, Zq, mp, Zp, sm.S, j);
-                const float u = accept_uniform(a.seed, (uint32_t)b, (uint32_t)c);
+                const float px = prob_of(lp, P.lmax, ip, c);
+                const float r = residual_at(lq, lp, Q, iq, P, ip, c, sm.invS, j);
+                const float u = accept_uniform(a.seed, (uint32_t)b, (uint32_t)ch);
                 if (px <= 0.f || u < r / px) {
                     ++acc_n;
-                    if (tid == 0) { sm.path[acc_n] = c; sm.emit[acc_n - 1] = x; }
-                    v = c;
-                    moved = 1;
+                    if (tid == 0) { sm.path[acc_n] = ch; sm.emit[acc_n - 1] = x; }
+                    v = ch;
+                    moved = true;
+                    break;
+                }
+                if (ch == sm.lastkid[v]) {
+                    // Last child rejected: the final token is drawn from norm(max(0,
+                    // r_j - p)); its normaliser is a common factor of the race, so the
+                    // race runs directly on the unnormalised weights.
+                    fused = true;
                     break;
                 }
                 // ---------- pass: residual normaliser S_{j+1} ----------
                 float s = 0.f;
                 if (vec4) {
-#pragma unroll 2
-                    for (int t = lo + 4 * tid; t < hi; t += 4 * kThreads) {
-                        float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-                        float4 b4 = __ldg(reinterpret_cast<const float4*>(prow + t));
-                        float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
+                    for (int t = lo + 4 * tid; t < hi; t += 4 * NT) {
+                        const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
+                        const float4 b4 = __ldg(reinterpret_cast<const float4*>(prow + t));
+                        const float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float rr = residual_at(ax[e], bx[e], T, mq, Zq, mp, Zp, sm.S, j);
-                            s += fmaxf(0.f, rr - expf(bx[e] / T - mp) / Zp);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            s += fmaxf(0.f, residual_at(ax[e], bx[e], Q, iq, P, ip, c, sm.invS, j) -
+                                                prob_of(bx[e], P.lmax, ip, c));
                     }
                 } else {
-                    for (int t = lo + tid; t < hi; t += kThreads) {
-                        float rr = residual_at(qrow[t], prow[t], T, mq, Zq, mp, Zp, sm.S, j);
-                        s += fmaxf(0.f, rr - expf(prow[t] / T - mp) / Zp);
-                    }
+                    for (int t = lo + tid; t < hi; t += NT)
+                        s += fmaxf(0.f, residual_at(qrow[t], prow[t], Q, iq, P, ip, c, sm.invS, j) -
+                                            prob_of(prow[t], P.lmax, ip, c));
                 }
-                s = warp_sum(s);
-                if (lane == 0) sm.red[warp][0] = s;
-                __syncthreads();
-                if (tid == 0) {
-                    float t = 0.f;
-                    for (int w = 0; w < kWarps; ++w) t += sm.red[w][0];
-                    sm.x[buf].f[0] = t;
-                }
-                Sync<CS>::all();
-                float S = 0.f;
-#pragma unroll
-                for (int r2 = 0; r2 < CS; ++r2) S += Sync<CS>::slot(sm, buf, r2)->f[0];
-                buf ^= 1;
+                const float S = C::sum(sm, buf, s);
                 ++j;
-                if (tid == 0) sm.S[j] = S;
+                if (tid == 0) sm.invS[j] = S > 0.f ? 1.f / S : 0.f;
                 __syncthreads();
             }
             if (moved) continue;
-            // ---------- pass: exponential race over q_cur ----------
-            KeyIdx best{-1.f, 0x7fffffff};
-            if (vec4) {
-                for (int t = lo + 4 * tid; t < hi; t += 4 * kThreads) {
-                    float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-                    float4 b4 = prow ? __ldg(reinterpret_cast<const float4*>(prow + t))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                    uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, (uint32_t)b, kTagRace),
-                                            k0, k1);
-                    float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
-                    uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float rr = residual_at(ax[e], bx[e], T, mq, Zq, mp, Zp, sm.S, j);
-                        if (rr > 0.f) {
-                            float key = rr / -logf(unit_open(wx[e]));
-                            KeyIdx cand{key, t + e};
-                            if (ki_better(cand, best)) best = cand;
-                        }
-                    }
+            // ---------- pass: exponential race for the final token ----------
+            int bad2 = 0;
+            KeyIdx best;
+            if (fused) {
+                const int jj = j;
+                best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
+                                      [&](float lq2, float lp2) {
+                                          return fmaxf(0.f, residual_at(lq2, lp2, Q, iq, P, ip, c,
+                                                                        sm.invS, jj) -
+                                                                prob_of(lp2, P.lmax, ip, c));
+                                      });
+                best = C::argmax(sm, buf, best, bad2);
+                if (best.i == 0x7fffffff) {
+                    // the clamped residual is all zero: keep q_cur (= r_j)
+                    best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
+                                          [&](float lq2, float lp2) {
+                                              return residual_at(lq2, lp2, Q, iq, P, ip, c, sm.invS, jj);
+                                          });
+                    best = C::argmax(sm, buf, best, bad2);
                 }
             } else {
-                for (int t = lo + tid; t < hi; t += kThreads) {
-                    float rr = residual_at(qrow[t], prow ? prow[t] : 0.f, T, mq, Zq, mp, Zp, sm.S, j);
-                    if (rr > 0.f) {
-                        uint4 w = philox4x32_10(
-                            make_uint4((uint32_t)t >> 2, 0u, (uint32_t)b, kTagRace), k0, k1);
-                        uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-                        float key = rr / -logf(unit_open(wx[t & 3]));
-                        KeyIdx cand{key, t};
-                        if (ki_better(cand, best)) best = cand;
-                    }
-                }
+                const int jj = j;
+                best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
+                                      [&](float lq2, float lp2) {
+                                          return residual_at(lq2, lp2, Q, iq, P, ip, c, sm.invS, jj);
+                                      });
+                best = C::argmax(sm, buf, best, bad2);
             }
-            best = warp_argmax(best);
-            if (lane == 0) { sm.red[warp][0] = best.k; sm.redi[warp] = best.i; }
-            __syncthreads();
-            if (tid == 0) {
-                KeyIdx bb{-1.f, 0x7fffffff};
-                for (int w = 0; w < kWarps; ++w) {
-                    KeyIdx c{sm.red[w][0], sm.redi[w]};
-                    if (ki_better(c, bb)) bb = c;
-                }
-                sm.x[buf].f[0] = bb.k;
-                sm.x[buf].i = bb.i;
+            if (best.i == 0x7fffffff) {
+                err = EAGLE_DEV_NONFINITE;
+                break;
             }
-            Sync<CS>::all();
-            KeyIdx bb{-1.f, 0x7fffffff};
-#pragma unroll
-            for (int r2 = 0; r2 < CS; ++r2) {
-                const Slot* s = Sync<CS>::slot(sm, buf, r2);
-                KeyIdx c{s->f[0], s->i};
-                if (ki_better(c, bb)) bb = c;
-            }
-            buf ^= 1;
-            y = bb.i;
+            y = best.i;
         } else {
             // ---------- greedy: argmax of the target row ----------
             KeyIdx best{-INFINITY, 0x7fffffff};
             int bad = 0;
             if (vec4) {
-                for (int t = lo + 4 * tid; t < hi; t += 4 * kThreads) {
-                    float4 l4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-                    float lx[4] = {l4.x, l4.y, l4.z, l4.w};
+                for (int t = lo + 4 * tid; t < hi; t += 4 * NT) {
+                    const float4 l4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
+                    bad |= bad4(l4);
+                    const float lx[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        bad |= not_finite_logit(lx[e]);
-                        KeyIdx c{lx[e], t + e};
-                        if (ki_better(c, best)) best = c;
+                        const KeyIdx cand{lx[e], t + e};
+                        if (ki_better(cand, best)) best = cand;
                     }
                 }
             } else {
-                for (int t = lo + tid; t < hi; t += kThreads) {
-                    float l = qrow[t];
-                    bad |= not_finite_logit(l);
-                    KeyIdx c{l, t};
-                    if (ki_better(c, best)) best = c;
+                for (int t = lo + tid; t < hi; t += NT) {
+                    const float l = qrow[t];
+                    bad |= isnan(l) | (l == INFINITY);
+                    const KeyIdx cand{l, t};
+                    if (ki_better(cand, best)) best = cand;
                 }
             }
-            best = warp_argmax(best);
-            bad = __any_sync(0xffffffffu, bad);
-            if (lane == 0) { sm.red[warp][0] = best.k; sm.redi[warp] = best.i; sm.redbad[warp] = bad; }
-            __syncthreads();
-            if (tid == 0) {
-                KeyIdx bb{-INFINITY, 0x7fffffff};
-                int bd = 0;
-                for (int w = 0; w < kWarps; ++w) {
-                    KeyIdx c{sm.red[w][0], sm.redi[w]};
-                    if (ki_better(c, bb)) bb = c;
-                    bd |= sm.redbad[w];
-                }
-                sm.x[buf].f[0] = bb.k;
-                sm.x[buf].i = bb.i;
-                sm.x[buf].bad = bd;
-            }
-            Sync<CS>::all();
-            KeyIdx bb{-INFINITY, 0x7fffffff};
-            int bd = 0;
-#pragma unroll
-            for (int r2 = 0; r2 < CS; ++r2) {
-                const Slot* s = Sync<CS>::slot(sm, buf, r2);
-                KeyIdx c{s->f[0], s->i};
-                if (ki_better(c, bb)) bb = c;
-                bd |= s->bad;
-            }
-            buf ^= 1;
-            if (bd || bb.k == -INFINITY) {
+            best = C::argmax(sm, buf, best, bad);
+            if (bad || best.k == -INFINITY) {
                 err = EAGLE_DEV_NONFINITE;
                 break;
             }
-            const int g = bb.i;
-            for (int c = v + 1; c < n && kids; ++c) {
-                if (sm.parent[c] == v && sm.tok[c] == g) {
+            const int g = best.i;
+            bool moved = false;
+            for (int ch = v + 1; ch < n && kids; ++ch) {
+                if (sm.parent[ch] == v && sm.tok[ch] == g) {
                     ++acc_n;
-                    if (tid == 0) { sm.path[acc_n] = c; sm.emit[acc_n - 1] = g; }
-                    v = c;
-                    moved = 1;
+                    if (tid == 0) { sm.path[acc_n] = ch; sm.emit[acc_n - 1] = g; }
+                    v = ch;
+                    moved = true;
                     break;
                 }
             }
@@ -430,7 +519,7 @@ __global__ void __launch_bounds__(kThreads) verify_walk_kernel(VerifyArgs a) {
         const int Dp1 = a.D + 1;
         int32_t* P = a.path + (int64_t)b * Dp1;
         int32_t* E = a.emit + (int64_t)b * Dp1;
-        for (int t = tid; t < Dp1; t += kThreads) {
+        for (int t = tid; t < Dp1; t += NT) {
             if (err) {
                 P[t] = -1;
                 E[t] = -1;
@@ -445,77 +534,93 @@ __global__ void __launch_bounds__(kThreads) verify_walk_kernel(VerifyArgs a) {
         }
     }
     // No CTA may leave while a peer can still read its exchange slots.
-    Sync<CS>::all();
+    C::sync();
 }
 
 // ---------------------------------------------------------------------------
-// Standalone row statistics: one CTA per row (grid-stride).
+// Standalone row statistics: one CTA per row (grid-stride), loads hoisted four
+// float4 deep; (max, sum) in the exp2 domain; argmax only when asked.
 // ---------------------------------------------------------------------------
 constexpr int kStatThreads = 256;
 
+template <bool STATS, bool ARGMAX>
 __global__ void __launch_bounds__(kStatThreads)
-softmax_stats_kernel(const float* __restrict__ logits, int64_t rows, int V, float T,
+softmax_stats_kernel(const float* __restrict__ logits, int64_t rows, int V, float T, float c,
                      float* row_max, float* row_sum, int32_t* row_argmax, int32_t* dev_status) {
-    __shared__ float red_f[kStatThreads / 32][2];
+    __shared__ float red_f[kStatThreads / 32][3];
     __shared__ int red_i[kStatThreads / 32];
     __shared__ int red_bad[kStatThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool vec4 = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const float* row = logits + r * (int64_t)V;
-        MaxSum ms{-INFINITY, 0.f};
+        RowStat st{-INFINITY, 0.f};
         KeyIdx best{-INFINITY, 0x7fffffff};
         int bad = 0;
-        if (vec4) {
-#pragma unroll 4
-            for (int t = 4 * tid; t < V; t += 4 * kStatThreads) {
-                float4 l4 = __ldg(reinterpret_cast<const float4*>(row + t));
-                float lx[4] = {l4.x, l4.y, l4.z, l4.w};
+        auto take4 = [&](float4 l4, int t) {
+            bad |= bad4(l4);
+            if (STATS) rs_push4(st, l4, c);
+            if (ARGMAX) {
+                const float lx[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    bad |= not_finite_logit(lx[e]);
-                    KeyIdx c{lx[e], t + e};
-                    if (ki_better(c, best)) best = c;
-                    if (T > 0.f) ms_push(ms, lx[e] / T);
+                    const KeyIdx cand{lx[e], t + e};
+                    if (ki_better(cand, best)) best = cand;
                 }
             }
+        };
+        if (vec4) {
+            const float4* r4 = reinterpret_cast<const float4*>(row);
+            const int n4 = V >> 2;
+            int t = tid;
+            for (; t + 3 * kStatThreads < n4; t += 4 * kStatThreads) {
+                const float4 a0 = __ldg(r4 + t), a1 = __ldg(r4 + t + kStatThreads);
+                const float4 a2 = __ldg(r4 + t + 2 * kStatThreads), a3 = __ldg(r4 + t + 3 * kStatThreads);
+                take4(a0, 4 * t);
+                take4(a1, 4 * (t + kStatThreads));
+                take4(a2, 4 * (t + 2 * kStatThreads));
+                take4(a3, 4 * (t + 3 * kStatThreads));
+            }
+            for (; t < n4; t += kStatThreads) take4(__ldg(r4 + t), 4 * t);
         } else {
             for (int t = tid; t < V; t += kStatThreads) {
-                float l = row[t];
-                bad |= not_finite_logit(l);
-                KeyIdx c{l, t};
-                if (ki_better(c, best)) best = c;
-                if (T > 0.f) ms_push(ms, l / T);
+                const float l = row[t];
+                bad |= isnan(l) | (l == INFINITY);
+                if (STATS) rs_push1(st, l, c);
+                if (ARGMAX) {
+                    const KeyIdx cand{l, t};
+                    if (ki_better(cand, best)) best = cand;
+                }
             }
         }
-        ms = warp_ms(ms);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            st = rs_combine(st, RowStat{__shfl_xor_sync(~0u, st.lmax, o), __shfl_xor_sync(~0u, st.S, o)}, c);
         best = warp_argmax(best);
         bad = __any_sync(0xffffffffu, bad);
         if (lane == 0) {
-            red_f[warp][0] = ms.m; red_f[warp][1] = ms.s;
+            red_f[warp][0] = st.lmax; red_f[warp][1] = st.S; red_f[warp][2] = best.k;
             red_i[warp] = best.i;
             red_bad[warp] = bad;
-            // keep the argmax key next to its index
         }
-        __shared__ float red_k[kStatThreads / 32];
-        if (lane == 0) red_k[warp] = best.k;
         __syncthreads();
         if (tid == 0) {
-            MaxSum m{-INFINITY, 0.f};
+            RowStat m{-INFINITY, 0.f};
             KeyIdx bb{-INFINITY, 0x7fffffff};
             int bd = 0;
             for (int w = 0; w < kStatThreads / 32; ++w) {
-                m = ms_combine(m, MaxSum{red_f[w][0], red_f[w][1]});
-                KeyIdx c{red_k[w], red_i[w]};
-                if (ki_better(c, bb)) bb = c;
+                m = rs_combine(m, RowStat{red_f[w][0], red_f[w][1]}, c);
+                const KeyIdx cand{red_f[w][2], red_i[w]};
+                if (ki_better(cand, bb)) bb = cand;
                 bd |= red_bad[w];
             }
-            if (bd || bb.k == -INFINITY) flag_error(dev_status, EAGLE_DEV_NONFINITE);
-            if (T > 0.f) {
-                if (row_max) row_max[r] = m.m;
-                if (row_sum) row_sum[r] = m.s;
+            if (bd || (STATS && m.lmax == -INFINITY) || (ARGMAX && bb.k == -INFINITY))
+                flag_error(dev_status, EAGLE_DEV_NONFINITE);
+            if (STATS) {
+                row_max[r] = m.lmax / T;
+                row_sum[r] = m.S;
             }
-            if (row_argmax) row_argmax[r] = bb.i;
+            if (ARGMAX) row_argmax[r] = bb.i;
         }
         __syncthreads();
     }
@@ -531,9 +636,11 @@ int verify_cluster_size(int B) {
     if (forced > 0) return forced;
     const int sms = device_sm_count();
     int cs = 8;
-    while (cs > 1 && (int64_t)B * cs > 2LL * sms) cs >>= 1;
+    while (cs > 1 && (int64_t)B * cs > 4LL * sms) cs >>= 1;
     return cs;
 }
+
+constexpr int kVerifyThreads = 256;
 
 }  // namespace
 }  // namespace eagle
@@ -557,15 +664,17 @@ extern "C" eagle_status eagle_verify_accept(const float* target_logits, const fl
         if (!draft_row && R != n) return EAGLE_ERR_SHAPE;
     }
     if (B == 0) return EAGLE_OK;
+    const float c = temperature > 0.f ? kLog2e / temperature : 0.f;
     VerifyArgs a{target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, max_depth,
-                 temperature, seed, accept_len, path, emit, row_stats, dev_status};
+                 temperature, c, seed, accept_len, path, emit, row_stats, dev_status};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    constexpr int NT = kVerifyThreads;
     cudaError_t e;
     switch (verify_cluster_size(B)) {
-        case 8: e = launch_clustered(verify_walk_kernel<8>, B, 8, kThreads, 0, s, a); break;
-        case 4: e = launch_clustered(verify_walk_kernel<4>, B, 4, kThreads, 0, s, a); break;
-        case 2: e = launch_clustered(verify_walk_kernel<2>, B, 2, kThreads, 0, s, a); break;
-        default: e = launch_clustered(verify_walk_kernel<1>, B, 1, kThreads, 0, s, a); break;
+        case 8: e = launch_clustered(verify_walk_kernel<8, NT>, B, 8, NT, 0, s, a); break;
+        case 4: e = launch_clustered(verify_walk_kernel<4, NT>, B, 4, NT, 0, s, a); break;
+        case 2: e = launch_clustered(verify_walk_kernel<2, NT>, B, 2, NT, 0, s, a); break;
+        default: e = launch_clustered(verify_walk_kernel<1, NT>, B, 1, NT, 0, s, a); break;
     }
     return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
@@ -576,13 +685,23 @@ extern "C" eagle_status eagle_softmax_stats(const float* logits, int64_t rows, i
                                             eagle_stream_t stream) {
     if (!logits || rows < 0 || V < 1) return EAGLE_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
-    if (temperature > 0.f && (!row_max || !row_sum)) return EAGLE_ERR_INVALID_ARG;
-    if (temperature == 0.f && !row_argmax) return EAGLE_ERR_INVALID_ARG;
+    const bool stats = temperature > 0.f;
+    if (stats && (!row_max || !row_sum)) return EAGLE_ERR_INVALID_ARG;
+    if (!stats && !row_argmax) return EAGLE_ERR_INVALID_ARG;
     if (rows == 0) return EAGLE_OK;
     const int64_t cap = (int64_t)device_sm_count() * 8;
     const int grid = (int)(rows < cap ? rows : cap);
-    softmax_stats_kernel<<<grid, kStatThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        logits, rows, V, temperature, row_max, row_sum, row_argmax, dev_status);
+    const float c = stats ? kLog2e / temperature : 0.f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (stats && row_argmax)
+        softmax_stats_kernel<true, true><<<grid, kStatThreads, 0, s>>>(
+            logits, rows, V, temperature, c, row_max, row_sum, row_argmax, dev_status);
+    else if (stats)
+        softmax_stats_kernel<true, false><<<grid, kStatThreads, 0, s>>>(
+            logits, rows, V, temperature, c, row_max, row_sum, row_argmax, dev_status);
+    else
+        softmax_stats_kernel<false, true><<<grid, kStatThreads, 0, s>>>(
+            logits, rows, V, temperature, c, row_max, row_sum, row_argmax, dev_status);
     EAGLE_CHECK_LAUNCH();
     return EAGLE_OK;
 }

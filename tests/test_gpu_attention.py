@@ -87,8 +87,8 @@ def test_llama70b_shape_sweep_points(B, L):
 
 def test_capacity_and_tree_errors_set_status_and_zero_output():
     import eagle_tree_speculative_gb300 as E
-    q, k, v, kv_len = W.attn_inputs(2, 4, 2, 1, 128, [10, 3], 14, seed=8)
+    q, k, v, kv_len = W.attn_inputs(2, 4, 2, 1, 128, [10, 3], 13, seed=8)
     parent = np.array([[-1, 0, 1, 2], [-1, 2, 0, 1]], np.int32)     # second tree invalid
     got, st = _run(q, k, v, kv_len, parent, 0.1)
-    assert st & E.EAGLE_DEV_CAPACITY and st & E.EAGLE_DEV_BAD_TREE   # 10 + 4 > 14 in seq 0
+    assert st & E.EAGLE_DEV_CAPACITY and st & E.EAGLE_DEV_BAD_TREE   # 10 + 4 > 13 in seq 0
     assert np.all(got == 0)

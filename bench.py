@@ -139,6 +139,8 @@ class Step:
         # each expanded node plus N(0, sigma^2) noise, a fresh N(0, s^2) row for leaves
         self.expand()
         torch.cuda.synchronize()
+        self.gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                        for _ in range(D)]
         s = float(c.w_std * np.sqrt(H))
         rows = self.draft_row.long()
         self.target = torch.empty(B, n, V, device=dev)
@@ -149,26 +151,31 @@ class Step:
             self.target[b] = torch.where(has[:, None], self.logits[b, r.clamp(min=0)] + noise,
                                          torch.randn(n, V, device=dev, generator=g) * s)
         torch.cuda.synchronize()
-        self.gemm_events = []
+        self.gemm_ms = 0.0          # accumulated in-kernel GEMM time of timed steps
+        self.gemm_rows = 0
 
     def expand(self, time_gemm=False):
-        E, torch = self.E, self.torch
+        E = self.E
         for lvl in range(1, self.D + 1):
             k_in = 1 if lvl == 1 else self.k
             off = 0 if lvl == 1 else 1 + (lvl - 2) * self.k
             if time_gemm:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record()
+                self.gemm_ev[lvl - 1][0].record()
             E.eagle_lmhead_gemm(self.hidden[lvl - 1].view(self.B * k_in, self.H), self.w,
                                 out=self.logits, ldo=self.V, rows_per_group=k_in,
                                 group_stride=self.R, row_offset=off, dev_status=self.status)
             if time_gemm:
-                e1.record()
-                self.gemm_events.append((e0, e1, self.B * k_in))
+                self.gemm_ev[lvl - 1][1].record()
             E.eagle2_expand(lvl, lvl == self.D, self.logits, self.k, self.D, self.n, self.state,
                             out_tokens=self.tokens, out_parent=self.parent,
                             out_draft_row=self.draft_row, dev_status=self.status)
+
+    def collect_gemm_times(self):
+        """Add the GEMM launch times recorded by the last time_gemm step (events are reused)."""
+        for lvl in range(1, self.D + 1):
+            e0, e1 = self.gemm_ev[lvl - 1]
+            self.gemm_ms += e0.elapsed_time(e1)
+            self.gemm_rows += self.B * (1 if lvl == 1 else self.k)
 
     def run(self, seed, time_gemm=False):
         E = self.E
@@ -215,28 +222,47 @@ def run_ours(args, rank, world, dist):
     if int(st.status.item()) != 0:
         raise RuntimeError(f"device status {int(st.status.item())} during warm-up")
 
-    # -------- device-resident timed region --------
+    # -------- device-resident timed region: the captured step, replayed --------
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            st.run(77)
+        graph.replay()
+        torch.cuda.synchronize()
+    except Exception as exc:  # capture unsupported: time the eager calls instead
+        graph = None
+        print(f"graph capture failed ({exc}); timing eager launches", file=sys.stderr)
     if dist:
         dist.barrier()
     clocks = ClockSampler(local)
     clocks.start()
-    accepted = torch.zeros((), dtype=torch.int64, device=dev)
-
-    def body(i):
-        st.run(i, time_gemm=True)
-        accepted.add_(st.accept_len.sum() + st.B)
-
-    ms = time_region(body, args.steps, torch)
+    if graph is not None:
+        ms = time_region(lambda i: graph.replay(), args.steps, torch)
+    else:
+        ms = time_region(lambda i: st.run(i), args.steps, torch)
     clk = clocks.stop()
     if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     ms_per_step = ms / args.steps
-    tok_per_step = float(accepted.item()) / args.steps
-    # dominant kernel: the LM-head GEMM, timed per launch inside the region
-    gemm_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in st.gemm_events)
-    gemm_rows = sum(m for _, _, m in st.gemm_events)
+    acc_graph = float(st.accept_len.sum().item() + st.B)   # the replayed step's accepted tokens
+
+    # -------- eager timed region: per-launch GEMM times (CUDA events on the stream) --------
+    accepted = torch.zeros((), dtype=torch.int64, device=dev)
+    eager_steps = max(10, min(args.steps, 50))
+    torch.cuda.synchronize()
+    t_eager = 0.0
+    for i in range(eager_steps):
+        e0 = time.perf_counter()
+        st.run(i, time_gemm=True)
+        accepted.add_(st.accept_len.sum() + st.B)
+        torch.cuda.synchronize()
+        t_eager += time.perf_counter() - e0
+        st.collect_gemm_times()
+    tok_per_step = float(accepted.item()) / eager_steps
+    gemm_ms, gemm_rows = st.gemm_ms, st.gemm_rows
     gemm_flops = 2.0 * gemm_rows * st.H * st.V
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
@@ -245,7 +271,7 @@ def run_ours(args, rank, world, dist):
     br = breakdown(st, torch)
 
     # -------- end to end through the public API with host buffers --------
-    e2e = run_e2e(st, torch, max(5, min(args.steps, 20)))
+    e2e = run_e2e(st, torch, max(5, min(args.steps, 20)), graph)
     if int(st.status.item()) != 0:
         raise RuntimeError(f"device status {int(st.status.item())}")
 
@@ -257,6 +283,8 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4),
+        "timing": "CUDA graph of one step replayed" if graph is not None else "eager launches",
+        "eager_ms_per_step_wall": round(1e3 * t_eager / eager_steps, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -273,15 +301,18 @@ def run_ours(args, rank, world, dist):
                    "parallelism": f"replicas x{world} (sequence-sharded, no collective)"},
         "accepted_tokens_per_s": round(world * tok_per_step * 1000.0 / ms_per_step, 1),
         "mean_accept_len_plus_1": round(tok_per_step / st.B, 4),
+        "graph_step_accepted_tokens": acc_graph,
         "roofline": {"kernel": "lmhead_gemm_kernel (tcgen05)", "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peak, 4), "traffic": None,
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained",
-                     "flops_per_step": gemm_flops / args.steps,
-                     "ms_per_step_in_kernel": round(gemm_ms / args.steps, 4)},
+                     "flops_per_step": gemm_flops / eager_steps,
+                     "ms_per_step_in_kernel": round(gemm_ms / eager_steps, 4),
+                     "timed": f"{eager_steps} eager steps, events around each launch"},
         "breakdown_ms": br,
         "e2e": e2e,
         "gpu_launches": st.launches_per_step() * args.steps,
+        "gpu_launches_note": "library kernels per step x timed steps",
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -325,9 +356,11 @@ def breakdown(st, torch, reps=20):
     return res
 
 
-def run_e2e(st, torch, steps):
-    """The same step through the public API with the step's inputs in pinned host memory:
-    H2D of the hidden states, queries and target logits, D2H of the emitted tokens."""
+def run_e2e(st, torch, steps, graph=None):
+    """The same step with the step's inputs in pinned host memory: H2D of the hidden
+    states, queries and target logits into the step's device buffers, the step (the
+    captured graph of library calls when available, else the eager calls), D2H of the
+    emitted tokens."""
     host_hidden = [h.cpu().pin_memory() for h in st.hidden]
     host_target = st.target.cpu().pin_memory()
     host_q = st.q.cpu().pin_memory()
@@ -342,7 +375,10 @@ def run_e2e(st, torch, steps):
             dst.copy_(src, non_blocking=True)
         st.target.copy_(host_target, non_blocking=True)
         st.q.copy_(host_q, non_blocking=True)
-        st.run(5000 + i)
+        if graph is not None:
+            graph.replay()
+        else:
+            st.run(5000 + i)
         out_acc.copy_(st.accept_len, non_blocking=True)
         out_emit.copy_(st.emit, non_blocking=True)
 

@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace eagle {
 namespace {
@@ -35,13 +36,9 @@ constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr uint32_t TMEM_COLS = 2 * BN;          // two fp32 accumulators
 constexpr int kThreads = 192;
-constexpr long long kTimeoutCycles = 4000000000LL;
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
-// B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at 17-22,
-// M >> 4 at 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor: M = 128, N = 256, bf16 A and B both K-major, fp32 D.
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN, 0, 0);
 
 struct GemmArgs {
     float* out;
@@ -51,100 +48,6 @@ struct GemmArgs {
     int64_t group_stride, row_offset;
     int32_t* dev_status;
 };
-
-__device__ __forceinline__ uint32_t s32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// ---------------- mbarrier ----------------
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok;
-}
-// Bounded wait.  Returns false when the shared abort flag is up or the wait
-// exceeded the limit (which raises the flag).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          bool honour_abort = true) {
-    const long long t0 = clock64();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 127u) == 127u) {
-            if (honour_abort && *abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// ---------------- TMA ----------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-        "%4}], [%2];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-// ---------------- tcgen05 ----------------
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, K-major, 128-byte swizzle: start address
-// >> 4 (bits 0-13), leading offset 16 B (unused for this layout, bits 16-29),
-// stride between 8-row groups 1024 B (bits 32-45), descriptor version 1
-// (bits 46-47), layout SWIZZLE_128B = 2 (bits 61-63).  Stepping K by 16 bf16
-// inside the 128-byte row adds 32 bytes to the start address.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -183,11 +86,7 @@ lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                         s32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+        tmem_alloc(s32(tmem_slot), TMEM_COLS);
     }
     tc_fence_before();
     __syncthreads();
@@ -228,7 +127,7 @@ lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const uint32_t a0 = s32(sA + stage * A_BYTES), b0 = s32(sB + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        umma_bf16(d, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32),
+                        umma_f16(d, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), kIdesc,
                                   (kb | k) != 0 ? 1u : 0u);
                     umma_commit(s32(&empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -288,9 +187,7 @@ lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     if (threadIdx.x == 0 && *abort_flag) flag_error(g.dev_status, EAGLE_DEV_TIMEOUT);
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

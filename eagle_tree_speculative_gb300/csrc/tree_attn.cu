@@ -15,9 +15,13 @@
 // ldmatrix is conflict-free); QK^T and PV run on bf16 mma.sync with fp32
 // accumulators and an online softmax in registers.  Committed keys may be
 // split across CTAs (split-KV) and merged by a log-sum-exp combine kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdlib>
 
 #include "common.cuh"
+#include "tree_attn_tc.cuh"
 
 namespace eagle {
 namespace {
@@ -339,6 +343,56 @@ int attn_splits(int B, int n, int Hq, int Hkv, int Lmax) {
     return splits < 1 ? 1 : splits;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// K or V cache viewed as a 2-D [B * Hkv * Lmax, 128] bf16 matrix; 64 x 64 boxes.
+bool kv_map(CUtensorMap* map, const void* base, int64_t rows) {
+    auto fn = attn_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)attn_tc::TBN};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool use_mma_sync_kernel() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("EAGLE_ATTN_MMA_SYNC");
+        v = (e && e[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+int tc_row_groups(int n, int G) { return (n * G + attn_tc::ROWS_PER_CTA - 1) / attn_tc::ROWS_PER_CTA; }
+
+int tc_splits(int B, int n, int Hq, int Hkv, int Lmax) {
+    const int G = Hq / Hkv;
+    const int64_t ctas = (int64_t)B * Hkv * tc_row_groups(n, G);
+    const int sms = device_sm_count();
+    int splits = (int)((2 * sms + ctas - 1) / ctas);
+    const int max_by_len = (Lmax - n) / (4 * attn_tc::TBN);
+    splits = splits < max_by_len ? splits : max_by_len;
+    splits = splits < kMaxSplits ? splits : kMaxSplits;
+    return splits < 1 ? 1 : splits;
+}
+
 }  // namespace
 }  // namespace eagle
 
@@ -347,7 +401,8 @@ using namespace eagle;
 extern "C" size_t eagle_tree_attn_workspace_size(int B, int n, int Hq, int Hkv, int head_dim,
                                                  int Lmax) {
     if (B < 1 || n < 1 || Hkv < 1 || Hq % Hkv != 0 || head_dim != kHeadDim || Lmax < n) return 0;
-    const int splits = attn_splits(B, n, Hq, Hkv, Lmax);
+    const int s1 = attn_splits(B, n, Hq, Hkv, Lmax), s2 = tc_splits(B, n, Hq, Hkv, Lmax);
+    const int splits = s1 > s2 ? s1 : s2;
     if (splits == 1) return 0;
     return (size_t)splits * B * n * Hq * (kHeadDim + 2) * sizeof(float);
 }
@@ -363,12 +418,11 @@ extern "C" eagle_status eagle_tree_attn(const void* q, const void* k_cache, cons
     for (const void* p : {q, k_cache, v_cache, (const void*)out})
         if (reinterpret_cast<uintptr_t>(p) & 15) return EAGLE_ERR_INVALID_ARG;
     if (B == 0) return EAGLE_OK;
-    const int splits = attn_splits(B, n, Hq, Hkv, Lmax);
-    const size_t need = eagle_tree_attn_workspace_size(B, n, Hq, Hkv, head_dim, Lmax);
+    const bool v1 = use_mma_sync_kernel();
+    const int splits = v1 ? attn_splits(B, n, Hq, Hkv, Lmax) : tc_splits(B, n, Hq, Hkv, Lmax);
+    const size_t need = splits > 1 ? (size_t)splits * B * n * Hq * (kHeadDim + 2) * sizeof(float) : 0;
     if (need > 0 && (!workspace || ws_bytes < need)) return EAGLE_ERR_CAPACITY;
     const int G = Hq / Hkv;
-    const int nw = attn_warps(n, G);
-    const int rb = (n * G + 16 * nw - 1) / (16 * nw);
     AttnArgs a;
     a.q = static_cast<const uint16_t*>(q);
     a.k = static_cast<const uint16_t*>(k_cache);
@@ -383,16 +437,35 @@ extern "C" eagle_status eagle_tree_attn(const void* q, const void* k_cache, cons
     a.scale_log2 = scale * 1.4426950408889634f;
     a.dev_status = dev_status;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t smem = 2 * 2 * kTileBytes;
-    dim3 grid((unsigned)rb, (unsigned)(Hkv * splits), (unsigned)B);
-    if (nw == 8) {
-        if (cudaFuncSetAttribute(tree_attn_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (!v1) {
+        CUtensorMap mk, mv;
+        const int64_t kv_rows = (int64_t)B * Hkv * Lmax;
+        if (kv_rows > 0x7fffffffLL) return EAGLE_ERR_SHAPE;
+        if (!kv_map(&mk, k_cache, kv_rows) || !kv_map(&mv, v_cache, kv_rows)) return EAGLE_ERR_CUDA;
+        attn_tc::Args t;
+        t.q = a.q; t.out = a.out; t.ws_o = a.ws_o; t.ws_ml = a.ws_ml; t.kv_len = kv_len;
+        t.parent = parent; t.B = B; t.n = n; t.Hq = Hq; t.Hkv = Hkv; t.G = G; t.Lmax = Lmax;
+        t.splits = splits; t.scale_log2 = a.scale_log2; t.dev_status = dev_status;
+        if (cudaFuncSetAttribute(attn_tc::tree_attn_tc_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn_tc::SMEM_BYTES) != cudaSuccess)
             return EAGLE_ERR_CUDA;
-        tree_attn_kernel<8><<<grid, 256, smem, s>>>(a);
+        dim3 grid((unsigned)tc_row_groups(n, G), (unsigned)(Hkv * splits), (unsigned)B);
+        attn_tc::tree_attn_tc_kernel<<<grid, attn_tc::kThreads, attn_tc::SMEM_BYTES, s>>>(mk, mv, t);
     } else {
-        if (cudaFuncSetAttribute(tree_attn_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return EAGLE_ERR_CUDA;
-        tree_attn_kernel<4><<<grid, 128, smem, s>>>(a);
+        const int nw = attn_warps(n, G);
+        const int rb = (n * G + 16 * nw - 1) / (16 * nw);
+        const size_t smem = 2 * 2 * kTileBytes;
+        dim3 grid((unsigned)rb, (unsigned)(Hkv * splits), (unsigned)B);
+        if (nw == 8) {
+            if (cudaFuncSetAttribute(tree_attn_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return EAGLE_ERR_CUDA;
+            tree_attn_kernel<8><<<grid, 256, smem, s>>>(a);
+        } else {
+            if (cudaFuncSetAttribute(tree_attn_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+                return EAGLE_ERR_CUDA;
+            tree_attn_kernel<4><<<grid, 128, smem, s>>>(a);
+        }
     }
     EAGLE_CHECK_LAUNCH();
     if (splits > 1) {

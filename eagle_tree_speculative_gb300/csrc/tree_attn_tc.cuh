@@ -1,0 +1,459 @@
+// Tree attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Method: see tree_attn.cu (node i attends to the committed rows 0..L_b-1 and
+// to the tree rows L_b + j for j = i or an ancestor of i).
+//
+// One CTA owns 128 query rows (one M-tile) of one (sequence, kv head, KV split):
+// the Hq/Hkv query heads that share the kv head are packed as rows (row r =
+// node r / G, head kvh * G + r % G); larger groups take several CTAs, adjacent
+// in the grid so they share each K/V tile through L2.  Keys come in tiles of
+// 128: the QK^T MMA is then N = 128 wide, which balances its shared-memory
+// operand traffic (A and B 4 KB each per K-step) against tensor time.  Roles:
+//   warps 0, 2  lane 0 of warp 0 streams 128-key K tiles and lane 0 of warp 2
+//               V tiles by TMA, each into its own 3-stage ring, starting at once,
+//               and asks L2 for tiles further on so each shared-memory load waits
+//               on L2 rather than DRAM;
+//   warps 1-7   first stage Q in shared memory (128B-swizzled, K-major);
+//   warp 1      owns TMEM (S: two 128-column fp32 buffers; P: two 64-column
+//               bf16-pair buffers; O: 128 columns = all 512) and one thread
+//               issues the MMAs: S = Q K^T (M=128, N=128, K=16, both operands
+//               K-major) and O += P V (M=128, N=128, P read from TMEM, V an
+//               MN-major shared-memory operand).  The QK^T of tile j+2 goes out
+//               as soon as the softmax has read S of tile j, so it overlaps the
+//               whole softmax of tile j; the PV of tile j follows its P.
+//   warps 4-7   softmax: one thread per row reads its 128 scores from TMEM,
+//               applies the tree mask,
+//               keeps a running (reference max, sum) in the exp2 domain, and
+//               writes P = 2^(s - max) as packed bf16 into its P buffer in
+//               TMEM, where the PV MMA reads it.
+// The output accumulator is rescaled (TMEM
+// load / store) only when a row maximum grows by more than 2^8, otherwise the
+// stale reference is kept; every P and the final O / l use the same reference,
+// so the result is exact up to rounding.  Every wait is bounded.
+//
+// Barrier protocol: each barrier completes once per tile (or once per two
+// tiles when indexed by tile parity); a waiter is never more than one
+// completion behind, so a single phase bit identifies the completion it wants.
+//   k_full/k_empty[t % 3], v_full/v_empty[t % 3]   TMA rings (32 KB stages)
+//   s_free[j%2]              S of tile j read     (softmax -> MMA)
+// and (tile % 2, (tile / 2) & 1) names a completion of the tile-parity barriers.
+//   s_full[j%2]              QK^T of tile j done  (MMA -> softmax)
+//   p_full[j%2]              P of tile j in TMEM  (softmax -> MMA); the softmax
+//                            runs at most one tile ahead of the MMA thread
+//   pv_done[j%2]             PV of tile j done    (MMA -> softmax); the softmax
+//                            waits for tile j-2 each tile and for tile j-1 only
+//                            before rescaling O
+#pragma once
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace eagle {
+namespace attn_tc {
+
+constexpr int TBN = 128;                          // keys per tile
+constexpr int KSTAGES = 3;                        // K ring
+constexpr int VSTAGES = 3;                        // V ring
+static_assert(KSTAGES == VSTAGES, "one producer loop serves both rings");
+constexpr int kPrefetch = 3;                      // L2 prefetch distance beyond each ring
+constexpr int NSBUF = 2;                          // S and P buffers in TMEM
+constexpr int ROWS_PER_CTA = 128;                 // one M-tile
+constexpr int Q_BYTES = 128 * kHeadDim * 2;       // 32 KB: two 64-column boxes of 16 KB
+constexpr int KV_BOX_BYTES = TBN * 64 * 2;        // 16 KB: 128 keys x 64 dims
+constexpr int K_BYTES = 2 * KV_BOX_BYTES;         // 32 KB (one K or V tile)
+constexpr int SMEM_BYTES = Q_BYTES + (KSTAGES + VSTAGES) * K_BYTES + 2048;
+constexpr int kThreads = 256;                     // warps 0-3 roles, 4-7 softmax
+constexpr uint32_t TMEM_COLS = 512;
+// TMEM columns: S[buf] at buf * 128, P[buf] (bf16 pairs) at 256 + buf * 64, O at 384
+constexpr uint32_t S_COL0 = 0, P_COL0 = 256, O_COL0 = 384;
+constexpr float kRescaleThreshold = 8.f;          // log2 units
+
+constexpr uint32_t kIdescQK = idesc_bf16(128, TBN, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, 0, 1);
+
+struct Args {
+    const uint16_t* q;
+    uint16_t* out;
+    float* ws_o;
+    float* ws_ml;
+    const int32_t* kv_len;
+    const int32_t* parent;
+    int B, n, Hq, Hkv, G, Lmax, splits;
+    float scale_log2;
+    int32_t* dev_status;
+};
+
+struct Bars {
+    uint64_t k_full[KSTAGES];
+    uint64_t k_empty[KSTAGES];
+    uint64_t v_full[VSTAGES];
+    uint64_t v_empty[VSTAGES];
+    uint64_t s_full[NSBUF];          // [tile parity]
+    uint64_t s_free[NSBUF];
+    uint64_t p_full[NSBUF];
+    uint64_t pv_done[NSBUF];
+    uint64_t drain;
+    uint32_t tmem_slot;
+    int abort_flag;
+    int err;
+    int pad;
+    unsigned long long anc[kMaxNodes];
+};
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;                                   // 32 KB
+    uint8_t* sK = sQ + Q_BYTES;                           // [KSTAGES][32 KB]
+    uint8_t* sV = sK + KSTAGES * K_BYTES;                 // [VSTAGES][32 KB]
+    Bars* bars = reinterpret_cast<Bars*>(sV + VSTAGES * K_BYTES);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rg = blockIdx.x;
+    const int kvh = blockIdx.y / a.splits, split = blockIdx.y % a.splits;
+    const int b = blockIdx.z;
+    const int n = a.n, G = a.G, rows = n * G;
+    const int row0 = rg * ROWS_PER_CTA;
+    const int L = a.kv_len[b];
+
+    if (tid == 0) {
+        int err = 0;
+        const int32_t* par = a.parent + (int64_t)b * n;
+        if (par[0] != -1) err = EAGLE_DEV_BAD_TREE;
+        bars->anc[0] = 1ull;
+        for (int i = 1; i < n && !err; ++i) {
+            const int p = par[i];
+            if (p < 0 || p >= i) { err = EAGLE_DEV_BAD_TREE; break; }
+            bars->anc[i] = bars->anc[p] | (1ull << i);
+        }
+        if (L < 0 || (int64_t)L + n > a.Lmax) err |= EAGLE_DEV_CAPACITY;
+        if (err && rg == 0 && blockIdx.y == 0) flag_error(a.dev_status, err);
+        bars->err = err;
+        for (int s = 0; s < KSTAGES; ++s) {
+            mbar_init(s32(&bars->k_full[s]), 1);
+            mbar_init(s32(&bars->k_empty[s]), 1);
+        }
+        for (int s = 0; s < VSTAGES; ++s) {
+            mbar_init(s32(&bars->v_full[s]), 1);
+            mbar_init(s32(&bars->v_empty[s]), 1);
+        }
+        for (int p = 0; p < NSBUF; ++p) {
+            mbar_init(s32(&bars->s_full[p]), 1);
+            mbar_init(s32(&bars->s_free[p]), 4);
+            mbar_init(s32(&bars->p_full[p]), 4);
+            mbar_init(s32(&bars->pv_done[p]), 1);
+        }
+        mbar_init(s32(&bars->drain), 1);
+        bars->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+    }
+    if (warp == 1) tmem_alloc(s32(&bars->tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    const bool err = bars->err != 0;
+
+    // key range of this split: committed keys are chunked, the last split adds the tree
+    int chunk = (L + a.splits - 1) / a.splits;
+    chunk = (chunk + TBN - 1) / TBN * TBN;
+    const int kb = err ? 0 : min(L, split * chunk);
+    const int ke = err ? 0 : ((split == a.splits - 1) ? L + n : min(L, kb + chunk));
+    const int T = err ? 0 : (ke - kb + TBN - 1) / TBN;
+    const int kvrow0 = (b * a.Hkv + kvh) * a.Lmax;
+
+    // ---- Q -> shared memory (warps 1-7, while warp 0 already streams K/V) ----
+    if (warp > 0) {
+        constexpr int kLoaders = kThreads - 32;
+        for (int c = tid - 32; c < ROWS_PER_CTA * 16; c += kLoaders) {
+            const int rr = c >> 4, c16 = c & 15;
+            const int r = row0 + rr;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows) {
+                const int i = r / G, g = r % G;
+                v = __ldg(reinterpret_cast<const uint4*>(
+                          a.q + (((int64_t)b * n + i) * a.Hq + kvh * G + g) * kHeadDim) + c16);
+            }
+            uint8_t* box = sQ + (c16 >> 3) * (Q_BYTES / 2);
+            *reinterpret_cast<uint4*>(box + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads - 32) : "memory");
+    }
+
+    if (warp == 0 || warp == 2) {
+        if (lane == 0 && T > 0) {
+            // ---------------- TMA producers: K (warp 0) and V (warp 2) ----------------
+            // Two independent rings, so neither load waits behind the other's stage.
+            const bool isK = warp == 0;
+            const CUtensorMap* map = isK ? &tmap_k : &tmap_v;
+            uint8_t* ring = isK ? sK : sV;
+            uint64_t* full = isK ? bars->k_full : bars->v_full;
+            uint64_t* empty = isK ? bars->k_empty : bars->v_empty;
+            constexpr int NS = KSTAGES;   // == VSTAGES
+            for (int t = 0; t < T; ++t) {
+                const int st = t % NS;
+                if (!mbar_wait(s32(&empty[st]), (((uint32_t)t / NS) & 1u) ^ 1u, abort_flag)) break;
+                // L2 prefetch kPrefetch tiles beyond the ring, paced with the loads
+                if (t == 0) {
+                    for (int jp = NS; jp < min(T, NS + kPrefetch); ++jp) {
+                        tma_prefetch_2d(map, 0, kvrow0 + kb + jp * TBN);
+                        tma_prefetch_2d(map, 64, kvrow0 + kb + jp * TBN);
+                    }
+                } else if (t + NS + kPrefetch - 1 < T) {
+                    const int yp = kvrow0 + kb + (t + NS + kPrefetch - 1) * TBN;
+                    tma_prefetch_2d(map, 0, yp);
+                    tma_prefetch_2d(map, 64, yp);
+                }
+                const uint32_t fb = s32(&full[st]);
+                mbar_expect_tx(fb, K_BYTES);
+                const int y = kvrow0 + kb + t * TBN;
+                tma_load_2d(s32(ring + st * K_BYTES), map, fb, 0, y);
+                tma_load_2d(s32(ring + st * K_BYTES + KV_BOX_BYTES), map, fb, 64, y);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && T > 0) {
+            // ---------------- MMA issuer ----------------
+            // Descriptors are built once; every operand below differs from its base
+            // only in the 14-bit start-address field (all addresses < 256 KB), so an
+            // MMA costs two adds.  Offsets are compile-time constants after unrolling.
+            const uint64_t dQ = sw128_desc(s32(sQ));
+            const uint64_t dK0 = sw128_desc(s32(sK));
+            const uint64_t dV0 = sw128_desc_mn(s32(sV), KV_BOX_BYTES, 1024);
+            const uint32_t ocol = tmem + O_COL0;
+            auto issue_qk = [&](int j) {     // S[j % 2] = Q K_j^T; frees K stage j
+                const uint64_t dk = dK0 + (uint64_t)(((j % KSTAGES) * K_BYTES) >> 4);
+                const uint32_t scol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
+#pragma unroll
+                for (int k = 0; k < kHeadDim / 16; ++k) {
+                    const uint32_t off = (k >> 2) * (Q_BYTES / 2) + (k & 3) * 32;
+                    umma_f16(scol, dQ + (uint64_t)(off >> 4),
+                             dk + (uint64_t)((((k >> 2) * KV_BOX_BYTES) + (k & 3) * 32) >> 4),
+                             kIdescQK, k > 0 ? 1u : 0u);
+                }
+                umma_commit(s32(&bars->s_full[j % NSBUF]));
+                umma_commit(s32(&bars->k_empty[j % KSTAGES]));
+            };
+            auto issue_pv = [&](int j) {     // O += P[j % 2] V_j; frees V stage j
+                const uint64_t dv = dV0 + (uint64_t)(((j % VSTAGES) * K_BYTES) >> 4);
+                const uint32_t pcol = tmem + P_COL0 + (uint32_t)((j % NSBUF) * (TBN / 2));
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+                for (int k = 0; k < TBN / 16; ++k)   // 16 keys = 8 packed TMEM columns
+                    umma_f16_ts(ocol, pcol + k * 8, dv + (uint64_t)((k * 16 * 128) >> 4), kIdescPV,
+                                k > 0 ? 1u : acc0);
+                umma_commit(s32(&bars->pv_done[j % NSBUF]));
+                umma_commit(s32(&bars->v_empty[j % VSTAGES]));
+            };
+            auto wait_on = [&](uint64_t* bar, uint32_t parity) {
+                if (!mbar_wait(s32(bar), parity, abort_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; ok && j < min(T, NSBUF); ++j) {
+                ok = wait_on(&bars->k_full[j % KSTAGES], ((uint32_t)j / KSTAGES) & 1u);
+                if (ok) issue_qk(j);
+            }
+            for (int j = 0; ok && j < T; ++j) {
+                // next scores first: S[j % 2] is free as soon as the softmax has read it
+                if (j + NSBUF < T) {
+                    const int jq = j + NSBUF;
+                    if (!wait_on(&bars->s_free[j % NSBUF], ((uint32_t)j / NSBUF) & 1u)) break;
+                    if (!wait_on(&bars->k_full[jq % KSTAGES], ((uint32_t)jq / KSTAGES) & 1u)) break;
+                    issue_qk(jq);
+                }
+                if (!wait_on(&bars->p_full[j % NSBUF], ((uint32_t)j / NSBUF) & 1u)) break;
+                if (!wait_on(&bars->v_full[j % VSTAGES], ((uint32_t)j / VSTAGES) & 1u)) break;
+                issue_pv(j);
+            }
+            umma_commit(s32(&bars->drain));
+            mbar_wait(s32(&bars->drain), 0u, abort_flag, /*honour_abort=*/false);
+        }
+    } else if (warp >= 4) {
+        // ---------------- softmax: one thread per query row ----------------
+        const int q4 = warp & 3;                         // TMEM lane quadrant
+        const int rr = q4 * 32 + lane;
+        const int r = row0 + rr;
+        const bool valid = r < rows;
+        const int i = valid ? r / G : 0;
+        const unsigned long long anc = valid ? bars->anc[i] : 0ull;
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        const uint32_t s_addr0 = tmem + lane_base + S_COL0;
+        const uint32_t p_addr0 = tmem + lane_base + P_COL0;
+        const uint32_t o_addr = tmem + lane_base + O_COL0;
+        const float sc = a.scale_log2;
+        float mref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < T; ++j) {
+            bool got = mbar_wait(s32(&bars->s_full[j % NSBUF]), ((uint32_t)j / NSBUF) & 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t s_addr = s_addr0 + (uint32_t)((j % NSBUF) * TBN);
+            float x[TBN];
+            {
+                uint32_t u0[32], u1[32], u2[32], u3[32];
+                tmem_ld32_nowait(s_addr, u0);
+                tmem_ld32_nowait(s_addr + 32, u1);
+                tmem_ld32_nowait(s_addr + 64, u2);
+                tmem_ld32_nowait(s_addr + 96, u3);
+                asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+                // the scores are in registers: let the MMA reuse this S buffer
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s32(&bars->s_free[j % NSBUF]));
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    x[c] = __uint_as_float(u0[c]);
+                    x[32 + c] = __uint_as_float(u1[c]);
+                    x[64 + c] = __uint_as_float(u2[c]);
+                    x[96 + c] = __uint_as_float(u3[c]);
+                }
+            }
+            const int key0 = kb + j * TBN;
+            if (key0 + TBN > L || key0 + TBN > ke || !valid) {
+                // visibility of the tile's keys as a 128-bit map: committed keys below L,
+                // tree key L + t visible iff bit t of the ancestor mask, nothing from ke on
+                uint64_t vis[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int k0 = key0 + 64 * w;
+                    const int nc = min(max(L - k0, 0), 64), ne = min(max(ke - k0, 0), 64);
+                    const uint64_t committed = nc >= 64 ? ~0ull : ((1ull << nc) - 1ull);
+                    const uint64_t upto = ne >= 64 ? ~0ull : ((1ull << ne) - 1ull);
+                    const int sh = L - k0;                     // tree key t sits at bit t + sh
+                    const uint64_t tree = (sh >= 64 || sh <= -64) ? 0ull
+                                          : (sh >= 0 ? anc << sh : anc >> (-sh));
+                    vis[w] = valid ? ((committed | tree) & upto) : 0ull;
+                }
+#pragma unroll
+                for (int c = 0; c < TBN; ++c)
+                    if (!((vis[c >> 6] >> (c & 63)) & 1ull)) x[c] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < TBN; ++c) mx = fmaxf(mx, x[c]);
+            mx *= sc;                              // scale > 0 commutes with max
+            float alpha = 1.f;
+            if (mx > mref + kRescaleThreshold || (mref == -INFINITY && mx > -INFINITY)) {
+                alpha = mref == -INFINITY ? 0.f : exp2f(mref - mx);
+                mref = mx;
+                l *= alpha;
+            }
+            // PV of tile j-2 is long done (the one completion pending on this barrier);
+            // waiting keeps the phase bookkeeping exact.  PV of tile j-1 is awaited
+            // only before the output accumulator is rescaled.
+            if (j >= NSBUF) {
+                got = mbar_wait(s32(&bars->pv_done[j % NSBUF]), ((uint32_t)(j - NSBUF) / NSBUF) & 1u,
+                                abort_flag);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            }
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                got = mbar_wait(s32(&bars->pv_done[(j - 1) % NSBUF]), ((uint32_t)(j - 1) / NSBUF) & 1u,
+                                abort_flag);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < kHeadDim / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + cc * 32, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(o_addr + cc * 32, o);
+                }
+            }
+            const float base = mref == -INFINITY ? 0.f : mref;
+            float ps = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(x[64 * h + 2 * e], sc, -base));
+                    const float p1 = ex2_approx(fmaf(x[64 * h + 2 * e + 1], sc, -base));
+                    ps += p0 + p1;
+                    pk[e] = pack2(p0, p1);
+                }
+                tmem_st32(p_addr0 + (uint32_t)((j % NSBUF) * (TBN / 2) + 32 * h), pk);   // P, bf16 pairs
+            }
+            l += ps;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s32(&bars->p_full[j % NSBUF]));
+        }
+        bool got = ok && T > 0 ? mbar_wait(s32(&bars->pv_done[(T - 1) % NSBUF]),
+                                           ((uint32_t)(T - 1) / NSBUF) & 1u, abort_flag)
+                               : false;
+        got = __all_sync(0xffffffffu, got);
+        tc_fence_after();
+        const int h = kvh * G + (valid ? r % G : 0);
+        const int64_t orow = ((int64_t)b * n + i) * a.Hq + h;
+        const float inv = (got && l > 0.f) ? 1.f / l : 0.f;
+        for (int cc = 0; cc < kHeadDim / 32; ++cc) {
+            uint32_t o[32];
+            if (got) tmem_ld32(o_addr + cc * 32, o);
+            else
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            if (!valid) continue;
+            if (a.splits == 1) {
+                uint16_t* dst = a.out + orow * kHeadDim + cc * 32;
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    const uint4 w = make_uint4(
+                        pack2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                        pack2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                        pack2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                        pack2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                    *reinterpret_cast<uint4*>(dst + e) = w;
+                }
+            } else {
+                const int64_t R = (int64_t)a.B * n * a.Hq;
+                float* dst = a.ws_o + ((int64_t)split * R + orow) * kHeadDim + cc * 32;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) =
+                        make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                    __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+            }
+        }
+        if (valid && a.splits > 1) {
+            const int64_t R = (int64_t)a.B * n * a.Hq;
+            *reinterpret_cast<float2*>(a.ws_ml + ((int64_t)split * R + orow) * 2) =
+                got ? make_float2(mref, l) : make_float2(-INFINITY, 0.f);
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *abort_flag) flag_error(a.dev_status, EAGLE_DEV_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace attn_tc
+}  // namespace eagle

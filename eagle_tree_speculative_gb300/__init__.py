@@ -166,6 +166,29 @@ def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=
         _ptr(frontier_tokens), _ptr(_status(dev_status, logits.device)), _stream(stream)))
 
 
+def eagle2_expand_static_state(level, final, logits, top_k, depth, n_out, hidden=None,
+                               lm_head_w=None, out_tokens=None, out_parent=None,
+                               out_draft_row=None, frontier_tokens=None, dev_status=None,
+                               stream=None):
+    """eagle2_expand with the tree state kept in the library's own fixed device array
+    (no scratch argument; one tree at a time per device, levels in order)."""
+    _dev(logits, "logits", torch.float32)
+    B, R, V = logits.shape
+    H = 0
+    if hidden is not None:
+        _dev(hidden, "hidden", torch.bfloat16)
+        _dev(lm_head_w, "lm_head_w", torch.bfloat16)
+        H = hidden.shape[-1]
+    for name, t in (("out_tokens", out_tokens), ("out_parent", out_parent),
+                    ("out_draft_row", out_draft_row), ("frontier_tokens", frontier_tokens)):
+        if t is not None:
+            _dev(t, name, torch.int32)
+    _check("eagle2_expand_static_state", lib().eagle2_expand_static_state(
+        int(level), int(final), _ptr(hidden), _ptr(lm_head_w), _ptr(logits), B, H, V, top_k,
+        depth, n_out, _ptr(out_tokens), _ptr(out_parent), _ptr(out_draft_row),
+        _ptr(frontier_tokens), _ptr(_status(dev_status, logits.device)), _stream(stream)))
+
+
 def eagle_softmax_stats(logits, temperature, row_max=None, row_sum=None, row_argmax=None,
                         dev_status=None, stream=None):
     _dev(logits, "logits", torch.float32)

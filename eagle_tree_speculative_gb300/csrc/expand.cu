@@ -19,6 +19,7 @@
 // The draft LM-head GEMM (lmhead_gemm.cu) writes the level's logits rows first
 // when hidden states are given.
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -433,4 +434,60 @@ extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
         EAGLE_CHECK_LAUNCH();
     }
     return EAGLE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the tree state lives in a file-scope device array.
+// ---------------------------------------------------------------------------
+namespace eagle {
+namespace {
+
+// Fixed home of the tree state for eagle2_expand_static_state.  It exists on
+// every device that loads the library, from load until process exit.
+constexpr size_t kStaticStateBytes = size_t(4) << 20;   // 4 MiB
+static __device__ __align__(256) unsigned char g_static_tree_state[kStaticStateBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_tree_state on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+eagle_status static_state_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EAGLE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return EAGLE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_tree_state) != cudaSuccess || p == nullptr)
+            return EAGLE_ERR_CUDA;
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return EAGLE_OK;
+}
+
+}  // namespace
+}  // namespace eagle
+
+extern "C" eagle_status eagle2_expand_static_state(int level, int final, const void* hidden,
+                                                   const void* lm_head_w, float* logits, int B,
+                                                   int H, int V, int top_k, int depth, int n_out,
+                                                   int32_t* out_tokens, int32_t* out_parent,
+                                                   int32_t* out_draft_row,
+                                                   int32_t* frontier_tokens, int32_t* dev_status,
+                                                   eagle_stream_t stream) {
+    const size_t need = eagle2_tree_state_size(B, top_k, depth);
+    if (need == 0 && B != 0) return EAGLE_ERR_SHAPE;
+    if (need > kStaticStateBytes) return EAGLE_ERR_CAPACITY;
+    void* state = nullptr;
+    const eagle_status st = static_state_address(&state);
+    if (st != EAGLE_OK) return st;
+    // Level 1 writes every field of a sequence's state that later levels read,
+    // so the array needs no clearing between trees.
+    return eagle2_expand(level, final, hidden, lm_head_w, logits, B, H, V, top_k, depth, n_out,
+                         state, kStaticStateBytes, out_tokens, out_parent, out_draft_row,
+                         frontier_tokens, dev_status, stream);
 }

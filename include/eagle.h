@@ -34,8 +34,9 @@
  *     affected sequence (accept_len = -1 where there is one), and ORs an
  *     EAGLE_DEV_* bit into *dev_status (an int32 in device memory the caller
  *     zeroes and reads when it synchronises).  dev_status may be NULL.
- *   - No global mutable state; calls on different streams are independent
- *     unless they share output buffers.
+ *   - No global mutable state, except the fixed tree-state array behind
+ *     eagle2_expand_static_state; other calls on different streams are
+ *     independent unless they share output buffers.
  *   - Shapes: n (tree nodes, root included) <= 64; head_dim == 128;
  *     Hq % Hkv == 0; temperature == 0 selects greedy decoding.
  */
@@ -189,6 +190,37 @@ eagle_status eagle2_expand(int level, int final, const void* hidden, const void*
                            void* tree_state, size_t state_bytes, int32_t* out_tokens,
                            int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
                            int32_t* dev_status, eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle2_expand_static_state -- eagle2_expand without caller-provided scratch.
+ * No counterpart in the paper: this is a deployment convenience of this library.
+ * It is for callers that cannot allocate device memory themselves: a serving
+ * loop that reserves all of its device memory once at start-up and may not
+ * allocate afterwards (cudaMalloc can synchronise the device and stall other
+ * work), or code that sits behind an allocator owned by another framework and
+ * has no way to obtain raw device memory of its own.
+ * The tree state lives in a file-scope device array of 4 MiB that the library
+ * holds on every device that loads it, until the process exits.  Arguments,
+ * outputs and errors are those of eagle2_expand, minus tree_state/state_bytes.
+ *   - Returns EAGLE_ERR_CAPACITY, launching nothing, when
+ *     eagle2_tree_state_size(B, top_k, depth) exceeds 4 MiB (for top_k = 10,
+ *     depth = 8 that is 16,348 bytes per sequence: up to 256 sequences).
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents: the levels of one tree must run in order, and calls that overlap
+ *     on the GPU (other streams, other host threads, another tree in between)
+ *     race.  Level 1 rewrites everything later levels read, so nothing needs
+ *     clearing between trees.
+ *   - Allocates nothing: no cudaMalloc / cudaFree, no allocating library call.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle2_expand_static_state(int level, int final, const void* hidden,
+                                        const void* lm_head_w, float* logits, int B, int H, int V,
+                                        int top_k, int depth, int n_out, int32_t* out_tokens,
+                                        int32_t* out_parent, int32_t* out_draft_row,
+                                        int32_t* frontier_tokens, int32_t* dev_status,
+                                        eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * eagle_softmax_stats -- per-row temperature softmax statistics.

@@ -32,6 +32,9 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "tree-verify steps/sec & accepted tokens/s at B=64; HBM GB/s vs roofline"
+# DRAM bytes (read + write) of one 640 x 4096 -> 128256 LM-head GEMM launch, from an
+# ncu capture of the current kernel: 1.0965e9 read + 0.3010e9 written.
+GEMM_LAUNCH_DRAM_BYTES = 1.3976e9
 CFG = W.CONFIGS["eagle3_b64"]
 SEED = 0
 
@@ -141,18 +144,13 @@ class Step:
         torch.cuda.synchronize()
         self.gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                         for _ in range(D)]
-        s = float(c.w_std * np.sqrt(H))
-        rows = self.draft_row.long()
-        self.target = torch.empty(B, n, V, device=dev)
-        for b in range(B):
-            r = rows[b]
-            has = r >= 0
-            noise = torch.randn(n, V, device=dev, generator=g) * c.sigma
-            self.target[b] = torch.where(has[:, None], self.logits[b, r.clamp(min=0)] + noise,
-                                         torch.randn(n, V, device=dev, generator=g) * s)
+        self.target = synth_target(torch, self.logits, self.draft_row, c.sigma,
+                                   float(c.w_std * np.sqrt(H)), g)
         torch.cuda.synchronize()
         self.gemm_ms = 0.0          # accumulated in-kernel GEMM time of timed steps
         self.gemm_rows = 0
+        self.gemm_full_ms = 0.0     # the same for the full-width levels (B x top_k rows)
+        self.gemm_full_launches = 0
 
     def expand(self, time_gemm=False):
         E = self.E
@@ -174,8 +172,12 @@ class Step:
         """Add the GEMM launch times recorded by the last time_gemm step (events are reused)."""
         for lvl in range(1, self.D + 1):
             e0, e1 = self.gemm_ev[lvl - 1]
-            self.gemm_ms += e0.elapsed_time(e1)
+            t = e0.elapsed_time(e1)
+            self.gemm_ms += t
             self.gemm_rows += self.B * (1 if lvl == 1 else self.k)
+            if lvl > 1:
+                self.gemm_full_ms += t
+                self.gemm_full_launches += 1
 
     def run(self, seed, time_gemm=False):
         E = self.E
@@ -195,6 +197,40 @@ class Step:
         c = CFG
         ws = self.E.tree_attn_workspace_size(self.B, self.n, c.Hq, c.Hkv, c.head_dim, c.Lmax)
         return self.D * 3 + 1 + (2 if ws else 1) + 1 + 1
+
+
+def synth_target(torch, logits, draft_row, sigma, leaf_std, g):
+    """Target logits per tree node: the node's draft row plus N(0, sigma^2) noise where
+    the node was expanded, a fresh N(0, leaf_std^2) row for a leaf."""
+    B, n = draft_row.shape
+    V = logits.shape[-1]
+    rows = draft_row.long()
+    target = torch.empty(B, n, V, device=logits.device)
+    for b in range(B):
+        r = rows[b]
+        noise = torch.randn(n, V, device=logits.device, generator=g) * sigma
+        target[b] = torch.where((r >= 0)[:, None], logits[b, r.clamp(min=0)] + noise,
+                                torch.randn(n, V, device=logits.device, generator=g) * leaf_std)
+    return target
+
+
+def reduce_over_ranks(x, dist, device, op):
+    """Max ("max") or sum ("sum") of a per-rank figure over all ranks; no-op alone.
+
+    Ranks run independent batches, so this is the only exchange: the slowest rank's
+    timed region and the total accepted tokens."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def step_throughput(world, ms_per_step):
+    """Whole-job steps/s: every rank completes one step of its own batch per
+    ms_per_step (the max over ranks)."""
+    return world * 1000.0 / ms_per_step
 
 
 def time_region(fn, steps, torch):
@@ -242,10 +278,7 @@ def run_ours(args, rank, world, dist):
     else:
         ms = time_region(lambda i: st.run(i), args.steps, torch)
     clk = clocks.stop()
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_over_ranks(ms, dist, dev, "max")
     ms_per_step = ms / args.steps
     acc_graph = float(st.accept_len.sum().item() + st.B)   # the replayed step's accepted tokens
 
@@ -262,9 +295,13 @@ def run_ours(args, rank, world, dist):
         t_eager += time.perf_counter() - e0
         st.collect_gemm_times()
     tok_per_step = float(accepted.item()) / eager_steps
+    tok_all_ranks = reduce_over_ranks(tok_per_step, dist, dev, "sum")
     gemm_ms, gemm_rows = st.gemm_ms, st.gemm_rows
     gemm_flops = 2.0 * gemm_rows * st.H * st.V
-    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    # roofline of the dominant kernel: the full-width GEMM launches (640 x 4096 -> 128256)
+    full_ms = st.gemm_full_ms / st.gemm_full_launches
+    full_flops = 2.0 * st.B * st.k * st.H * st.V
+    gemm_tflops = full_flops / (full_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
 
     # -------- per-call breakdown (separate short timing) --------
@@ -277,7 +314,7 @@ def run_ours(args, rank, world, dist):
 
     out = {
         "metric": METRIC,
-        "value": round(world * 1000.0 / ms_per_step, 3),
+        "value": round(step_throughput(world, ms_per_step), 3),
         "unit": "steps/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -299,15 +336,20 @@ def run_ours(args, rank, world, dist):
                    "compact_layers": CFG.n_layers, "temperature": 1.0,
                    "l2": "inputs larger than L2 (LM head 1.05 GB, logits 2.3 GB, KV 1.1 GB/layer)",
                    "parallelism": f"replicas x{world} (sequence-sharded, no collective)"},
-        "accepted_tokens_per_s": round(world * tok_per_step * 1000.0 / ms_per_step, 1),
-        "mean_accept_len_plus_1": round(tok_per_step / st.B, 4),
+        "accepted_tokens_per_s": round(tok_all_ranks * 1000.0 / ms_per_step, 1),
+        "mean_accept_len_plus_1": round(tok_all_ranks / (world * st.B), 4),
         "graph_step_accepted_tokens": acc_graph,
-        "roofline": {"kernel": "lmhead_gemm_kernel (tcgen05)", "bound": "tensor",
+        "roofline": {"kernel": "lmhead_gemm_kernel (tcgen05), 640 x 4096 -> 128256 launches",
+                     "bound": "tensor",
                      "achieved": round(gemm_tflops, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / peak, 4), "traffic": None,
+                     "frac": round(gemm_tflops / peak, 4), "traffic": GEMM_LAUNCH_DRAM_BYTES,
+                     "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                     "640-row launch (ncu); algorithmic 1.384e9",
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained",
-                     "flops_per_step": gemm_flops / eager_steps,
-                     "ms_per_step_in_kernel": round(gemm_ms / eager_steps, 4),
+                     "flops_per_launch": full_flops,
+                     "ms_per_launch": round(full_ms, 4),
+                     "gemm_ms_per_step_all_levels": round(gemm_ms / eager_steps, 4),
+                     "gemm_flops_per_step_all_levels": gemm_flops / eager_steps,
                      "timed": f"{eager_steps} eager steps, events around each launch"},
         "breakdown_ms": br,
         "e2e": e2e,
@@ -491,6 +533,111 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+KERNEL_CASES = ("gemm", "topk", "attn", "verify", "compact", "softmax")
+
+
+def kernel_case(name, reps):
+    """Launch one library call `reps` times on a single-kernel workload of the step's
+    shapes (inputs larger than L2, a few GB on the device), for profiler captures.
+
+      gemm     LM-head GEMM of one full level: 640 x 4096 -> 128256
+      topk     expansion levels 1-2 over [64, 71, 128256] draft logits: the level-2
+               launch is the full 640-row top-10
+      attn     tree attention, one layer, B=64, 32/8 heads, KV 4096, 60 nodes
+      verify   verify-and-accept, B=32, 60 nodes, V=128256, T=1
+      compact  KV compaction, 32 layers, B=4 (8 kv heads, Lmax 4156)
+      softmax  softmax statistics of [32, 60, 128256] target logits
+    """
+    import torch
+
+    import eagle_tree_speculative_gb300 as E
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = CFG
+    g = torch.Generator(device=dev).manual_seed(SEED + 11)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    leaf_std = float(c.w_std * np.sqrt(c.H))
+
+    def normal(shape, std, dtype=torch.float32):      # generated in place: no f32 temporaries
+        return torch.empty(shape, dtype=dtype, device=dev).normal_(0.0, std, generator=g)
+
+    def expanded(B):
+        logits = normal((B, c.R, c.V), leaf_std)
+        state = torch.empty(E.tree_state_size(B, c.top_k, c.depth), dtype=torch.uint8, device=dev)
+        tok = torch.empty(B, c.n, dtype=torch.int32, device=dev)
+        par, row = torch.empty_like(tok), torch.empty_like(tok)
+        for lvl in range(1, c.depth + 1):
+            E.eagle2_expand(lvl, lvl == c.depth, logits, c.top_k, c.depth, c.n, state,
+                            out_tokens=tok, out_parent=par, out_draft_row=row, dev_status=st)
+        return logits, state, tok, par, row
+
+    if name == "gemm":
+        M = c.B * c.top_k
+        h = normal((M, c.H), 1.0, torch.bfloat16)
+        w = normal((c.V, c.H), c.w_std, torch.bfloat16)
+        out = torch.empty(M, c.V, device=dev)
+        fn = lambda: E.eagle_lmhead_gemm(h, w, out=out, dev_status=st)  # noqa: E731
+    elif name == "topk":
+        logits = normal((c.B, c.R, c.V), leaf_std)
+        state = torch.empty(E.tree_state_size(c.B, c.top_k, c.depth), dtype=torch.uint8,
+                            device=dev)
+
+        def fn():
+            for lvl in (1, 2):
+                E.eagle2_expand(lvl, 0, logits, c.top_k, c.depth, c.n, state, dev_status=st)
+    elif name == "attn":
+        B = c.B
+        _, _, _, par, _ = expanded(8)
+        parent = par.repeat(B // 8, 1).contiguous()
+        q = normal((B, c.n, c.Hq, c.head_dim), 1.0, torch.bfloat16)
+        kc = normal((B, c.Hkv, c.Lmax, c.head_dim), 1.0, torch.bfloat16)
+        vc = normal((B, c.Hkv, c.Lmax, c.head_dim), 1.0, torch.bfloat16)
+        kv_len = torch.full((B,), c.L, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        ws = E.tree_attn_workspace_size(B, c.n, c.Hq, c.Hkv, c.head_dim, c.Lmax)
+        wsb = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: E.eagle_tree_attn(q, kc, vc, kv_len, parent, out=out,  # noqa: E731
+                                       workspace=wsb, dev_status=st)
+    elif name in ("verify", "softmax"):
+        B = 32
+        logits, _, tok, par, row = expanded(B)
+        target = synth_target(torch, logits, row, c.sigma, leaf_std, g)
+        if name == "verify":
+            fn = lambda: E.eagle_verify_accept(target, logits, tok, par, c.depth, 1.0, 7,  # noqa
+                                               draft_row=row, dev_status=st)
+        else:
+            fn = lambda: E.eagle_softmax_stats(target, 1.0, dev_status=st)  # noqa: E731
+    elif name == "compact":
+        B = 4
+        shape = (c.n_layers, B, c.Hkv, c.Lmax, c.head_dim)
+        kc = normal(shape, 1.0, torch.bfloat16)
+        vc = normal(shape, 1.0, torch.bfloat16)
+        kv_len0 = torch.full((B,), c.L, dtype=torch.int32, device=dev)
+        kv_len = kv_len0.clone()
+        # every sequence accepts a path of depth 6 through nodes 0, 2, 5, 9, 14, 20, 27
+        path = torch.full((B, c.depth + 1), -1, dtype=torch.int32, device=dev)
+        path[:, :7] = torch.tensor([0, 2, 5, 9, 14, 20, 27], dtype=torch.int32)
+        acc = torch.full((B,), 6, dtype=torch.int32, device=dev)
+
+        def fn():
+            E.eagle_kv_compact(kc, vc, kv_len, path, acc, c.depth, dev_status=st)
+            kv_len.copy_(kv_len0)
+    else:
+        raise ValueError(name)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    status = int(st.item())
+    print(json.dumps({"kernel_case": name, "reps": reps,
+                      "ms_per_call": round(e0.elapsed_time(e1) / reps, 4), "dev_status": status}))
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,7 +646,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-case", choices=KERNEL_CASES, default=None,
+                    help="profile helper: launch one call on its own workload and exit")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.kernel_case:
+        kernel_case(args.kernel_case, args.reps)
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

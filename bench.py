@@ -624,6 +624,7 @@ def kernel_case(name, reps):
             kv_len.copy_(kv_len0)
     else:
         raise ValueError(name)
+    fn()                                   # warm-up (first-call set-up stays untimed)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()

@@ -7,12 +7,16 @@
 // reranking keeps the global top-n nodes by V for verification.
 //
 // Kernels per level:
-//   row_topk_kernel  one CTA per frontier row: temperature-1 softmax statistics
-//                    and the row's top-k tokens (logit desc, token asc) in one
-//                    pass over the vocabulary; confidences c = exp(l - m) / Z.
-//   select_kernel    one CTA per sequence: the k_in * k candidates of the level,
-//                    V_child = V_parent * c in float32, the next frontier = the k
-//                    best by (V desc, id asc), and draft-row assignment.
+//   row_topk_kernel  one CTA per (frontier row, vocabulary segment): the
+//                    segment's temperature-1 softmax statistics (max, sum of
+//                    exponentials) and its top-k tokens (logit desc, token asc) in
+//                    one pass; up to 4 segments per row spread the rows evenly
+//                    over the SMs.
+//   select_kernel    one CTA per sequence: merges each row's segments into the
+//                    row's top-k and confidences c = exp(l - m) / Z, forms the
+//                    k_in * k candidates of the level, V_child = V_parent * c in
+//                    float32, the next frontier = the k best by (V desc, id asc),
+//                    and assigns draft rows.
 //   rerank_kernel    one CTA per sequence: bitonic sort of every candidate by
 //                    (V desc, depth asc, id asc), keep n-1 plus the root, then
 //                    sort those by (depth asc, V desc, id asc) and re-index parents.
@@ -34,17 +38,17 @@ namespace {
 
 constexpr int kKMax = 16;
 constexpr int kDepthMax = 16;
+constexpr int kSegMax = 4;        // vocabulary segments per draft row
 
 // Per-sequence tree state, 32-bit words:
-//   [0] non-finite flag  [1..3] reserved
+//   [0..3] reserved
 //   value[C] f32, parent[C], token[C], depth[C], row[C], frontier[kKMax],
-//   row_tok[kKMax * kKMax], row_conf[kKMax * kKMax] f32
+//   per (frontier row s < k, segment g < kSegMax), at index s * kSegMax + g:
+//   seg_stat[3] (max f32, sum f32, non-finite flag), seg_val[k] f32, seg_tok[k]
 struct StateView {
-    int C, k;
-    int64_t stride;  // words per sequence
     __host__ __device__ static int cand_count(int k, int D) { return 1 + k + (D - 1) * k * k; }
     __host__ __device__ static int64_t words(int k, int D) {
-        return 4 + 5LL * cand_count(k, D) + kKMax + 2LL * kKMax * kKMax;
+        return 4 + 5LL * cand_count(k, D) + kKMax + (int64_t)k * kSegMax * (3 + 2LL * k);
     }
 };
 
@@ -56,8 +60,9 @@ struct SeqState {
     int* depth;
     int* row;
     int* frontier;
-    int* row_tok;
-    float* row_conf;
+    int* seg_stat;    // [k * kSegMax][3]
+    float* seg_val;   // [k * kSegMax][k]
+    int* seg_tok;     // [k * kSegMax][k]
 };
 
 __device__ __forceinline__ SeqState seq_state(void* base, int b, int k, int D) {
@@ -71,8 +76,9 @@ __device__ __forceinline__ SeqState seq_state(void* base, int b, int k, int D) {
     s.depth = p + 4 + 3 * C;
     s.row = p + 4 + 4 * C;
     s.frontier = p + 4 + 5 * C;
-    s.row_tok = s.frontier + kKMax;
-    s.row_conf = reinterpret_cast<float*>(s.row_tok + kKMax * kKMax);
+    s.seg_stat = s.frontier + kKMax;
+    s.seg_val = reinterpret_cast<float*>(s.seg_stat + 3 * k * kSegMax);
+    s.seg_tok = s.seg_stat + 3 * k * kSegMax + k * k * kSegMax;
     return s;
 }
 
@@ -81,14 +87,23 @@ __device__ __forceinline__ bool topk_better(float v, int i, float w, int j) {
 }
 
 // ---------------------------------------------------------------------------
-// Row softmax statistics + top-k in one pass over the vocabulary.
+// Segment softmax statistics + top-k in one pass over the segment.
 // Statistics: each thread keeps an online (max, sum) with sum = sum
 // 2^((l - max) log2 e).  Top-k: each warp keeps ONE sorted list distributed
 // over its lanes (lane j holds the j-th best, order: logit desc, token asc).
-// A chunk of 4 logits per lane is filtered against the warp's current k-th
-// best (a ballot); the rare survivors are inserted one at a time with a
-// shuffle shift.  The block then merges the per-warp lists the same way.
+// Every lane loads 8 float4 chunks before using them.  Before the first chunks
+// are used, each warp takes the k-th largest of its 32 lane maxima over them:
+// k elements of the segment reach it, so it bounds the segment's k-th best from
+// below, and the block keeps the largest such bound in shared memory (raised
+// again whenever a warp's own k-th best passes it).  A chunk is tested through
+// its maximum against that threshold (one vote per chunk); the rare surviving
+// elements are inserted one at a time with a shuffle shift.  At the end every
+// entry of the per-warp lists finds its rank among all of them in parallel, and
+// the segment's statistics and top-k go to the tree state.
 constexpr int kTopkThreads = 256;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkUnroll = 8;                 // float4 loads in flight per thread
+constexpr int kSegMinElems = 8192;             // shortest segment worth its own CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Insert (v, i) into the warp list (lv, li) sorted desc; all lanes call with the
@@ -105,18 +120,54 @@ __device__ __forceinline__ void warp_list_insert(float& lv, int& li, float v, in
     }
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+// The j-th largest of the warp's 32 values (bitonic sort, descending).
+__device__ __forceinline__ float warp_kth_largest(float x, int j) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float y = __shfl_xor_sync(0xffffffffu, x, stride);
+            const bool desc = (lane & size) == 0;               // direction of this block
+            const bool lower = (lane & stride) == 0;
+            x = (lower == desc) ? fmaxf(x, y) : fminf(x, y);
+        }
+    return __shfl_sync(0xffffffffu, x, j);
+}
+
+// Segments per row: one when the rows alone give every SM two CTAs, otherwise
+// enough (at most kSegMax, none shorter than kSegMinElems) to come close.
+int topk_segments(int V, int rows, int sms) {
+    if (rows >= 2 * sms) return 1;
+    int sgs = (2 * sms + rows - 1) / rows;
+    const int by_len = (V + kSegMinElems - 1) / kSegMinElems;
+    sgs = sgs < by_len ? sgs : by_len;
+    return sgs < 1 ? 1 : (sgs > kSegMax ? kSegMax : sgs);
+}
+
+__device__ __forceinline__ float ex2f_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 5)
 row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int V, int k, int D,
-                void* state, int32_t* dev_status) {
-    __shared__ float s_v[kTopkThreads / 32][kKMax];
-    __shared__ int s_i[kTopkThreads / 32][kKMax];
-    __shared__ float s_red[kTopkThreads / 32][2];
-    __shared__ int s_bad[kTopkThreads / 32];
-    __shared__ float s_pick_v[kKMax];
-    __shared__ int s_pick_i[kKMax];
+                int nseg, void* state) {
+    __shared__ float s_v[kTopkWarps * kKMax];
+    __shared__ int s_i[kTopkWarps * kKMax];
+    __shared__ float s_red[kTopkWarps][2];
+    __shared__ int s_bad[kTopkWarps];
+    __shared__ float s_thr;                    // a lower bound on the block's k-th best
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x / k_in, s = blockIdx.x % k_in;
+    if (tid == 0) s_thr = -INFINITY;
+    volatile float* thr_p = &s_thr;
+    const int row = blockIdx.x / nseg, seg = blockIdx.x % nseg;
+    const int b = row / k_in, s = row % k_in;
     const float* x = logits + ((int64_t)b * R + off + s) * (int64_t)V;
+    // segment [e0, e1), a multiple of 4 elements long except at the end of the row
+    const int seg_len = ((V + nseg - 1) / nseg + 3) & ~3;
+    const int e0 = min(V, seg * seg_len), e1 = min(V, e0 + seg_len);
 
     float lv = -INFINITY;            // warp list entry of this lane
     int li = 0x7fffffff;
@@ -124,10 +175,12 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
     int ti = 0x7fffffff;
     float m = -INFINITY, sum = 0.f;
     int bad = 0;
+    float thr = -INFINITY;
 
+    // lanes whose candidate beats the warp's k-th best and reaches the block's
+    // threshold insert it, one at a time
     auto offer = [&](float v, int i, bool mine) {
-        // lanes with a surviving candidate insert it, one lane at a time
-        unsigned ball = __ballot_sync(0xffffffffu, mine && topk_better(v, i, tv, ti));
+        unsigned ball = __ballot_sync(0xffffffffu, mine && v >= thr && topk_better(v, i, tv, ti));
         while (ball) {
             const int src = __ffs(ball) - 1;
             ball &= ball - 1;
@@ -137,56 +190,77 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
                 warp_list_insert(lv, li, cv, ci);
                 tv = __shfl_sync(0xffffffffu, lv, k - 1);
                 ti = __shfl_sync(0xffffffffu, li, k - 1);
+                // publish a raised k-th best (a lost race only leaves a lower bound)
+                if (lane == 0 && tv > *thr_p) *thr_p = tv;
             }
         }
-    };
-    auto chunk4 = [&](float4 l4, int t, bool valid) {
-        if (valid) {
-            bad |= isnan(l4.x) | isnan(l4.y) | isnan(l4.z) | isnan(l4.w) | (l4.x == INFINITY) |
-                   (l4.y == INFINITY) | (l4.z == INFINITY) | (l4.w == INFINITY);
-            const float mx = fmaxf(fmaxf(l4.x, l4.y), fmaxf(l4.z, l4.w));
-            if (mx > m) {
-                sum = (m == -INFINITY) ? 0.f : sum * exp2f((m - mx) * kLog2e);
-                m = mx;
-            }
-            if (m != -INFINITY)
-                sum += exp2f((l4.x - m) * kLog2e) + exp2f((l4.y - m) * kLog2e) +
-                       exp2f((l4.z - m) * kLog2e) + exp2f((l4.w - m) * kLog2e);
-        }
-        offer(l4.x, t, valid);
-        offer(l4.y, t + 1, valid);
-        offer(l4.z, t + 2, valid);
-        offer(l4.w, t + 3, valid);
     };
 
     if (((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0)) {
-        const float4* x4 = reinterpret_cast<const float4*>(x);
-        const int n4 = V >> 2;
-        // warp-uniform trip counts: every lane of a warp runs the same iterations
-        int base = warp * 32;
-        for (; base + 3 * kTopkThreads < n4; base += 4 * kTopkThreads) {
-            const int t = base + lane;
-            const float4 a0 = __ldg(x4 + t), a1 = __ldg(x4 + t + kTopkThreads);
-            const float4 a2 = __ldg(x4 + t + 2 * kTopkThreads), a3 = __ldg(x4 + t + 3 * kTopkThreads);
-            chunk4(a0, 4 * t, true);
-            chunk4(a1, 4 * (t + kTopkThreads), true);
-            chunk4(a2, 4 * (t + 2 * kTopkThreads), true);
-            chunk4(a3, 4 * (t + 3 * kTopkThreads), true);
-        }
-        for (; base < n4; base += kTopkThreads) {
-            const int t = base + lane;
-            const bool ok = t < n4;
-            chunk4(ok ? __ldg(x4 + t) : make_float4(0.f, 0.f, 0.f, 0.f), 4 * t, ok);
+        const float4* x4 = reinterpret_cast<const float4*>(x + e0);
+        const int n4 = (e1 - e0) >> 2;
+        // block-uniform trip counts: every lane runs every iteration (votes)
+        for (int base = 0; base < n4; base += kTopkUnroll * kTopkThreads) {
+            float4 c[kTopkUnroll];
+#pragma unroll
+            for (int u = 0; u < kTopkUnroll; ++u) {
+                const int t = base + u * kTopkThreads + tid;
+                c[u] = t < n4 ? __ldg(x4 + t) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            if (base == 0) {
+                // seed the threshold: the k-th largest lane maximum of each warp
+                float lmax = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < kTopkUnroll; ++u)
+                    lmax = fmaxf(lmax, fmaxf(fmaxf(c[u].x, c[u].y), fmaxf(c[u].z, c[u].w)));
+                const float est = warp_kth_largest(lmax, k - 1);
+                __syncthreads();                               // s_thr initialised
+                if (lane == 0 && est > *thr_p) *thr_p = est;
+                __syncthreads();
+            }
+            thr = fmaxf(tv, *thr_p);
+#pragma unroll
+            for (int u = 0; u < kTopkUnroll; ++u) {
+                const int t = base + u * kTopkThreads + tid;
+                const bool valid = t < n4;
+                const float4 l4 = c[u];
+                const float cm = fmaxf(fmaxf(l4.x, l4.y), fmaxf(l4.z, l4.w));
+                if (valid) {
+                    // NaN or +inf anywhere in the chunk makes its sum NaN or +inf
+                    const float s4 = (l4.x + l4.y) + (l4.z + l4.w);
+                    bad |= (s4 != s4) | (s4 == INFINITY);
+                    if (cm > m) {
+                        sum = (m == -INFINITY) ? 0.f : sum * ex2f_fast((m - cm) * kLog2e);
+                        m = cm;
+                    }
+                    if (m != -INFINITY)
+                        sum += ex2f_fast((l4.x - m) * kLog2e) + ex2f_fast((l4.y - m) * kLog2e) +
+                               ex2f_fast((l4.z - m) * kLog2e) + ex2f_fast((l4.w - m) * kLog2e);
+                }
+                // a chunk can only contribute if its maximum reaches the threshold
+                if (__any_sync(0xffffffffu, valid && cm >= thr)) {
+                    const int i0 = e0 + 4 * t;
+                    offer(l4.x, i0, valid);
+                    offer(l4.y, i0 + 1, valid);
+                    offer(l4.z, i0 + 2, valid);
+                    offer(l4.w, i0 + 3, valid);
+                    thr = fmaxf(tv, *thr_p);
+                }
+            }
         }
     } else {
-        for (int base = warp * 32; base < V; base += kTopkThreads) {
-            const int t = base + lane;
-            const bool ok = t < V;
+        __syncthreads();                                       // s_thr initialised
+        for (int base = e0; base < e1; base += kTopkThreads) {
+            const int t = base + tid;
+            const bool ok = t < e1;
             const float l = ok ? x[t] : 0.f;
             if (ok) {
-                bad |= isnan(l) | (l == INFINITY);
-                if (l > m) { sum = (m == -INFINITY) ? 0.f : sum * exp2f((m - l) * kLog2e); m = l; }
-                if (m != -INFINITY) sum += exp2f((l - m) * kLog2e);
+                bad |= (l != l) | (l == INFINITY);
+                if (l > m) {
+                    sum = (m == -INFINITY) ? 0.f : sum * ex2f_fast((m - l) * kLog2e);
+                    m = l;
+                }
+                if (m != -INFINITY) sum += ex2f_fast((l - m) * kLog2e);
             }
             offer(l, t, ok);
         }
@@ -200,52 +274,55 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
             if (m == -INFINITY) { m = om; sum = os; }
             else {
                 const float nm = fmaxf(m, om);
-                sum = sum * exp2f((m - nm) * kLog2e) + os * exp2f((om - nm) * kLog2e);
+                sum = sum * ex2f_fast((m - nm) * kLog2e) + os * ex2f_fast((om - nm) * kLog2e);
                 m = nm;
             }
         }
     }
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) { s_red[warp][0] = m; s_red[warp][1] = sum; s_bad[warp] = bad; }
-    if (lane < kKMax) { s_v[warp][lane] = lv; s_i[warp][lane] = li; }
+    if (lane < k) { s_v[warp * kKMax + lane] = lv; s_i[warp * kKMax + lane] = li; }
     __syncthreads();
-    if (warp == 0) {
-        lv = -INFINITY; li = 0x7fffffff;
-        tv = -INFINITY; ti = 0x7fffffff;
-        for (int w = 0; w < kTopkThreads / 32; ++w)
-            for (int j = 0; j < k; ++j) {
-                const float cv = s_v[w][j];
-                const int ci = s_i[w][j];
-                if (ci != 0x7fffffff && topk_better(cv, ci, tv, ti)) {
-                    warp_list_insert(lv, li, cv, ci);
-                    tv = __shfl_sync(0xffffffffu, lv, k - 1);
-                    ti = __shfl_sync(0xffffffffu, li, k - 1);
-                }
-            }
-        if (lane < k) { s_pick_v[lane] = lv; s_pick_i[lane] = li; }
+    SeqState st = seq_state(state, b, k, D);
+    const int slot = s * kSegMax + seg;
+    // rank of every list entry among all of them (entries are distinct tokens,
+    // or empty slots that rank below every token)
+    if (tid < kTopkWarps * k) {
+        const int w = tid / k, j = tid % k;
+        const float v = s_v[w * kKMax + j];
+        const int i = s_i[w * kKMax + j];
+        int rank = 0;
+        for (int w2 = 0; w2 < kTopkWarps; ++w2)
+            for (int j2 = 0; j2 < k; ++j2)
+                rank += topk_better(s_v[w2 * kKMax + j2], s_i[w2 * kKMax + j2], v, i);
+        if (rank < k && i != 0x7fffffff) {
+            st.seg_val[slot * k + rank] = v;
+            st.seg_tok[slot * k + rank] = i;
+        }
     }
-    __syncthreads();
     if (tid == 0) {
+        // fewer than k entries can only happen for a segment shorter than k
+        int cnt = 0;
+        for (int w = 0; w < kTopkWarps; ++w)
+            for (int j = 0; j < k; ++j) cnt += s_i[w * kKMax + j] != 0x7fffffff;
+        for (int j = cnt; j < k; ++j) {
+            st.seg_val[slot * k + j] = -INFINITY;
+            st.seg_tok[slot * k + j] = 0x7fffffff;
+        }
         float M = -INFINITY, S = 0.f;
         int bd = 0;
-        for (int w = 0; w < kTopkThreads / 32; ++w) {
+        for (int w = 0; w < kTopkWarps; ++w) {
             const float wm = s_red[w][0], ws = s_red[w][1];
             bd |= s_bad[w];
             if (wm == -INFINITY) continue;
             if (M == -INFINITY) { M = wm; S = ws; continue; }
             const float nm = fmaxf(M, wm);
-            S = S * exp2f((M - nm) * kLog2e) + ws * exp2f((wm - nm) * kLog2e);
+            S = S * ex2f_fast((M - nm) * kLog2e) + ws * ex2f_fast((wm - nm) * kLog2e);
             M = nm;
         }
-        SeqState st = seq_state(state, b, k, D);
-        if (bd || M == -INFINITY) {
-            st.hdr[0] = 1;
-            flag_error(dev_status, EAGLE_DEV_NONFINITE);
-        }
-        for (int j = 0; j < k; ++j) {
-            st.row_tok[s * kKMax + j] = s_pick_i[j];
-            st.row_conf[s * kKMax + j] = exp2f((s_pick_v[j] - M) * kLog2e) / S;
-        }
+        st.seg_stat[3 * slot] = __float_as_int(M);
+        st.seg_stat[3 * slot + 1] = __float_as_int(S);
+        st.seg_stat[3 * slot + 2] = bd;
     }
 }
 
@@ -253,12 +330,51 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
 constexpr int kSelectThreads = 256;
 
 __global__ void __launch_bounds__(kSelectThreads)
-select_kernel(int level, int final, int k, int D, void* state, int32_t* frontier_tokens) {
+select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t* frontier_tokens,
+              int32_t* dev_status) {
     __shared__ float s_val[kKMax * kKMax];
     __shared__ int s_id[kKMax * kKMax];
+    __shared__ float s_conf[kKMax * kKMax];     // [row s][rank j]: confidence of the row's j-th best
+    __shared__ int s_tok[kKMax * kKMax];
+    __shared__ float s_rowM[kKMax], s_rowS[kKMax];
     const int tid = threadIdx.x, b = blockIdx.x;
     SeqState st = seq_state(state, b, k, D);
     const int k_in = level == 1 ? 1 : k;
+    // ---- each row's softmax statistics from its segments ----
+    if (tid < k_in) {
+        float M = -INFINITY, S = 0.f;
+        int bd = 0;
+        for (int g = 0; g < nseg; ++g) {
+            const int slot = tid * kSegMax + g;
+            const float gm = __int_as_float(st.seg_stat[3 * slot]);
+            const float gs = __int_as_float(st.seg_stat[3 * slot + 1]);
+            bd |= st.seg_stat[3 * slot + 2];
+            if (gm == -INFINITY) continue;
+            if (M == -INFINITY) { M = gm; S = gs; continue; }
+            const float nm = fmaxf(M, gm);
+            S = S * exp2f((M - nm) * kLog2e) + gs * exp2f((gm - nm) * kLog2e);
+            M = nm;
+        }
+        if (bd || M == -INFINITY) flag_error(dev_status, EAGLE_DEV_NONFINITE);
+        s_rowM[tid] = M;
+        s_rowS[tid] = S;
+    }
+    __syncthreads();
+    // ---- each row's top-k: rank of every segment entry among the row's entries ----
+    for (int e = tid; e < k_in * nseg * k; e += kSelectThreads) {
+        const int row = e / (nseg * k), r = e % (nseg * k);
+        const int base = row * kSegMax * k;                 // first entry of the row
+        const float v = st.seg_val[base + r];
+        const int i = st.seg_tok[base + r];
+        int rank = 0;
+        for (int f = 0; f < nseg * k; ++f)
+            rank += topk_better(st.seg_val[base + f], st.seg_tok[base + f], v, i);
+        if (rank < k) {
+            s_tok[row * kKMax + rank] = i;
+            s_conf[row * kKMax + rank] = exp2f((v - s_rowM[row]) * kLog2e) / s_rowS[row];
+        }
+    }
+    __syncthreads();
     if (level == 1 && tid == 0) {
         st.value[0] = 1.0f;
         st.parent[0] = -1;
@@ -273,10 +389,10 @@ select_kernel(int level, int final, int k, int D, void* state, int32_t* frontier
         const int s = e / k, j = e % k;
         const int id = level == 1 ? 1 + j : 1 + k + (level - 2) * k * k + s * k + j;
         const int par = st.frontier[s];
-        const float val = __fmul_rn(st.value[par], st.row_conf[s * kKMax + j]);
+        const float val = __fmul_rn(st.value[par], s_conf[s * kKMax + j]);
         st.value[id] = val;
         st.parent[id] = par;
-        st.token[id] = st.row_tok[s * kKMax + j];
+        st.token[id] = s_tok[s * kKMax + j];
         st.depth[id] = level;
         st.row[id] = -1;
         s_val[e] = val;
@@ -414,11 +530,12 @@ extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
                                              (int64_t)R, off, dev_status, s);
         if (st != EAGLE_OK) return st;
     }
-    row_topk_kernel<<<B * k_in, kTopkThreads, 0, s>>>(logits, k_in, R, off, V, top_k, depth,
-                                                     tree_state, dev_status);
+    const int nseg = topk_segments(V, B * k_in, device_sm_count());
+    row_topk_kernel<<<B * k_in * nseg, kTopkThreads, 0, s>>>(logits, k_in, R, off, V, top_k, depth,
+                                                            nseg, tree_state);
     EAGLE_CHECK_LAUNCH();
-    select_kernel<<<B, kSelectThreads, 0, s>>>(level, final, top_k, depth, tree_state,
-                                                 frontier_tokens);
+    select_kernel<<<B, kSelectThreads, 0, s>>>(level, final, top_k, depth, nseg, tree_state,
+                                                 frontier_tokens, dev_status);
     EAGLE_CHECK_LAUNCH();
     if (final) {
         const int Cl = StateView::cand_count(top_k, level);

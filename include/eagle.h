@@ -204,7 +204,7 @@ eagle_status eagle2_expand(int level, int final, const void* hidden, const void*
  * outputs and errors are those of eagle2_expand, minus tree_state/state_bytes.
  *   - Returns EAGLE_ERR_CAPACITY, launching nothing, when
  *     eagle2_tree_state_size(B, top_k, depth) exceeds 4 MiB (for top_k = 10,
- *     depth = 8 that is 16,348 bytes per sequence: up to 256 sequences).
+ *     depth = 8 that is 17,980 bytes per sequence: up to 233 sequences).
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream
  *     capture.

@@ -50,7 +50,9 @@ def test_host_only_queries(lib_path):
     assert E.lib().eagle_abi_version() == 100
     assert E.lib().eagle_status_str(2) == b"EAGLE_ERR_SHAPE"
     # workspace and tree-state sizes are pure host arithmetic
-    assert E.tree_state_size(64, 10, 8) == 64 * 4 * (4 + 5 * 711 + 16 + 512)
+    # header, 5 words per candidate (711 at k=10, D=8), frontier, and per (row, segment)
+    # of up to 4 vocabulary segments: 3 statistics words + k values + k tokens
+    assert E.tree_state_size(64, 10, 8) == 64 * 4 * (4 + 5 * 711 + 16 + 10 * 4 * (3 + 2 * 10))
     assert E.tree_state_size(1, 17, 8) == 0                # top_k above the limit
     assert E.tree_attn_workspace_size(64, 60, 32, 8, 128, 4156) >= 0
     assert E.tree_attn_workspace_size(1, 60, 32, 8, 64, 4156) == 0    # head_dim != 128

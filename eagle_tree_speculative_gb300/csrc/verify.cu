@@ -87,19 +87,28 @@ __device__ __forceinline__ float prob_of(float l, float lmax, float inv, float c
     return exp2f((l - lmax) * c) * inv;
 }
 
-// Weight of token t in q_cur after j rejections at the current node:
-// r_0 = q(t); r_i = max(0, r_{i-1} - p(t)) / S_i (unchanged when S_i == 0);
-// invS[i] = 1 / S_i (0 marks S_i == 0).
-__device__ __forceinline__ float residual_at(float lq, float lp, RowStat Q, float iq, RowStat P,
-                                             float ip, float c, const float* invS, int j) {
-    float r = prob_of(lq, Q.lmax, iq, c);
-    if (j == 0) return r;
-    const float pp = prob_of(lp, P.lmax, ip, c);
-    for (int i = 1; i <= j; ++i) {
-        const float is = invS[i];
-        if (is > 0.f) r = fmaxf(0.f, r - pp) * is;
-    }
-    return r;
+// Weight of token t in q_cur after the rejections so far at the current node.
+// The rejection rule r_0 = q, r_j = max(0, r_{j-1} - p) / S_j (kept unchanged when
+// S_j == 0) unrolls to r_j(t) = max(0, q(t) - c_j p(t)) / D_j: by induction, with
+// c_0 = 0 and D_0 = 1, max(0, r_j - p) = max(0, q - (c_j + D_j) p) / D_j, so a
+// rejection pass sums s = sum_t max(0, q - (c_j + D_j) p) and sets
+// c_{j+1} = c_j + D_j, D_{j+1} = s (S_{j+1} = s / D_j).  Every pass and the
+// final race then cost O(1) per token, however many siblings were rejected.
+struct Residual {
+    float rc, rD, rinv;   // c_j, D_j, 1 / D_j
+};
+
+__device__ __forceinline__ float resid_weight(float lq, float lp, RowStat Q, float iq, RowStat P,
+                                              float ip, float c, const Residual& rs) {
+    const float q = prob_of(lq, Q.lmax, iq, c);
+    if (rs.rc == 0.f) return q;
+    return fmaxf(0.f, q - rs.rc * prob_of(lp, P.lmax, ip, c)) * rs.rinv;
+}
+
+// The unnormalised weight of the next residual, max(0, q - (c_j + D_j) p).
+__device__ __forceinline__ float next_resid(float lq, float lp, RowStat Q, float iq, RowStat P,
+                                            float ip, float c, float cnext) {
+    return fmaxf(0.f, prob_of(lq, Q.lmax, iq, c) - cnext * prob_of(lp, P.lmax, ip, c));
 }
 
 struct Slot {
@@ -115,13 +124,13 @@ struct VerifySmem {
     int row[kMaxNodes];
     int nkids[kMaxNodes];
     int lastkid[kMaxNodes];
-    float invS[kMaxNodes + 1];       // 1 / S_i of the residual normalisers at the current node
     int path[kMaxNodes + 1];
     int emit[kMaxNodes + 1];
     float red[NT / 32][4];
     int redi[NT / 32];
     int redbad[NT / 32];
     Slot x[2];                       // double-buffered exchange slot
+    Slot bc;                         // the cluster-wide result, for this CTA's threads
     int err;
 };
 
@@ -165,16 +174,30 @@ struct Cluster {
             sm.x[buf].bad = bd;
         }
         sync();
-        q = RowStat{-INFINITY, 0.f};
-        p = RowStat{-INFINITY, 0.f};
-        bad = 0;
-#pragma unroll
-        for (int r = 0; r < CS; ++r) {
-            const Slot* s = slot(sm, buf, r);
-            q = rs_combine(q, RowStat{s->f[0], s->f[1]}, c);
-            p = rs_combine(p, RowStat{s->f[2], s->f[3]}, c);
-            bad |= s->bad;
+        if (warp == 0) {
+            // lane r fetches CTA r's slot; lane 0 combines them in rank order
+            Slot mine{};
+            if (lane < CS) mine = *slot(sm, buf, lane);
+            RowStat a{-INFINITY, 0.f}, b{-INFINITY, 0.f};
+            int bd = 0;
+            for (int r = 0; r < CS; ++r) {       // every lane, same order
+                const float f0 = __shfl_sync(0xffffffffu, mine.f[0], r);
+                const float f1 = __shfl_sync(0xffffffffu, mine.f[1], r);
+                const float f2 = __shfl_sync(0xffffffffu, mine.f[2], r);
+                const float f3 = __shfl_sync(0xffffffffu, mine.f[3], r);
+                a = rs_combine(a, RowStat{f0, f1}, c);
+                b = rs_combine(b, RowStat{f2, f3}, c);
+                bd |= __shfl_sync(0xffffffffu, mine.bad, r);
+            }
+            if (lane == 0) {
+                sm.bc.f[0] = a.lmax; sm.bc.f[1] = a.S; sm.bc.f[2] = b.lmax; sm.bc.f[3] = b.S;
+                sm.bc.bad = bd;
+            }
         }
+        __syncthreads();
+        q = RowStat{sm.bc.f[0], sm.bc.f[1]};
+        p = RowStat{sm.bc.f[2], sm.bc.f[3]};
+        bad = sm.bc.bad;
         buf ^= 1;
     }
     __device__ static float sum(Smem& sm, int& buf, float v) {
@@ -188,9 +211,15 @@ struct Cluster {
             sm.x[buf].f[0] = t;
         }
         sync();
-        float S = 0.f;
-#pragma unroll
-        for (int r = 0; r < CS; ++r) S += slot(sm, buf, r)->f[0];
+        if (warp == 0) {
+            float mine = 0.f;
+            if (lane < CS) mine = slot(sm, buf, lane)->f[0];
+            float S = 0.f;
+            for (int r = 0; r < CS; ++r) S += __shfl_sync(0xffffffffu, mine, r);   // rank order
+            if (lane == 0) sm.bc.f[0] = S;
+        }
+        __syncthreads();
+        const float S = sm.bc.f[0];
         buf ^= 1;
         return S;
     }
@@ -213,15 +242,25 @@ struct Cluster {
             sm.x[buf].bad = bd;
         }
         sync();
-        KeyIdx b{-INFINITY, 0x7fffffff};
-        bad = 0;
-#pragma unroll
-        for (int r = 0; r < CS; ++r) {
-            const Slot* s = slot(sm, buf, r);
-            KeyIdx c{s->f[0], s->i};
-            if (ki_better(c, b)) b = c;
-            bad |= s->bad;
+        if (warp == 0) {
+            Slot mine{};
+            if (lane < CS) mine = *slot(sm, buf, lane);
+            KeyIdx b{-INFINITY, 0x7fffffff};
+            int bd = 0;
+            for (int r = 0; r < CS; ++r) {       // every lane, same order
+                const KeyIdx c{__shfl_sync(0xffffffffu, mine.f[0], r), __shfl_sync(0xffffffffu, mine.i, r)};
+                if (ki_better(c, b)) b = c;
+                bd |= __shfl_sync(0xffffffffu, mine.bad, r);
+            }
+            if (lane == 0) {
+                sm.bc.f[0] = b.k;
+                sm.bc.i = b.i;
+                sm.bc.bad = bd;
+            }
         }
+        __syncthreads();
+        const KeyIdx b{sm.bc.f[0], sm.bc.i};
+        bad = sm.bc.bad;
         buf ^= 1;
         return b;
     }
@@ -232,29 +271,64 @@ __device__ __forceinline__ int cta_rank_in_cluster(int cs) {
     return 0;
 }
 
+// E = -ln u' for the race uniform u' = (2 (w >> 9) + 1) 2^-24.  Near u' = 1 (where
+// the race is usually won: E is small) it uses the exact complement
+// v = 1 - u' = (2^24 - 2 (w >> 9) - 1) 2^-24 and the Taylor series of -ln(1 - v),
+// v + v^2/2 + v^3/3 + v^4/4 (truncation below v^5/5 < 2^-30 relative for
+// v < 2^-6); elsewhere -log2(u') ln 2 with the hardware log2, whose error is
+// then small relative to |log2 u'| > 0.02.
+__device__ __forceinline__ float race_exponential(uint32_t w) {
+    const uint32_t a = 2u * (w >> 9) + 1u;                 // u' = a 2^-24
+    const uint32_t comp = (1u << 24) - a;                   // v = comp 2^-24, exact
+    if (comp < (1u << 18)) {
+        const float v = (float)comp * 0x1p-24f;
+        return v * (1.f + v * (0.5f + v * (1.f / 3.f + v * 0.25f)));
+    }
+    return -__log2f((float)a * 0x1p-24f) * 0.69314718055994531f;
+}
+
 // Exponential race over the weights w_t (any positive scale): argmax_t w_t / E_t,
-// E_t = -ln u'_t.  `weight(lq, lp)` gives w_t from the two logits of token t.
+// E_t = -ln u'_t.  `weight(lq, lp)` gives w_t from the two logits of token t; the
+// generator is only run for 4-token blocks with some positive weight.
 template <int NT, class Weight>
 __device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* prow, int lo, int hi,
                                              bool vec4, uint32_t b, uint32_t k0, uint32_t k1,
                                              Weight weight) {
     KeyIdx best{-1.f, 0x7fffffff};
-    if (vec4) {
-        for (int t = lo + 4 * (int)threadIdx.x; t < hi; t += 4 * NT) {
-            const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-            const float4 b4 = prow ? __ldg(reinterpret_cast<const float4*>(prow + t))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    auto block4 = [&](float4 a4, float4 b4, int t) {
+        const float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
+        float rr[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) rr[e] = weight(ax[e], bx[e]);
+        if (rr[0] > 0.f || rr[1] > 0.f || rr[2] > 0.f || rr[3] > 0.f) {
             const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
-            const float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
             const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float rr = weight(ax[e], bx[e]);
-                if (rr > 0.f) {
-                    const KeyIdx cand{rr / -logf(unit_open(wx[e])), t + e};
+                if (rr[e] > 0.f) {
+                    const KeyIdx cand{__fdividef(rr[e], race_exponential(wx[e])), t + e};
                     if (ki_better(cand, best)) best = cand;
                 }
             }
+        }
+    };
+    if (vec4) {
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        int t = lo + 4 * (int)threadIdx.x;
+        for (; t + 12 * NT < hi; t += 16 * NT) {          // 4 float4 of each row in flight
+            float4 a4[4], b4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a4[u] = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * u * NT));
+                b4[u] = prow ? __ldg(reinterpret_cast<const float4*>(prow + t + 4 * u * NT)) : z;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) block4(a4[u], b4[u], t + 4 * u * NT);
+        }
+        for (; t < hi; t += 4 * NT) {
+            const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
+            const float4 b4 = prow ? __ldg(reinterpret_cast<const float4*>(prow + t)) : z;
+            block4(a4, b4, t);
         }
     } else {
         for (int t = lo + (int)threadIdx.x; t < hi; t += NT) {
@@ -262,7 +336,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* pro
             if (rr > 0.f) {
                 const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
                 const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-                const KeyIdx cand{rr / -logf(unit_open(wx[t & 3])), t};
+                const KeyIdx cand{__fdividef(rr, race_exponential(wx[t & 3])), t};
                 if (ki_better(cand, best)) best = cand;
             }
         }
@@ -290,26 +364,35 @@ __global__ void __launch_bounds__(NT) verify_walk_kernel(VerifyArgs a) {
         sm.nkids[tid] = 0;
         sm.lastkid[tid] = -1;
     }
+    if (tid == 0) sm.err = 0;
     __syncthreads();
-    if (tid == 0) {
+    // one thread per node: parent in [0, i) (root: -1), token in range, depth
+    // within D (walking up a strictly decreasing chain), children counts
+    if (tid < n) {
         int err = 0;
-        unsigned char depth[kMaxNodes];
-        if (sm.parent[0] != -1) err |= EAGLE_DEV_BAD_TREE;
-        depth[0] = 0;
-        for (int i = 1; i < n && !err; ++i) {
-            const int p = sm.parent[i];
-            if (p < 0 || p >= i) { err |= EAGLE_DEV_BAD_TREE; break; }
-            depth[i] = (unsigned char)(depth[p] + 1);
-            if (depth[i] > a.D) err |= EAGLE_DEV_DEPTH;
-            if (sm.tok[i] < 0 || sm.tok[i] >= V) err |= EAGLE_DEV_BAD_TOKEN;
-            sm.nkids[p] += 1;
-            sm.lastkid[p] = i;
+        const int p = sm.parent[tid];
+        if (tid == 0) {
+            if (p != -1) err |= EAGLE_DEV_BAD_TREE;
+        } else if (p < 0 || p >= tid) {
+            err |= EAGLE_DEV_BAD_TREE;
+        } else {
+            if (sm.tok[tid] < 0 || sm.tok[tid] >= V) err |= EAGLE_DEV_BAD_TOKEN;
+            int depth = 1, x = p;
+            while (x > 0) {
+                const int px = sm.parent[x];
+                if (px < 0 || px >= x) break;       // flagged by node x itself
+                x = px;
+                ++depth;
+            }
+            if (depth > a.D) err |= EAGLE_DEV_DEPTH;
+            atomicAdd(&sm.nkids[p], 1);
+            atomicMax(&sm.lastkid[p], tid);
         }
-        if (!err && a.T > 0.f)
-            for (int i = 0; i < n; ++i)
-                if (sm.nkids[i] && (sm.row[i] < 0 || sm.row[i] >= a.R)) err |= EAGLE_DEV_BAD_TOKEN;
-        sm.err = err;
+        if (err) atomicOr(&sm.err, err);
     }
+    __syncthreads();
+    if (tid < n && !sm.err && a.T > 0.f && sm.nkids[tid] && (sm.row[tid] < 0 || sm.row[tid] >= a.R))
+        atomicOr(&sm.err, EAGLE_DEV_BAD_TOKEN);
     __syncthreads();
 
     // ---- vocabulary slice of this CTA ----
@@ -336,20 +419,27 @@ __global__ void __launch_bounds__(NT) verify_walk_kernel(VerifyArgs a) {
             int bad = 0;
             if (vec4) {
                 int t = lo + 4 * tid;
-                for (; t + 4 * NT < hi; t += 8 * NT) {
-                    const float4 q0 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-                    const float4 q1 = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * NT));
-                    float4 p0 = make_float4(0.f, 0.f, 0.f, 0.f), p1 = p0;
+                // 4 float4 of each row in flight per thread
+                for (; t + 12 * NT < hi; t += 16 * NT) {
+                    float4 q4[4], p4[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        q4[u] = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * u * NT));
                     if (prow) {
-                        p0 = __ldg(reinterpret_cast<const float4*>(prow + t));
-                        p1 = __ldg(reinterpret_cast<const float4*>(prow + t + 4 * NT));
-                        bad |= bad4(p0) | bad4(p1);
-                        rs_push4(P, p0, c);
-                        rs_push4(P, p1, c);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            p4[u] = __ldg(reinterpret_cast<const float4*>(prow + t + 4 * u * NT));
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            bad |= bad4(p4[u]);
+                            rs_push4(P, p4[u], c);
+                        }
                     }
-                    bad |= bad4(q0) | bad4(q1);
-                    rs_push4(Q, q0, c);
-                    rs_push4(Q, q1, c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        bad |= bad4(q4[u]);
+                        rs_push4(Q, q4[u], c);
+                    }
                 }
                 for (; t < hi; t += 4 * NT) {
                     const float4 q0 = __ldg(reinterpret_cast<const float4*>(qrow + t));
@@ -389,14 +479,14 @@ __global__ void __launch_bounds__(NT) verify_walk_kernel(VerifyArgs a) {
             }
             const float iq = 1.f / Q.S, ip = prow ? 1.f / P.S : 0.f;
             // ---------- children in index order ----------
-            int j = 0;
+            Residual rs{0.f, 1.f, 1.f};
             bool moved = false, fused = false;
             for (int ch = v + 1; ch < n && kids; ++ch) {
                 if (sm.parent[ch] != v) continue;
                 const int x = sm.tok[ch];
                 const float lq = qrow[x], lp = prow[x];
                 const float px = prob_of(lp, P.lmax, ip, c);
-                const float r = residual_at(lq, lp, Q, iq, P, ip, c, sm.invS, j);
+                const float r = resid_weight(lq, lp, Q, iq, P, ip, c, rs);
                 const float u = accept_uniform(a.seed, (uint32_t)b, (uint32_t)ch);
                 if (px <= 0.f || u < r / px) {
                     ++acc_n;
@@ -412,54 +502,64 @@ __global__ void __launch_bounds__(NT) verify_walk_kernel(VerifyArgs a) {
                     fused = true;
                     break;
                 }
-                // ---------- pass: residual normaliser S_{j+1} ----------
+                // ---------- pass: the next residual's normaliser ----------
+                const float cnext = rs.rc + rs.rD;
                 float s = 0.f;
                 if (vec4) {
-                    for (int t = lo + 4 * tid; t < hi; t += 4 * NT) {
+                    int t = lo + 4 * tid;
+                    for (; t + 12 * NT < hi; t += 16 * NT) {      // 4 float4 of each row in flight
+                        float4 a4[4], b4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            a4[u] = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * u * NT));
+                            b4[u] = __ldg(reinterpret_cast<const float4*>(prow + t + 4 * u * NT));
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            s += next_resid(a4[u].x, b4[u].x, Q, iq, P, ip, c, cnext) +
+                                 next_resid(a4[u].y, b4[u].y, Q, iq, P, ip, c, cnext) +
+                                 next_resid(a4[u].z, b4[u].z, Q, iq, P, ip, c, cnext) +
+                                 next_resid(a4[u].w, b4[u].w, Q, iq, P, ip, c, cnext);
+                    }
+                    for (; t < hi; t += 4 * NT) {
                         const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
                         const float4 b4 = __ldg(reinterpret_cast<const float4*>(prow + t));
-                        const float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            s += fmaxf(0.f, residual_at(ax[e], bx[e], Q, iq, P, ip, c, sm.invS, j) -
-                                                prob_of(bx[e], P.lmax, ip, c));
+                        s += next_resid(a4.x, b4.x, Q, iq, P, ip, c, cnext) +
+                             next_resid(a4.y, b4.y, Q, iq, P, ip, c, cnext) +
+                             next_resid(a4.z, b4.z, Q, iq, P, ip, c, cnext) +
+                             next_resid(a4.w, b4.w, Q, iq, P, ip, c, cnext);
                     }
                 } else {
                     for (int t = lo + tid; t < hi; t += NT)
-                        s += fmaxf(0.f, residual_at(qrow[t], prow[t], Q, iq, P, ip, c, sm.invS, j) -
-                                            prob_of(prow[t], P.lmax, ip, c));
+                        s += next_resid(qrow[t], prow[t], Q, iq, P, ip, c, cnext);
                 }
                 const float S = C::sum(sm, buf, s);
-                ++j;
-                if (tid == 0) sm.invS[j] = S > 0.f ? 1.f / S : 0.f;
-                __syncthreads();
+                if (S > 0.f) rs = Residual{cnext, S, 1.f / S};   // else q_cur stays as it is
             }
             if (moved) continue;
             // ---------- pass: exponential race for the final token ----------
             int bad2 = 0;
             KeyIdx best;
             if (fused) {
-                const int jj = j;
+                // weights max(0, r_j - p), up to the positive factor 1 / D_j
+                const float cnext = rs.rc + rs.rD;
                 best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
                                       [&](float lq2, float lp2) {
-                                          return fmaxf(0.f, residual_at(lq2, lp2, Q, iq, P, ip, c,
-                                                                        sm.invS, jj) -
-                                                                prob_of(lp2, P.lmax, ip, c));
+                                          return next_resid(lq2, lp2, Q, iq, P, ip, c, cnext);
                                       });
                 best = C::argmax(sm, buf, best, bad2);
                 if (best.i == 0x7fffffff) {
                     // the clamped residual is all zero: keep q_cur (= r_j)
                     best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
                                           [&](float lq2, float lp2) {
-                                              return residual_at(lq2, lp2, Q, iq, P, ip, c, sm.invS, jj);
+                                              return resid_weight(lq2, lp2, Q, iq, P, ip, c, rs);
                                           });
                     best = C::argmax(sm, buf, best, bad2);
                 }
             } else {
-                const int jj = j;
                 best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
                                       [&](float lq2, float lp2) {
-                                          return residual_at(lq2, lp2, Q, iq, P, ip, c, sm.invS, jj);
+                                          return resid_weight(lq2, lp2, Q, iq, P, ip, c, rs);
                                       });
                 best = C::argmax(sm, buf, best, bad2);
             }

@@ -272,3 +272,35 @@ extern "C" const char* eagle_status_str(eagle_status s) {
 }
 
 extern "C" int eagle_abi_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that no
+// one completes, the same polling loop as the pipelines' waits but with the
+// caller's limit, then reports EAGLE_DEV_TIMEOUT and returns.
+namespace eagle {
+namespace {
+
+__global__ void wait_selftest_kernel(int32_t* dev_status, long long max_cycles) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(s32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    const long long t0 = clock64();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(s32(&bar), 0u)) return;            // never: no arrival
+        if ((it & 127u) == 127u && clock64() - t0 > max_cycles) break;
+    }
+    flag_error(dev_status, EAGLE_DEV_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace eagle
+
+extern "C" eagle_status eagle_wait_selftest(int32_t* dev_status, int64_t max_cycles,
+                                            eagle_stream_t stream) {
+    if (!dev_status || max_cycles < 1 || max_cycles > eagle::kTimeoutCycles) return EAGLE_ERR_INVALID_ARG;
+    eagle::wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        dev_status, (long long)max_cycles);
+    EAGLE_CHECK_LAUNCH();
+    return EAGLE_OK;
+}

@@ -249,6 +249,16 @@ eagle_status eagle_lmhead_gemm(const void* hidden, const void* w, float* out, in
                                int64_t row_offset, int32_t* dev_status, eagle_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
+/* ---------------------------------------------------------------------------
+ * eagle_wait_selftest -- exercises the bounded-wait path of the pipelined
+ * kernels.  No counterpart in the paper.  One thread waits on an mbarrier that
+ * nothing completes, polling it exactly as the pipelines do, for at most
+ * max_cycles SM clock cycles (1 .. 4e9), then ORs EAGLE_DEV_TIMEOUT into
+ * *dev_status (required, device memory) and returns.  Lets a caller (or a test)
+ * check that an expired wait reports a status and leaves the context usable.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_wait_selftest(int32_t* dev_status, int64_t max_cycles, eagle_stream_t stream);
+
 const char* eagle_status_str(eagle_status s);
 
 /* Library ABI version (major * 100 + minor). */

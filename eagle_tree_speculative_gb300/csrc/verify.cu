@@ -346,7 +346,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* pro
 
 // ---------------------------------------------------------------------------
 template <int CS, int NT>
-__global__ void __launch_bounds__(NT) verify_walk_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
     using C = Cluster<CS, NT>;
     __shared__ VerifySmem<NT> sm;
     const int tid = threadIdx.x;

@@ -120,6 +120,8 @@ class Step:
                        for l in range(1, D + 1)]
         self.logits = torch.empty(B, c.R, V, device=dev)          # draft-logit storage
         self.state = torch.empty(E.tree_state_size(B, k, D), dtype=torch.uint8, device=dev)
+        # per-tile softmax statistics and top-k from the GEMM epilogue (fused top-k)
+        self.partials = torch.empty(E.expand_scratch_size(B, V, k) // 4, device=dev)
         self.tokens = torch.empty(B, n, dtype=torch.int32, device=dev)
         self.parent = torch.empty_like(self.tokens)
         self.draft_row = torch.empty_like(self.tokens)
@@ -161,12 +163,14 @@ class Step:
                 self.gemm_ev[lvl - 1][0].record()
             E.eagle_lmhead_gemm(self.hidden[lvl - 1].view(self.B * k_in, self.H), self.w,
                                 out=self.logits, ldo=self.V, rows_per_group=k_in,
-                                group_stride=self.R, row_offset=off, dev_status=self.status)
+                                group_stride=self.R, row_offset=off, dev_status=self.status,
+                                partials=self.partials)
             if time_gemm:
                 self.gemm_ev[lvl - 1][1].record()
             E.eagle2_expand(lvl, lvl == self.D, self.logits, self.k, self.D, self.n, self.state,
                             out_tokens=self.tokens, out_parent=self.parent,
-                            out_draft_row=self.draft_row, dev_status=self.status)
+                            out_draft_row=self.draft_row, dev_status=self.status,
+                            partials=self.partials)
 
     def collect_gemm_times(self):
         """Add the GEMM launch times recorded by the last time_gemm step (events are reused)."""

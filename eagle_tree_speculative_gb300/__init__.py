@@ -143,10 +143,18 @@ def eagle_kv_compact(k_cache, v_cache, kv_len, path, accept_len, max_depth, dev_
         _stream(stream)))
 
 
+def expand_scratch_size(B, V, top_k) -> int:
+    return int(lib().eagle2_expand_scratch_size(B, V, top_k))
+
+
 def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=None,
                   lm_head_w=None, out_tokens=None, out_parent=None, out_draft_row=None,
-                  frontier_tokens=None, dev_status=None, stream=None):
-    """One EAGLE-2 level over draft-logit storage logits [B, R, V] (f32)."""
+                  frontier_tokens=None, dev_status=None, stream=None, partials=None):
+    """One EAGLE-2 level over draft-logit storage logits [B, R, V] (f32).  With a
+    partials buffer the level's statistics come from the GEMM epilogue's per-tile
+    partials (written by this call's GEMM when hidden is given, else by a prior
+    eagle_lmhead_gemm(..., partials=...) for the level's rows) and its top-k from a
+    rescan of the few tiles that can hold it."""
     _dev(logits, "logits", torch.float32)
     _dev(tree_state, "tree_state")
     B, R, V = logits.shape
@@ -160,10 +168,15 @@ def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=
         if t is not None:
             _dev(t, name, torch.int32)
     nbytes = tree_state.numel() * tree_state.element_size()
+    sbytes = 0
+    if partials is not None:
+        _dev(partials, "partials", torch.float32)
+        sbytes = partials.numel() * partials.element_size()
     _check("eagle2_expand", lib().eagle2_expand(
         int(level), int(final), _ptr(hidden), _ptr(lm_head_w), _ptr(logits), B, H, V, top_k, depth,
-        n_out, _ptr(tree_state), nbytes, _ptr(out_tokens), _ptr(out_parent), _ptr(out_draft_row),
-        _ptr(frontier_tokens), _ptr(_status(dev_status, logits.device)), _stream(stream)))
+        n_out, _ptr(tree_state), nbytes, _ptr(partials), sbytes, _ptr(out_tokens), _ptr(out_parent),
+        _ptr(out_draft_row), _ptr(frontier_tokens), _ptr(_status(dev_status, logits.device)),
+        _stream(stream)))
 
 
 def eagle2_expand_static_state(level, final, logits, top_k, depth, n_out, hidden=None,
@@ -208,8 +221,10 @@ def eagle_softmax_stats(logits, temperature, row_max=None, row_sum=None, row_arg
 
 
 def eagle_lmhead_gemm(hidden, w, out=None, ldo=None, rows_per_group=None, group_stride=0,
-                      row_offset=0, dev_status=None, stream=None):
-    """out[row(m)] = hidden[m] . W^T, hidden [M,K], w [N,K] bf16, out f32."""
+                      row_offset=0, dev_status=None, stream=None, partials=None):
+    """out[row(m)] = hidden[m] . W^T, hidden [M,K], w [N,K] bf16, out f32.  With a
+    partials buffer [M, ceil(N/256), 2] (f32) also each row's per-tile (max, sum of
+    exponentials)."""
     _dev(hidden, "hidden", torch.bfloat16)
     _dev(w, "w", torch.bfloat16)
     M, K = hidden.shape
@@ -219,7 +234,10 @@ def eagle_lmhead_gemm(hidden, w, out=None, ldo=None, rows_per_group=None, group_
     _dev(out, "out", torch.float32)
     ldo = N if ldo is None else ldo
     rpg = M if rows_per_group is None else rows_per_group
+    if partials is not None:
+        _dev(partials, "partials", torch.float32)
     _check("eagle_lmhead_gemm", lib().eagle_lmhead_gemm(
         _ptr(hidden), _ptr(w), _ptr(out), M, K, N, int(ldo), int(rpg), int(group_stride),
-        int(row_offset), _ptr(_status(dev_status, hidden.device)), _stream(stream)))
+        int(row_offset), _ptr(partials), _ptr(_status(dev_status, hidden.device)),
+        _stream(stream)))
     return out

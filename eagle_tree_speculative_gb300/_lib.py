@@ -25,12 +25,13 @@ SIGNATURES = {
                                  _P, _P]),
     "eagle_kv_compact": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "eagle2_tree_state_size": (_SZ, [_I, _I, _I]),
-    "eagle2_expand": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P, _P, _P, _P,
-                           _P]),
+    "eagle2_expand_scratch_size": (_SZ, [_I, _I, _I]),
+    "eagle2_expand": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _SZ, _P, _P, _P,
+                           _P, _P, _P]),
     "eagle2_expand_static_state": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _P, _P]),
     "eagle_softmax_stats": (_I, [_P, _I64, _I, _F, _P, _P, _P, _P, _P]),
-    "eagle_lmhead_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I64, _I, _I64, _I64, _P, _P]),
+    "eagle_lmhead_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I64, _I, _I64, _I64, _P, _P, _P]),
     "eagle_wait_selftest": (_I, [_P, _I64, _P]),
     "eagle_status_str": (ctypes.c_char_p, [_I]),
     "eagle_abi_version": (_I, []),

@@ -32,7 +32,9 @@ namespace eagle {
 // Defined in lmhead_gemm.cu.
 eagle_status lmhead_gemm_launch(const void* hidden, const void* w, float* out, int M, int K, int N,
                                 int64_t ldo, int rows_per_group, int64_t group_stride,
-                                int64_t row_offset, int32_t* dev_status, cudaStream_t stream);
+                                int64_t row_offset, int32_t* dev_status, cudaStream_t stream,
+                                float* part);
+constexpr int kGemmBN = 256;                    // columns per GEMM N-tile (one partial each)
 
 namespace {
 
@@ -327,6 +329,178 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
 }
 
 // ---------------------------------------------------------------------------
+// Top-k of a draft row from the LM-head GEMM's per-tile partials (fused path).
+// Each 256-column tile of the row has (max, sum of 2^((l - max) log2 e)) from the
+// GEMM's epilogue.  The row's statistics combine those in the exp2 domain.  Its
+// top-k: tau = the k-th largest tile maximum bounds the row's k-th best from below
+// (k tiles reach it), so every top-k entry lies in a tile whose maximum is >= tau;
+// only those tiles (about k of them) are read back from the logits row and fed to
+// the same warp lists as row_topk_kernel.  Exact, ties included.  The result goes
+// to segment 0 of the row in the tree state.
+constexpr int kMergeMaxTiles = 8192;                 // rows up to 2M columns
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_merge_kernel(const float* __restrict__ part, const float* __restrict__ logits, int k_in, int R,
+                  int off, int V, int num_n, int k, int D, void* state) {
+    __shared__ float s_v[kTopkWarps * kKMax];
+    __shared__ int s_i[kTopkWarps * kKMax];
+    __shared__ float s_red[kTopkWarps][2];
+    __shared__ int s_bad[kTopkWarps];
+    __shared__ float s_tau;
+    __shared__ int s_nsel;
+    __shared__ int s_sel[kMergeMaxTiles];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x, b = row / k_in, s = row % k_in;
+    const float2* P = reinterpret_cast<const float2*>(part) + (int64_t)row * num_n;
+    const float* x = logits + ((int64_t)b * R + off + s) * (int64_t)V;
+    if (tid == 0) s_nsel = 0;
+
+    float lv = -INFINITY, tv = -INFINITY, thr = -INFINITY;
+    int li = 0x7fffffff, ti = 0x7fffffff;
+    auto offer = [&](float v, int i, bool mine) {
+        unsigned ball = __ballot_sync(0xffffffffu, mine && v >= thr && topk_better(v, i, tv, ti));
+        while (ball) {
+            const int src = __ffs(ball) - 1;
+            ball &= ball - 1;
+            const float cv = __shfl_sync(0xffffffffu, v, src);
+            const int ci = __shfl_sync(0xffffffffu, i, src);
+            if (topk_better(cv, ci, tv, ti)) {
+                warp_list_insert(lv, li, cv, ci);
+                tv = __shfl_sync(0xffffffffu, lv, k - 1);
+                ti = __shfl_sync(0xffffffffu, li, k - 1);
+            }
+        }
+    };
+    // rank of this warp-list entry among all warps' entries (block-wide)
+    auto block_rank = [&](int w, int j) {
+        const float v = s_v[w * kKMax + j];
+        const int i = s_i[w * kKMax + j];
+        int rank = 0;
+        for (int w2 = 0; w2 < kTopkWarps; ++w2)
+            for (int j2 = 0; j2 < k; ++j2)
+                rank += topk_better(s_v[w2 * kKMax + j2], s_i[w2 * kKMax + j2], v, i);
+        return rank;
+    };
+
+    // ---- pass 1: statistics, and the k largest tile maxima ----
+    float m = -INFINITY, sum = 0.f;
+    int bad = 0;
+    for (int base = 0; base < num_n; base += kTopkThreads) {      // block-uniform trip count
+        const int t = base + tid;
+        const bool ok = t < num_n;
+        const float2 pr = ok ? P[t] : make_float2(-INFINITY, 0.f);
+        if (ok) {
+            bad |= (pr.y != pr.y) | (pr.x == INFINITY);
+            if (pr.x != -INFINITY) {
+                if (m == -INFINITY) { m = pr.x; sum = pr.y; }
+                else {
+                    const float nm = fmaxf(m, pr.x);
+                    sum = sum * ex2f_fast((m - nm) * kLog2e) + pr.y * ex2f_fast((pr.x - nm) * kLog2e);
+                    m = nm;
+                }
+            }
+        }
+        offer(pr.x, t, ok);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, o);
+        const float os = __shfl_xor_sync(0xffffffffu, sum, o);
+        if (om != -INFINITY) {
+            if (m == -INFINITY) { m = om; sum = os; }
+            else {
+                const float nm = fmaxf(m, om);
+                sum = sum * ex2f_fast((m - nm) * kLog2e) + os * ex2f_fast((om - nm) * kLog2e);
+                m = nm;
+            }
+        }
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) { s_red[warp][0] = m; s_red[warp][1] = sum; s_bad[warp] = bad; }
+    if (lane < k) { s_v[warp * kKMax + lane] = lv; s_i[warp * kKMax + lane] = li; }
+    __syncthreads();
+    if (tid < kTopkWarps * k) {
+        const int w = tid / k, j = tid % k;
+        // the entry of rank k - 1 is the k-th largest tile maximum (fewer tiles: -inf)
+        if (block_rank(w, j) == k - 1 && s_i[w * kKMax + j] != 0x7fffffff) s_tau = s_v[w * kKMax + j];
+    }
+    if (tid == 0) {
+        int cnt = 0;
+        for (int w = 0; w < kTopkWarps; ++w)
+            for (int j = 0; j < k; ++j) cnt += s_i[w * kKMax + j] != 0x7fffffff;
+        if (cnt < k) s_tau = -INFINITY;
+    }
+    __syncthreads();
+    const float tau = s_tau;
+    // ---- the tiles that can hold a top-k entry ----
+    for (int t = tid; t < num_n; t += kTopkThreads)
+        if (P[t].x >= tau) s_sel[atomicAdd(&s_nsel, 1)] = t;
+    __syncthreads();
+    const int nsel = s_nsel;
+    // ---- pass 2: those tiles' logits, one warp per tile ----
+    lv = -INFINITY; tv = -INFINITY; li = 0x7fffffff; ti = 0x7fffffff;
+    thr = tau;
+    const bool vec4 = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+    for (int q = warp; q < nsel; q += kTopkWarps) {                  // warp-uniform
+        const int c0 = s_sel[q] * kGemmBN;
+        const int c1 = min(V, c0 + kGemmBN);
+        if (vec4 && c1 - c0 == kGemmBN) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = c0 + 128 * h + 4 * lane;
+                const float4 l4 = __ldg(reinterpret_cast<const float4*>(x + c));
+                offer(l4.x, c, true);
+                offer(l4.y, c + 1, true);
+                offer(l4.z, c + 2, true);
+                offer(l4.w, c + 3, true);
+            }
+        } else {
+            for (int c = c0 + lane; c < c0 + kGemmBN; c += 32) {
+                const bool ok = c < c1;
+                offer(ok ? x[c] : -INFINITY, c, ok);
+            }
+        }
+    }
+    __syncthreads();                                  // everyone is done with s_v / s_i
+    if (lane < k) { s_v[warp * kKMax + lane] = lv; s_i[warp * kKMax + lane] = li; }
+    __syncthreads();
+    SeqState st = seq_state(state, b, k, D);
+    const int slot = s * kSegMax;
+    if (tid < kTopkWarps * k) {
+        const int w = tid / k, j = tid % k;
+        const int rank = block_rank(w, j);
+        const int i = s_i[w * kKMax + j];
+        if (rank < k && i != 0x7fffffff) {
+            st.seg_val[slot * k + rank] = s_v[w * kKMax + j];
+            st.seg_tok[slot * k + rank] = i;
+        }
+    }
+    if (tid == 0) {
+        int cnt = 0;
+        for (int w = 0; w < kTopkWarps; ++w)
+            for (int j = 0; j < k; ++j) cnt += s_i[w * kKMax + j] != 0x7fffffff;
+        for (int j = cnt; j < k; ++j) {
+            st.seg_val[slot * k + j] = -INFINITY;
+            st.seg_tok[slot * k + j] = 0x7fffffff;
+        }
+        float M = -INFINITY, S = 0.f;
+        int bd = 0;
+        for (int w = 0; w < kTopkWarps; ++w) {
+            const float wm = s_red[w][0], ws = s_red[w][1];
+            bd |= s_bad[w];
+            if (wm == -INFINITY) continue;
+            if (M == -INFINITY) { M = wm; S = ws; continue; }
+            const float nm = fmaxf(M, wm);
+            S = S * ex2f_fast((M - nm) * kLog2e) + ws * ex2f_fast((wm - nm) * kLog2e);
+            M = nm;
+        }
+        st.seg_stat[3 * slot] = __float_as_int(M);
+        st.seg_stat[3 * slot + 1] = __float_as_int(S);
+        st.seg_stat[3 * slot + 2] = bd;
+    }
+}
+
+// ---------------------------------------------------------------------------
 constexpr int kSelectThreads = 256;
 
 __global__ void __launch_bounds__(kSelectThreads)
@@ -500,10 +674,17 @@ extern "C" size_t eagle2_tree_state_size(int B, int top_k, int depth) {
     return (size_t)B * (size_t)StateView::words(top_k, depth) * 4u;
 }
 
+extern "C" size_t eagle2_expand_scratch_size(int B, int V, int top_k) {
+    if (B < 0 || V < 1 || top_k < 1 || top_k > kKMax) return 0;
+    const size_t tiles = ((size_t)V + kGemmBN - 1) / kGemmBN;
+    return (size_t)B * top_k * tiles * 2 * 4u;
+}
+
 extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
                                       const void* lm_head_w, float* logits, int B, int H, int V,
                                       int top_k, int depth, int n_out, void* tree_state,
-                                      size_t state_bytes, int32_t* out_tokens, int32_t* out_parent,
+                                      size_t state_bytes, float* partials, size_t partials_bytes,
+                                      int32_t* out_tokens, int32_t* out_parent,
                                       int32_t* out_draft_row, int32_t* frontier_tokens,
                                       int32_t* dev_status, eagle_stream_t stream) {
     if (B < 0 || V < 1 || top_k < 1 || depth < 1 || level < 1 || level > depth || !logits ||
@@ -520,6 +701,13 @@ extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
         if (n_out > have) return EAGLE_ERR_SHAPE;
     }
     if (hidden && (!lm_head_w || H < 1)) return EAGLE_ERR_INVALID_ARG;
+    // fused top-k: every 256-column tile of a row was (or is now) reduced by the
+    // GEMM's epilogue to its statistics and top-k; only those partials are merged
+    const bool fused = partials != nullptr;
+    if (fused && (partials_bytes < eagle2_expand_scratch_size(B, V, top_k) ||
+                  (reinterpret_cast<uintptr_t>(partials) & 7)))
+        return EAGLE_ERR_CAPACITY;
+    if (fused && (V + kGemmBN - 1) / kGemmBN > kMergeMaxTiles) return EAGLE_ERR_SHAPE;
     if (B == 0) return EAGLE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int R = 1 + (depth - 1) * top_k;
@@ -527,12 +715,20 @@ extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
     const int off = level == 1 ? 0 : 1 + (level - 2) * top_k;
     if (hidden) {
         eagle_status st = lmhead_gemm_launch(hidden, lm_head_w, logits, B * k_in, H, V, V, k_in,
-                                             (int64_t)R, off, dev_status, s);
+                                             (int64_t)R, off, dev_status, s,
+                                             partials);
         if (st != EAGLE_OK) return st;
     }
-    const int nseg = topk_segments(V, B * k_in, device_sm_count());
-    row_topk_kernel<<<B * k_in * nseg, kTopkThreads, 0, s>>>(logits, k_in, R, off, V, top_k, depth,
-                                                            nseg, tree_state);
+    int nseg = 1;
+    if (fused) {
+        const int num_n = (V + kGemmBN - 1) / kGemmBN;
+        topk_merge_kernel<<<B * k_in, kTopkThreads, 0, s>>>(partials, logits, k_in, R, off, V,
+                                                            num_n, top_k, depth, tree_state);
+    } else {
+        nseg = topk_segments(V, B * k_in, device_sm_count());
+        row_topk_kernel<<<B * k_in * nseg, kTopkThreads, 0, s>>>(logits, k_in, R, off, V, top_k,
+                                                                depth, nseg, tree_state);
+    }
     EAGLE_CHECK_LAUNCH();
     select_kernel<<<B, kSelectThreads, 0, s>>>(level, final, top_k, depth, nseg, tree_state,
                                                  frontier_tokens, dev_status);
@@ -605,6 +801,6 @@ extern "C" eagle_status eagle2_expand_static_state(int level, int final, const v
     // Level 1 writes every field of a sequence's state that later levels read,
     // so the array needs no clearing between trees.
     return eagle2_expand(level, final, hidden, lm_head_w, logits, B, H, V, top_k, depth, n_out,
-                         state, kStaticStateBytes, out_tokens, out_parent, out_draft_row,
-                         frontier_tokens, dev_status, stream);
+                         state, kStaticStateBytes, nullptr, 0, out_tokens, out_parent,
+                         out_draft_row, frontier_tokens, dev_status, stream);
 }

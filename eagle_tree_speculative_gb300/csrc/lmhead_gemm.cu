@@ -14,7 +14,11 @@
 //               tcgen05.commit; accumulators are double-buffered in TMEM so the
 //               epilogue of one tile overlaps the main loop of the next;
 //   warps 2-5   the epilogue: tcgen05.ld 32x32b from their TMEM lane quadrant,
-//               fp32 stores to the (possibly row-strided) output.
+//               fp32 stores to the (possibly row-strided) output; optionally each
+//               thread also reduces its row of the 256-column tile to a partial
+//               softmax statistic (max, sum of 2^((l - max) log2 e)), from which
+//               the expansion finds a row's top-k by rescanning only the few
+//               tiles whose maximum can hold one.
 // Tiles are visited M-fastest so the CTAs working on one 256-column slab of W
 // run together and share it through L2: W is read from HBM about once.
 // Every mbarrier wait is bounded (about two seconds); on expiry the kernel sets
@@ -47,7 +51,16 @@ struct GemmArgs {
     int rows_per_group;
     int64_t group_stride, row_offset;
     int32_t* dev_status;
+    float* part;     // optional: per (row, N-tile) (max, sum) of the tile's columns
 };
+
+constexpr float kLog2eG = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_fast_g(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -159,10 +172,29 @@ lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const int64_t grp = m / g.rows_per_group, within = m % g.rows_per_group;
                 orow = g.out + (grp * g.group_stride + g.row_offset + within) * g.ldo;
             }
+            // optional partial statistics of this row over the tile's columns
+            float pm = -INFINITY, ps = 0.f;
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
                 const int col = n0 + c * 32;
+                if (g.part && valid) {
+                    // online (max, sum of 2^((l - max) log2 e)) over the chunk's columns
+                    const int nv = min(32, g.N - col);
+                    float cmax = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < nv) cmax = fmaxf(cmax, __uint_as_float(r[j]));
+                    if (cmax > pm) {
+                        ps = (pm == -INFINITY) ? 0.f : ps * ex2_fast_g((pm - cmax) * kLog2eG);
+                        pm = cmax;
+                    }
+                    if (pm != -INFINITY) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nv) ps += ex2_fast_g((__uint_as_float(r[j]) - pm) * kLog2eG);
+                    }
+                }
                 if (valid) {
                     if (vec && col + 32 <= g.N) {
 #pragma unroll
@@ -177,6 +209,9 @@ lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                 }
             }
+            if (g.part && valid)
+                *reinterpret_cast<float2*>(g.part + ((int64_t)m * num_n + n0 / BN) * 2) =
+                    make_float2(pm, ps);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s32(&tempty[acc]));
@@ -221,7 +256,9 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows)
 
 eagle_status lmhead_gemm_launch(const void* hidden, const void* w, float* out, int M, int K, int N,
                                 int64_t ldo, int rows_per_group, int64_t group_stride,
-                                int64_t row_offset, int32_t* dev_status, cudaStream_t stream) {
+                                int64_t row_offset, int32_t* dev_status, cudaStream_t stream,
+                                float* part) {
+    if (part && (reinterpret_cast<uintptr_t>(part) & 7)) return EAGLE_ERR_INVALID_ARG;
     if (!hidden || !w || !out || M < 1 || N < 1 || K < BK || rows_per_group < 1 || ldo < N ||
         group_stride < 0 || row_offset < 0)
         return EAGLE_ERR_INVALID_ARG;
@@ -231,7 +268,7 @@ eagle_status lmhead_gemm_launch(const void* hidden, const void* w, float* out, i
         return EAGLE_ERR_INVALID_ARG;
     CUtensorMap ma, mb;
     if (!make_map(&ma, hidden, M, K, BM) || !make_map(&mb, w, N, K, BN)) return EAGLE_ERR_CUDA;
-    GemmArgs g{out, M, N, K, ldo, rows_per_group, group_stride, row_offset, dev_status};
+    GemmArgs g{out, M, N, K, ldo, rows_per_group, group_stride, row_offset, dev_status, part};
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
@@ -252,10 +289,11 @@ eagle_status lmhead_gemm_launch(const void* hidden, const void* w, float* out, i
 
 extern "C" eagle_status eagle_lmhead_gemm(const void* hidden, const void* w, float* out, int M,
                                           int K, int N, int64_t ldo, int rows_per_group,
-                                          int64_t group_stride, int64_t row_offset,
+                                          int64_t group_stride, int64_t row_offset, float* partials,
                                           int32_t* dev_status, eagle_stream_t stream) {
     return eagle::lmhead_gemm_launch(hidden, w, out, M, K, N, ldo, rows_per_group, group_stride,
-                                     row_offset, dev_status, reinterpret_cast<cudaStream_t>(stream));
+                                     row_offset, dev_status, reinterpret_cast<cudaStream_t>(stream),
+                                     partials);
 }
 
 extern "C" const char* eagle_status_str(eagle_status s) {

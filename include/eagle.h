@@ -176,6 +176,17 @@ eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, con
  *                 This level's rows are written (hidden != NULL) or read.
  *   tree_state    scratch of eagle2_tree_state_size(B, top_k, depth) bytes that
  *                 persists across the levels of one tree
+ *   partials      NULL: the level's top_k comes from one pass over its logits
+ *                 rows.  Otherwise f32 [B * k_in, ceil(V / 256), 2],
+ *                 eagle2_expand_scratch_size(B, V, top_k) bytes, 8-byte aligned:
+ *                 per 256-column tile of each row (row b * k_in + s) its max and
+ *                 sum of exponentials, as eagle_lmhead_gemm writes them; with
+ *                 hidden != NULL this call's GEMM writes them, otherwise the
+ *                 caller's eagle_lmhead_gemm(..., partials, ...) for this level's
+ *                 rows must have.  The row's statistics then come from the
+ *                 partials, and its top_k from rescanning only the tiles whose
+ *                 maximum reaches the k-th largest tile maximum (every top_k
+ *                 entry lies in one), instead of a pass over the whole row.
  *   out_tokens, out_parent, out_draft_row  int32 [B, n_out] (final only):
  *                 nodes in topological order (depth asc, V desc, id asc), root
  *                 first with token -1 and draft row 0; out_draft_row = -1 for
@@ -185,11 +196,12 @@ eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, con
  * depth <= 16.  Device errors: non-finite logit rows set EAGLE_DEV_NONFINITE.
  * ------------------------------------------------------------------------- */
 size_t eagle2_tree_state_size(int B, int top_k, int depth);
+size_t eagle2_expand_scratch_size(int B, int V, int top_k);
 eagle_status eagle2_expand(int level, int final, const void* hidden, const void* lm_head_w,
                            float* logits, int B, int H, int V, int top_k, int depth, int n_out,
-                           void* tree_state, size_t state_bytes, int32_t* out_tokens,
-                           int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
-                           int32_t* dev_status, eagle_stream_t stream);
+                           void* tree_state, size_t state_bytes, float* partials, size_t partials_bytes,
+                           int32_t* out_tokens, int32_t* out_parent, int32_t* out_draft_row,
+                           int32_t* frontier_tokens, int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * eagle2_expand_static_state -- eagle2_expand without caller-provided scratch.
@@ -201,7 +213,8 @@ eagle_status eagle2_expand(int level, int final, const void* hidden, const void*
  * has no way to obtain raw device memory of its own.
  * The tree state lives in a file-scope device array of 4 MiB that the library
  * holds on every device that loads it, until the process exits.  Arguments,
- * outputs and errors are those of eagle2_expand, minus tree_state/state_bytes.
+ * outputs and errors are those of eagle2_expand, minus tree_state/state_bytes
+ * and partials/partials_bytes (none: the top-k reads the logits rows).
  *   - Returns EAGLE_ERR_CAPACITY, launching nothing, when
  *     eagle2_tree_state_size(B, top_k, depth) exceeds 4 MiB (for top_k = 10,
  *     depth = 8 that is 17,980 bytes per sequence: up to 233 sequences).
@@ -243,10 +256,15 @@ eagle_status eagle_softmax_stats(const float* logits, int64_t rows, int V, float
  *   out    f32: row m of the product is stored at
  *          out + ((m / rows_per_group) * group_stride + row_offset + m % rows_per_group) * ldo
  *          (rows_per_group = M, group_stride = 0, row_offset = 0: a plain [M, ldo] matrix)
+ *   partials NULL, or f32 [M, ceil(N / 256), 2] (8-byte aligned): for each row
+ *          and 256-column tile, max l and sum 2^((l - max) log2 e) over the tile's
+ *          columns -- the temperature-1 softmax statistics of the row, tile by
+ *          tile, as eagle2_expand consumes them.
  * ------------------------------------------------------------------------- */
 eagle_status eagle_lmhead_gemm(const void* hidden, const void* w, float* out, int M, int K, int N,
                                int64_t ldo, int rows_per_group, int64_t group_stride,
-                               int64_t row_offset, int32_t* dev_status, eagle_stream_t stream);
+                               int64_t row_offset, float* partials, int32_t* dev_status,
+                               eagle_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 /* ---------------------------------------------------------------------------

@@ -99,7 +99,7 @@ def _compare_trees(ref, tok, par, row):
     return mism
 
 
-@pytest.mark.parametrize("name", ["eagle2_b1", "eagle3_b64"])
+@pytest.mark.parametrize("name", ["eagle2_b1", "eagle3_b64", "sweep_70b"])
 def test_expansion_from_logits_small_vocab(name):
     cfg = W.CONFIGS[name]
     B, V = 6, 3000
@@ -137,3 +137,99 @@ def test_expansion_fed_by_gemm_matches_expansion_of_its_logits():
     for b in range(B):
         assert par[b, 0] == -1 and all(0 <= par[b, i] < i for i in range(1, n_out))
         assert len(set(zip(par[b, 1:].tolist(), tok[b, 1:].tolist()))) == n_out - 1
+
+
+@pytest.mark.parametrize("M,N", [(37, 1000), (200, 2304), (130, 4096 + 77)])
+def test_gemm_partials_are_per_tile_statistics(M, N):
+    """The epilogue's per-tile partials against the GEMM's own fp32 output: tile max
+    bit-exact, sum of 2^((l - max) log2 e) to 1e-5 relative (fp64 reference); ragged
+    M and N tails."""
+    E = _E()
+    K = 256
+    h = W.to_bf16(W.normal((M, K), 1.0, 11, M)).cuda()
+    w = W.lm_head(N, K, 0.02, 11, block=1024).cuda()
+    tiles = (N + 255) // 256
+    part = torch.full((M, tiles, 2), float("nan"), device="cuda")
+    out = E.eagle_lmhead_gemm(h, w, partials=part)
+    torch.cuda.synchronize()
+    lg = out.cpu().numpy().astype(np.float64)
+    pt = part.cpu().numpy()
+    for t in range(tiles):
+        blk = lg[:, 256 * t: min(N, 256 * t + 256)]
+        mx = blk.max(1)
+        assert np.array_equal(pt[:, t, 0].astype(np.float64), mx)
+        ssum = np.exp(blk - mx[:, None]).sum(1)
+        np.testing.assert_allclose(pt[:, t, 1], ssum, rtol=1e-5)
+
+
+def test_fused_expansion_matches_unfused_expansion():
+    """hidden -> GEMM with per-tile partials -> merge gives the tree of the unfused
+    path (GEMM, then one pass over the logits) from the same hidden states, except
+    where the two fp32 summation orders leave a near-tie (GPU against GPU; the
+    unfused path is checked against the oracle above).  B=8, depth 4, V=32000."""
+    E = _E()
+    B, k, D, n_out, H, V = 8, 10, 4, 30, 1024, 32000
+    R = 1 + (D - 1) * k
+    w = W.lm_head(V, H, 0.02, 12, block=1024).cuda()
+    hid = [W.hidden_states(B, 1 if l == 1 else k, H, l, 12).cuda() for l in range(1, D + 1)]
+    part = torch.empty(E.expand_scratch_size(B, V, k) // 4, device="cuda")
+
+    def run(fused):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        state = torch.empty(E.tree_state_size(B, k, D), dtype=torch.uint8, device="cuda")
+        lg = torch.zeros(B, R, V, device="cuda")
+        tok = torch.empty(B, n_out, dtype=torch.int32, device="cuda")
+        par, row = torch.empty_like(tok), torch.empty_like(tok)
+        for lvl in range(1, D + 1):
+            E.eagle2_expand(lvl, lvl == D, lg, k, D, n_out, state, hidden=hid[lvl - 1], lm_head_w=w,
+                            out_tokens=tok, out_parent=par, out_draft_row=row, dev_status=st,
+                            partials=part if fused else None)
+        torch.cuda.synchronize()
+        return tok.cpu().numpy(), par.cpu().numpy(), row.cpu().numpy(), int(st.item()), lg
+
+    t1, p1, r1, s1, lg1 = run(True)
+    t0, p0, r0, s0, lg0 = run(False)
+    assert s0 == 0 and s1 == 0
+    assert torch.equal(lg0, lg1)                       # the logits rows are written either way
+    same = [(np.array_equal(t1[b], t0[b]) and np.array_equal(p1[b], p0[b]) and
+             np.array_equal(r1[b], r0[b])) for b in range(B)]
+    assert sum(same) >= B - 1
+
+
+def _expand_tree(E, B, k, D, n_out, V, w, hid, part):
+    R = 1 + (D - 1) * k
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    state = torch.empty(E.tree_state_size(B, k, D), dtype=torch.uint8, device="cuda")
+    lg = torch.zeros(B, R, V, device="cuda")
+    tok = torch.empty(B, n_out, dtype=torch.int32, device="cuda")
+    par, row = torch.empty_like(tok), torch.empty_like(tok)
+    for lvl in range(1, D + 1):
+        E.eagle2_expand(lvl, lvl == D, lg, k, D, n_out, state, hidden=hid[lvl - 1], lm_head_w=w,
+                        out_tokens=tok, out_parent=par, out_draft_row=row, dev_status=st,
+                        partials=part)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), par.cpu().numpy(), row.cpu().numpy(), int(st.item())
+
+
+def test_fused_expansion_tied_logits():
+    """LM-head rows repeated with period 500, so every logit of a row occurs 64 times
+    in 64 different tiles: the k largest tile maxima all tie, every one of the 64
+    tiles holding the row's best value is read back, and the top-k must be the k
+    lowest columns of that value, as the one-pass top-k gives.  Within a row the
+    children's path values tie exactly, so fused and unfused trees agree token for
+    token.  B=8, k=10, depth 3, V=32000."""
+    E = _E()
+    B, k, D, n_out, H, V = 8, 10, 3, 20, 512, 32000
+    base = W.lm_head(500, H, 0.02, 13, block=500)
+    w = base.repeat(V // 500, 1).contiguous().cuda()
+    hid = [W.hidden_states(B, 1 if l == 1 else k, H, l, 13).cuda() for l in range(1, D + 1)]
+    part = torch.empty(E.expand_scratch_size(B, V, k) // 4, device="cuda")
+    t1, p1, r1, s1 = _expand_tree(E, B, k, D, n_out, V, w, hid, part)
+    t0, p0, r0, s0 = _expand_tree(E, B, k, D, n_out, V, w, hid, None)
+    assert s0 == 0 and s1 == 0
+    for b in range(B):
+        # level-1 children: the 10 lowest columns of the root row's best value
+        kids = sorted(t1[b, 1:][p1[b, 1:] == 0].tolist())
+        assert len(kids) > 0
+        assert all(t % 500 == kids[0] % 500 for t in kids)
+    assert np.array_equal(t1, t0) and np.array_equal(p1, p0) and np.array_equal(r1, r0)

@@ -89,6 +89,22 @@ def test_eagle2_tree_b1_shape_matches_oracle(T):
     assert ref["accept_len"].mean() > 0.5     # the synthetic draft is informative
 
 
+@pytest.mark.parametrize("V,T,sigma", [(32000, 0.0, 0.5), (32000, 1.0, 0.5), (128256, 0.0, 0.5),
+                                         (128256, 1.0, 0.5), (32000, 1.0, 0.1), (32000, 1.0, 1.0)])
+def test_llama70b_sweep_trees_match_oracle(V, T, sigma):
+    """Sweep shape: 48-node depth-6 top-10 trees, B=8, across vocabulary, temperature
+    and draft noise (sigma sets how often the draft is accepted)."""
+    cfg = W.CONFIGS["sweep_70b"]
+    tgt, drows, tree = _tree_case(cfg, 8, seed=31, V=V, sigma=sigma)
+    ref = oracle.verify_accept(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, T, seed=13,
+                               draft_row=tree["draft_row"])
+    acc, path, emit, st = _run_gpu(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, T, 13,
+                                   draft_row=tree["draft_row"])
+    assert st == 0 and (ref["status"] == 0).all()
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+    assert_tie_budget(dec, ties)
+
+
 def test_eagle3_tree_b64_full_size_matches_oracle():
     """Full B=64, n=60, depth 8, V=128256 verify (sigma 0.3, T=1)."""
     cfg = W.CONFIGS["eagle3_b64"]

@@ -47,7 +47,7 @@ def _run_tree(logits, k, D, n_out, static, hidden=None, w=None):
         if static:
             rc = L.eagle2_expand_static_state(*common_head, *common_tail)
         else:
-            rc = L.eagle2_expand(*common_head, state.data_ptr(), state.numel(), *common_tail)
+            rc = L.eagle2_expand(*common_head, state.data_ptr(), state.numel(), None, 0, *common_tail)
         assert rc == 0, E.lib().eagle_status_str(rc)
     torch.cuda.synchronize()
     return (tok.cpu().numpy(), par.cpu().numpy(), row.cpu().numpy(), fr.cpu().numpy(),

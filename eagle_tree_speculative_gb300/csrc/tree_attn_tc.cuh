@@ -187,18 +187,30 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     // ---- Q -> shared memory (warps 1-7, while warp 0 already streams K/V) ----
     if (warp > 0) {
+        // all of a thread's 16-byte pieces are loaded before any is stored, so the
+        // tile costs one memory round trip rather than one per piece
         constexpr int kLoaders = kThreads - 32;
-        for (int c = tid - 32; c < ROWS_PER_CTA * 16; c += kLoaders) {
-            const int rr = c >> 4, c16 = c & 15;
-            const int r = row0 + rr;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows) {
+        constexpr int kPieces = ROWS_PER_CTA * 16;
+        constexpr int kPer = (kPieces + kLoaders - 1) / kLoaders;
+        uint4 v[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int c = tid - 32 + u * kLoaders;
+            const int r = row0 + (c >> 4);
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (c < kPieces && r < rows) {
                 const int i = r / G, g = r % G;
-                v = __ldg(reinterpret_cast<const uint4*>(
-                          a.q + (((int64_t)b * n + i) * a.Hq + kvh * G + g) * kHeadDim) + c16);
+                v[u] = __ldg(reinterpret_cast<const uint4*>(
+                             a.q + (((int64_t)b * n + i) * a.Hq + kvh * G + g) * kHeadDim) + (c & 15));
             }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int c = tid - 32 + u * kLoaders;
+            if (c >= kPieces) continue;
+            const int rr = c >> 4, c16 = c & 15;
             uint8_t* box = sQ + (c16 >> 3) * (Q_BYTES / 2);
-            *reinterpret_cast<uint4*>(box + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4)) = v;
+            *reinterpret_cast<uint4*>(box + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4)) = v[u];
         }
         fence_proxy_async_smem();
         asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads - 32) : "memory");
@@ -279,17 +291,36 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 ok = wait_on(&bars->k_full[j % KSTAGES], ((uint32_t)j / KSTAGES) & 1u);
                 if (ok) issue_qk(j);
             }
-            for (int j = 0; ok && j < T; ++j) {
-                // next scores first: S[j % 2] is free as soon as the softmax has read it
-                if (j + NSBUF < T) {
-                    const int jq = j + NSBUF;
-                    if (!wait_on(&bars->s_free[j % NSBUF], ((uint32_t)j / NSBUF) & 1u)) break;
-                    if (!wait_on(&bars->k_full[jq % KSTAGES], ((uint32_t)jq / KSTAGES) & 1u)) break;
-                    issue_qk(jq);
+            // Issue whichever is ready first: QK^T of tile js (its S buffer read by the
+            // softmax of tile js-2, its K tile landed) or PV of tile jp (its P written,
+            // its V tile landed), so a late K tile never holds back a PV and its V
+            // stage, and a late P never holds back the next scores.  Each completion
+            // tested is the next one of its barrier, so one parity bit names it.
+            int js = min(T, NSBUF), jp = 0;
+            long long t_last = clock64();
+            uint32_t idle = 0;
+            while (ok && jp < T) {
+                bool progressed = false;
+                if (js < T &&
+                    mbar_try_wait(s32(&bars->s_free[js % NSBUF]), ((uint32_t)(js - NSBUF) / NSBUF) & 1u) &&
+                    mbar_try_wait(s32(&bars->k_full[js % KSTAGES]), ((uint32_t)js / KSTAGES) & 1u)) {
+                    tc_fence_after();
+                    issue_qk(js++);
+                    progressed = true;
                 }
-                if (!wait_on(&bars->p_full[j % NSBUF], ((uint32_t)j / NSBUF) & 1u)) break;
-                if (!wait_on(&bars->v_full[j % VSTAGES], ((uint32_t)j / VSTAGES) & 1u)) break;
-                issue_pv(j);
+                if (jp < js &&
+                    mbar_try_wait(s32(&bars->p_full[jp % NSBUF]), ((uint32_t)jp / NSBUF) & 1u) &&
+                    mbar_try_wait(s32(&bars->v_full[jp % VSTAGES]), ((uint32_t)jp / VSTAGES) & 1u)) {
+                    tc_fence_after();
+                    issue_pv(jp++);
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = clock64();
+                } else if ((++idle & 63u) == 0u) {
+                    if (*abort_flag) ok = false;
+                    else if (clock64() - t_last > kTimeoutCycles) { *abort_flag = 1; ok = false; }
+                }
             }
             umma_commit(s32(&bars->drain));
             mbar_wait(s32(&bars->drain), 0u, abort_flag, /*honour_abort=*/false);
@@ -354,9 +385,16 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int c = 0; c < TBN; ++c)
                     if (!((vis[c >> 6] >> (c & 63)) & 1ull)) x[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            // row max over the tile: eight independent chains, then a tree
+            float m8[8];
 #pragma unroll
-            for (int c = 0; c < TBN; ++c) mx = fmaxf(mx, x[c]);
+            for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+            for (int c = 8; c < TBN; c += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], x[c + e]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             mx *= sc;                              // scale > 0 commutes with max
             float alpha = 1.f;
             if (mx > mref + kRescaleThreshold || (mref == -INFINITY && mx > -INFINITY)) {
@@ -387,7 +425,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
             }
             const float base = mref == -INFINITY ? 0.f : mref;
-            float ps = 0.f;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};      // four partial sums, no long FADD chain
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
@@ -395,12 +433,12 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int e = 0; e < 32; ++e) {
                     const float p0 = ex2_approx(fmaf(x[64 * h + 2 * e], sc, -base));
                     const float p1 = ex2_approx(fmaf(x[64 * h + 2 * e + 1], sc, -base));
-                    ps += p0 + p1;
+                    ps[e & 3] += p0 + p1;
                     pk[e] = pack2(p0, p1);
                 }
                 tmem_st32(p_addr0 + (uint32_t)((j % NSBUF) * (TBN / 2) + 32 * h), pk);   // P, bf16 pairs
             }
-            l += ps;
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s32(&bars->p_full[j % NSBUF]));

@@ -7,42 +7,39 @@
 // the Hq/Hkv query heads that share the kv head are packed as rows (row r =
 // node r / G, head kvh * G + r % G); larger groups take several CTAs, adjacent
 // in the grid so they share each K/V tile through L2.  Keys come in tiles of
-// 128: the QK^T MMA is then N = 128 wide, which balances its shared-memory
-// operand traffic (A and B 4 KB each per K-step) against tensor time.  Roles:
+// 128 (the QK^T MMA is N = 128 wide).  Roles:
 //   warps 0, 2  lane 0 of warp 0 streams 128-key K tiles and lane 0 of warp 2
 //               V tiles by TMA, each into its own 3-stage ring, starting at once,
-//               and asks L2 for tiles further on so each shared-memory load waits
-//               on L2 rather than DRAM;
-//   warps 1-7   first stage Q in shared memory (128B-swizzled, K-major);
-//   warp 1      owns TMEM (S: two 128-column fp32 buffers; P: two 64-column
-//               bf16-pair buffers; O: 128 columns = all 512) and one thread
-//               issues the MMAs: S = Q K^T (M=128, N=128, K=16, both operands
-//               K-major) and O += P V (M=128, N=128, P read from TMEM, V an
-//               MN-major shared-memory operand).  The QK^T of tile j+2 goes out
-//               as soon as the softmax has read S of tile j, so it overlaps the
-//               whole softmax of tile j; the PV of tile j follows its P.
-//   warps 4-7   softmax: one thread per row reads its 128 scores from TMEM,
-//               applies the tree mask,
-//               keeps a running (reference max, sum) in the exp2 domain, and
-//               writes P = 2^(s - max) as packed bf16 into its P buffer in
-//               TMEM, where the PV MMA reads it.
-// The output accumulator is rescaled (TMEM
-// load / store) only when a row maximum grows by more than 2^8, otherwise the
-// stale reference is kept; every P and the final O / l use the same reference,
-// so the result is exact up to rounding.  Every wait is bounded.
+//               and asks L2 for tiles further on;
+//   warp 1      owns TMEM (S: two 128-column fp32 buffers, P written as bf16
+//               pairs over the first 64 columns of its S buffer; O: 128 columns;
+//               Q: 64 columns of bf16 pairs) and one thread issues the MMAs:
+//               S = Q K^T (M=128, N=128, K=16; Q read from TMEM, K a K-major
+//               shared-memory operand) and O += P V (P read from TMEM, V an
+//               MN-major shared-memory operand), each as soon as its operands
+//               are in, so a late K tile never holds back a PV or the reverse;
+//   warps 4-7   softmax: one thread per query row; each first parks its row of Q
+//               in TMEM, then per tile reads its 128 scores from TMEM, applies the
+//               tree mask, keeps a running (reference max, sum) in the exp2
+//               domain, and writes P = 2^(s - max) as packed bf16 over the scores,
+//               where the PV MMA reads it.
+// Keeping Q in TMEM leaves the shared-memory bandwidth to the TMA writes and
+// the K / V operand reads.  The output accumulator is rescaled (TMEM load /
+// store) only when a row maximum grows by more than 2^8, otherwise the stale
+// reference is kept; every P and the final O / l use the same reference, so the
+// result is exact up to rounding.  Every wait is bounded.
 //
 // Barrier protocol: each barrier completes once per tile (or once per two
 // tiles when indexed by tile parity); a waiter is never more than one
 // completion behind, so a single phase bit identifies the completion it wants.
 //   k_full/k_empty[t % 3], v_full/v_empty[t % 3]   TMA rings (32 KB stages)
-//   s_free[j%2]              S of tile j read     (softmax -> MMA)
-// and (tile % 2, (tile / 2) & 1) names a completion of the tile-parity barriers.
+//   q_full                   Q parked in TMEM      (softmax warps -> MMA)
+// and (tile % 2, (tile / 2) & 1) names a completion of the tile-parity barriers:
 //   s_full[j%2]              QK^T of tile j done  (MMA -> softmax)
-//   p_full[j%2]              P of tile j in TMEM  (softmax -> MMA); the softmax
-//                            runs at most one tile ahead of the MMA thread
-//   pv_done[j%2]             PV of tile j done    (MMA -> softmax); the softmax
-//                            waits for tile j-2 each tile and for tile j-1 only
-//                            before rescaling O
+//   p_full[j%2]              P of tile j in TMEM  (softmax -> MMA)
+//   pv_done[j%2]             PV of tile j done    (MMA -> MMA, before QK^T of
+//                            tile j+2 overwrites that buffer; MMA -> softmax,
+//                            before O is rescaled or read)
 #pragma once
 
 #include "common.cuh"
@@ -54,18 +51,17 @@ namespace attn_tc {
 constexpr int TBN = 128;                          // keys per tile
 constexpr int KSTAGES = 3;                        // K ring
 constexpr int VSTAGES = 3;                        // V ring
-static_assert(KSTAGES == VSTAGES, "one producer loop serves both rings");
 constexpr int kPrefetch = 3;                      // L2 prefetch distance beyond each ring
 constexpr int NSBUF = 2;                          // S and P buffers in TMEM
 constexpr int ROWS_PER_CTA = 128;                 // one M-tile
-constexpr int Q_BYTES = 128 * kHeadDim * 2;       // 32 KB: two 64-column boxes of 16 KB
 constexpr int KV_BOX_BYTES = TBN * 64 * 2;        // 16 KB: 128 keys x 64 dims
 constexpr int K_BYTES = 2 * KV_BOX_BYTES;         // 32 KB (one K or V tile)
-constexpr int SMEM_BYTES = Q_BYTES + (KSTAGES + VSTAGES) * K_BYTES + 2048;
+constexpr int SMEM_BYTES = (KSTAGES + VSTAGES) * K_BYTES + 2048;
 constexpr int kThreads = 256;                     // warps 0-3 roles, 4-7 softmax
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: S[buf] at buf * 128, P[buf] (bf16 pairs) at 256 + buf * 64, O at 384
-constexpr uint32_t S_COL0 = 0, P_COL0 = 256, O_COL0 = 384;
+// TMEM columns: S[buf] at buf * 128 (P[buf], bf16 pairs, is written over the first 64
+// columns of S[buf]), O at 256, Q (bf16 pairs) at 384
+constexpr uint32_t S_COL0 = 0, O_COL0 = 256, Q_COL0 = 384;
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, TBN, 0, 0);
@@ -89,7 +85,7 @@ struct Bars {
     uint64_t v_full[VSTAGES];
     uint64_t v_empty[VSTAGES];
     uint64_t s_full[NSBUF];          // [tile parity]
-    uint64_t s_free[NSBUF];
+    uint64_t q_full;
     uint64_t p_full[NSBUF];
     uint64_t pv_done[NSBUF];
     uint64_t drain;
@@ -123,8 +119,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem;                                   // 32 KB
-    uint8_t* sK = sQ + Q_BYTES;                           // [KSTAGES][32 KB]
+    uint8_t* sK = smem;                                   // [KSTAGES][32 KB]
     uint8_t* sV = sK + KSTAGES * K_BYTES;                 // [VSTAGES][32 KB]
     Bars* bars = reinterpret_cast<Bars*>(sV + VSTAGES * K_BYTES);
     volatile int* abort_flag = &bars->abort_flag;
@@ -136,6 +131,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int n = a.n, G = a.G, rows = n * G;
     const int row0 = rg * ROWS_PER_CTA;
     const int L = a.kv_len[b];
+    // softmax threads: this thread's query row (bf16 pairs), loaded now, parked in TMEM later
+    uint4 qrow[kHeadDim / 8];
+    if (warp >= 4) {
+        const int r = row0 + (warp & 3) * 32 + lane;
+#pragma unroll
+        for (int u = 0; u < kHeadDim / 8; ++u) qrow[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + (((int64_t)b * n + r / G) * a.Hq + kvh * G + r % G) * kHeadDim);
+#pragma unroll
+            for (int u = 0; u < kHeadDim / 8; ++u) qrow[u] = __ldg(src + u);
+        }
+    }
 
     if (tid == 0) {
         int err = 0;
@@ -160,11 +168,11 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         for (int p = 0; p < NSBUF; ++p) {
             mbar_init(s32(&bars->s_full[p]), 1);
-            mbar_init(s32(&bars->s_free[p]), 4);
             mbar_init(s32(&bars->p_full[p]), 4);
             mbar_init(s32(&bars->pv_done[p]), 1);
         }
         mbar_init(s32(&bars->drain), 1);
+        mbar_init(s32(&bars->q_full), 4);
         bars->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
@@ -185,35 +193,22 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int T = err ? 0 : (ke - kb + TBN - 1) / TBN;
     const int kvrow0 = (b * a.Hkv + kvh) * a.Lmax;
 
-    // ---- Q -> shared memory (warps 1-7, while warp 0 already streams K/V) ----
-    if (warp > 0) {
-        // all of a thread's 16-byte pieces are loaded before any is stored, so the
-        // tile costs one memory round trip rather than one per piece
-        constexpr int kLoaders = kThreads - 32;
-        constexpr int kPieces = ROWS_PER_CTA * 16;
-        constexpr int kPer = (kPieces + kLoaders - 1) / kLoaders;
-        uint4 v[kPer];
+    // ---- Q -> TMEM (softmax warps, one lane = one row), while K/V already stream ----
+    if (warp >= 4) {
+        const uint32_t qaddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + Q_COL0;
+        uint32_t w[32];
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int c = tid - 32 + u * kLoaders;
-            const int r = row0 + (c >> 4);
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (c < kPieces && r < rows) {
-                const int i = r / G, g = r % G;
-                v[u] = __ldg(reinterpret_cast<const uint4*>(
-                             a.q + (((int64_t)b * n + i) * a.Hq + kvh * G + g) * kHeadDim) + (c & 15));
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint4 v = qrow[8 * h + u];
+                w[4 * u] = v.x; w[4 * u + 1] = v.y; w[4 * u + 2] = v.z; w[4 * u + 3] = v.w;
             }
+            tmem_st32(qaddr + 32 * h, w);
         }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int c = tid - 32 + u * kLoaders;
-            if (c >= kPieces) continue;
-            const int rr = c >> 4, c16 = c & 15;
-            uint8_t* box = sQ + (c16 >> 3) * (Q_BYTES / 2);
-            *reinterpret_cast<uint4*>(box + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4)) = v[u];
-        }
-        fence_proxy_async_smem();
-        asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads - 32) : "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s32(&bars->q_full));
     }
 
     if (warp == 0 || warp == 2) {
@@ -225,7 +220,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             uint8_t* ring = isK ? sK : sV;
             uint64_t* full = isK ? bars->k_full : bars->v_full;
             uint64_t* empty = isK ? bars->k_empty : bars->v_empty;
-            constexpr int NS = KSTAGES;   // == VSTAGES
+            const int NS = isK ? KSTAGES : VSTAGES;
             for (int t = 0; t < T; ++t) {
                 const int st = t % NS;
                 if (!mbar_wait(s32(&empty[st]), (((uint32_t)t / NS) & 1u) ^ 1u, abort_flag)) break;
@@ -253,26 +248,23 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             // Descriptors are built once; every operand below differs from its base
             // only in the 14-bit start-address field (all addresses < 256 KB), so an
             // MMA costs two adds.  Offsets are compile-time constants after unrolling.
-            const uint64_t dQ = sw128_desc(s32(sQ));
             const uint64_t dK0 = sw128_desc(s32(sK));
             const uint64_t dV0 = sw128_desc_mn(s32(sV), KV_BOX_BYTES, 1024);
             const uint32_t ocol = tmem + O_COL0;
-            auto issue_qk = [&](int j) {     // S[j % 2] = Q K_j^T; frees K stage j
+            auto issue_qk = [&](int j) {     // S[j % 2] = Q K_j^T (Q from TMEM); frees K stage j
                 const uint64_t dk = dK0 + (uint64_t)(((j % KSTAGES) * K_BYTES) >> 4);
                 const uint32_t scol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
 #pragma unroll
-                for (int k = 0; k < kHeadDim / 16; ++k) {
-                    const uint32_t off = (k >> 2) * (Q_BYTES / 2) + (k & 3) * 32;
-                    umma_f16(scol, dQ + (uint64_t)(off >> 4),
-                             dk + (uint64_t)((((k >> 2) * KV_BOX_BYTES) + (k & 3) * 32) >> 4),
-                             kIdescQK, k > 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < kHeadDim / 16; ++k)   // 16 dims = 8 packed TMEM columns
+                    umma_f16_ts(scol, tmem + Q_COL0 + k * 8,
+                                dk + (uint64_t)((((k >> 2) * KV_BOX_BYTES) + (k & 3) * 32) >> 4),
+                                kIdescQK, k > 0 ? 1u : 0u);
                 umma_commit(s32(&bars->s_full[j % NSBUF]));
                 umma_commit(s32(&bars->k_empty[j % KSTAGES]));
             };
             auto issue_pv = [&](int j) {     // O += P[j % 2] V_j; frees V stage j
                 const uint64_t dv = dV0 + (uint64_t)(((j % VSTAGES) * K_BYTES) >> 4);
-                const uint32_t pcol = tmem + P_COL0 + (uint32_t)((j % NSBUF) * (TBN / 2));
+                const uint32_t pcol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
                 const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
                 for (int k = 0; k < TBN / 16; ++k)   // 16 keys = 8 packed TMEM columns
@@ -286,15 +278,15 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tc_fence_after();
                 return true;
             };
-            bool ok = true;
+            bool ok = wait_on(&bars->q_full, 0u);
             for (int j = 0; ok && j < min(T, NSBUF); ++j) {
                 ok = wait_on(&bars->k_full[j % KSTAGES], ((uint32_t)j / KSTAGES) & 1u);
                 if (ok) issue_qk(j);
             }
-            // Issue whichever is ready first: QK^T of tile js (its S buffer read by the
-            // softmax of tile js-2, its K tile landed) or PV of tile jp (its P written,
-            // its V tile landed), so a late K tile never holds back a PV and its V
-            // stage, and a late P never holds back the next scores.  Each completion
+            // Issue whichever is ready first: QK^T of tile js (its S buffer, which held
+            // P of tile js-2, consumed by that tile's PV; its K tile landed) or PV of
+            // tile jp (its P written, its V tile landed), so a late K tile never holds
+            // back a PV and its V stage, and a late P never holds back the next scores.  Each completion
             // tested is the next one of its barrier, so one parity bit names it.
             int js = min(T, NSBUF), jp = 0;
             long long t_last = clock64();
@@ -302,7 +294,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             while (ok && jp < T) {
                 bool progressed = false;
                 if (js < T &&
-                    mbar_try_wait(s32(&bars->s_free[js % NSBUF]), ((uint32_t)(js - NSBUF) / NSBUF) & 1u) &&
+                    mbar_try_wait(s32(&bars->pv_done[js % NSBUF]), ((uint32_t)(js - NSBUF) / NSBUF) & 1u) &&
                     mbar_try_wait(s32(&bars->k_full[js % KSTAGES]), ((uint32_t)js / KSTAGES) & 1u)) {
                     tc_fence_after();
                     issue_qk(js++);
@@ -335,7 +327,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const unsigned long long anc = valid ? bars->anc[i] : 0ull;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const uint32_t s_addr0 = tmem + lane_base + S_COL0;
-        const uint32_t p_addr0 = tmem + lane_base + P_COL0;
         const uint32_t o_addr = tmem + lane_base + O_COL0;
         const float sc = a.scale_log2;
         float mref = -INFINITY, l = 0.f;
@@ -353,10 +344,6 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 tmem_ld32_nowait(s_addr + 64, u2);
                 tmem_ld32_nowait(s_addr + 96, u3);
                 asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-                // the scores are in registers: let the MMA reuse this S buffer
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s32(&bars->s_free[j % NSBUF]));
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     x[c] = __uint_as_float(u0[c]);
@@ -402,14 +389,9 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 mref = mx;
                 l *= alpha;
             }
-            // PV of tile j-2 is long done (the one completion pending on this barrier);
-            // waiting keeps the phase bookkeeping exact.  PV of tile j-1 is awaited
-            // only before the output accumulator is rescaled.
-            if (j >= NSBUF) {
-                got = mbar_wait(s32(&bars->pv_done[j % NSBUF]), ((uint32_t)(j - NSBUF) / NSBUF) & 1u,
-                                abort_flag);
-                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            }
+            // P of tile j goes over S of tile j, whose MMA was issued after the PV of
+            // tile j-2 had finished with that buffer.  PV of tile j-1 is awaited only
+            // before the output accumulator is rescaled.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 got = mbar_wait(s32(&bars->pv_done[(j - 1) % NSBUF]), ((uint32_t)(j - 1) / NSBUF) & 1u,
                                 abort_flag);
@@ -436,7 +418,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     ps[e & 3] += p0 + p1;
                     pk[e] = pack2(p0, p1);
                 }
-                tmem_st32(p_addr0 + (uint32_t)((j % NSBUF) * (TBN / 2) + 32 * h), pk);   // P, bf16 pairs
+                tmem_st32(s_addr + (uint32_t)(32 * h), pk);   // P, bf16 pairs, over S
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             tc_fence_before();

@@ -537,7 +537,7 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
-KERNEL_CASES = ("gemm", "topk", "attn", "verify", "compact", "softmax")
+KERNEL_CASES = ("gemm", "topk", "fused", "attn", "verify", "compact", "softmax")
 
 
 def kernel_case(name, reps):
@@ -547,6 +547,9 @@ def kernel_case(name, reps):
       gemm     LM-head GEMM of one full level: 640 x 4096 -> 128256
       topk     expansion levels 1-2 over [64, 71, 128256] draft logits: the level-2
                launch is the full 640-row top-10
+      fused    expansion levels 1-2 from hidden states, as the step runs them: GEMM
+               with per-tile (max, sum) partials, then the top-k merge that rescans
+               only the tiles able to hold a row's top-10
       attn     tree attention, one layer, B=64, 32/8 heads, KV 4096, 60 nodes
       verify   verify-and-accept, B=32, 60 nodes, V=128256, T=1
       compact  KV compaction, 32 layers, B=4 (8 kv heads, Lmax 4156)
@@ -589,6 +592,18 @@ def kernel_case(name, reps):
         def fn():
             for lvl in (1, 2):
                 E.eagle2_expand(lvl, 0, logits, c.top_k, c.depth, c.n, state, dev_status=st)
+    elif name == "fused":
+        B, k = c.B, c.top_k
+        w = normal((c.V, c.H), c.w_std, torch.bfloat16)
+        hid = [normal((B, 1 if lvl == 1 else k, c.H), 1.0, torch.bfloat16) for lvl in (1, 2)]
+        logits = torch.empty(B, c.R, c.V, device=dev)
+        state = torch.empty(E.tree_state_size(B, k, c.depth), dtype=torch.uint8, device=dev)
+        part = torch.empty(E.expand_scratch_size(B, c.V, k) // 4, device=dev)
+
+        def fn():
+            for lvl in (1, 2):
+                E.eagle2_expand(lvl, 0, logits, k, c.depth, c.n, state, hidden=hid[lvl - 1],
+                                lm_head_w=w, partials=part, dev_status=st)
     elif name == "attn":
         B = c.B
         _, _, _, par, _ = expanded(8)

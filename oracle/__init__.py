@@ -168,6 +168,37 @@ def verify_accept(target, draft, tokens, parent, max_depth: int, T: float, seed:
     return out
 
 
+def d2t_scatter(draft, d2t, V: int):
+    """Draft logits over a draft vocabulary of Vd tokens, f32 [..., Vd], placed in the
+    target vocabulary of V tokens: draft id d sits at target id d + d2t[d], and every
+    target id no draft id maps to gets -inf (probability 0).  This is what the draft
+    distribution p is, as a function of target tokens, when the draft head has its own
+    smaller vocabulary and the table d2t (int [Vd]) maps its outputs back (Guide,
+    "EAGLE-3：取消特征约束…": the draft head ranks its own candidates and the table
+    returns them to target ids).  The map must be one-to-one into [0, V)."""
+    x = np.asarray(draft, np.float32)
+    d2t = np.asarray(d2t, np.int64)
+    Vd = x.shape[-1]
+    assert d2t.shape == (Vd,)
+    tgt_id = np.arange(Vd) + d2t
+    assert tgt_id.min() >= 0 and tgt_id.max() < V, "d2t maps outside the target vocabulary"
+    assert np.unique(tgt_id).size == Vd, "d2t maps two draft ids to one target id"
+    full = np.full(x.shape[:-1] + (V,), -np.inf, np.float32)
+    full[..., tgt_id] = x
+    return full
+
+
+def verify_accept_d2t(target, draft, d2t, tokens, parent, max_depth: int, T: float, seed: int,
+                      draft_row=None, u_override=None):
+    """verify_accept with draft rows over the draft vocabulary (f32 [B, R, Vd]) and the
+    draft-to-target table d2t (int [Vd]); tokens are target ids.  p over the target
+    vocabulary is the draft softmax at ids d + d2t[d] and 0 elsewhere (d2t_scatter);
+    the walk is then the one of verify_accept, unchanged."""
+    V = np.asarray(target).shape[-1]
+    return verify_accept(target, d2t_scatter(draft, d2t, V), tokens, parent, max_depth, T, seed,
+                         draft_row=draft_row, u_override=u_override)
+
+
 def sample_rows(logits, T: float, seed: int):
     """One token per row of logits [B, rows, V] from softmax(row / T) (argmax at T = 0)."""
     x = _c(logits, np.float32)
@@ -322,16 +353,24 @@ class Eagle2Tree:
                     value=values)
 
 
-def eagle2_from_logits(logits, top_k: int, depth: int, n_out: int, root_tokens=None):
-    """Whole expansion + rerank from per-row draft logits f32 [B, R, V] (R = draft_rows)."""
+def eagle2_from_logits(logits, top_k: int, depth: int, n_out: int, root_tokens=None, d2t=None):
+    """Whole expansion + rerank from per-row draft logits f32 [B, R, V] (R = draft_rows).
+    With d2t (int [V]), the rows are over a draft vocabulary and each chosen draft id d
+    enters the tree as the target id d + d2t[d]; the ranking (top-k by logit, ties to the
+    lower draft id) and the values are those of the draft vocabulary."""
     x = _c(logits, np.float32)
     B, R, V = x.shape
     assert R >= draft_rows(top_k, depth)
+    if d2t is not None:
+        d2t = np.asarray(d2t, np.int64)
+        assert d2t.shape == (V,)
     trees = [Eagle2Tree(top_k, depth) for _ in range(B)]
     for lvl in range(1, depth + 1):
         off = level_row_offset(lvl, top_k)
         k_in = 1 if lvl == 1 else top_k
         tok, conf, st = row_topk(x[:, off:off + k_in], top_k)
+        if d2t is not None:
+            tok = (tok + d2t[tok]).astype(np.int32)
         for b in range(B):
             trees[b].expand(tok[b], conf[b].astype(np.float32))
     outs = [t.rerank(n_out, -1 if root_tokens is None else int(root_tokens[b]))

@@ -148,3 +148,20 @@ def test_kv_compact_skips_failed_sequences_and_checks_capacity():
     path = np.array([[0, 1, -1, -1], [0, 3, -1, -1]], np.int32)
     st = oracle.kv_compact(k, v, kv_len, path, np.array([-1, 1], np.int32), D)
     assert st == oracle.ORC_CAPACITY and list(kv_len) == [2, 6]
+
+
+def test_eagle2_with_d2t_maps_tokens_and_keeps_the_tree():
+    """A draft vocabulary: the tree (parents, values, draft rows) is the one the draft
+    ids give, and each node's token is its draft id's target id d + d2t[d]."""
+    B, k, D, n_out, Vd, V = 3, 4, 3, 10, 40, 100
+    R = oracle.draft_rows(k, D)
+    g = W.rng(3, 46)
+    logits = g.normal(0, 2, size=(B, R, Vd)).astype(np.float32)
+    ids = np.sort(g.choice(V, size=Vd, replace=False))
+    d2t = (ids - np.arange(Vd)).astype(np.int32)
+    plain = oracle.eagle2_from_logits(logits, k, D, n_out)
+    mapped = oracle.eagle2_from_logits(logits, k, D, n_out, d2t=d2t)
+    for key in ("parent", "draft_row", "cand", "value"):
+        assert np.array_equal(plain[key], mapped[key])
+    assert (mapped["tokens"][:, 0] == -1).all()
+    assert np.array_equal(mapped["tokens"][:, 1:], ids[plain["tokens"][:, 1:]])

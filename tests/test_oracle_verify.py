@@ -300,3 +300,107 @@ def test_tree_222_exact_enumeration():
 def test_random_small_trees_exact_enumeration(seed):
     parent = W.random_tree(7, 4, seed)
     _monte_carlo_vs_exact(parent, V=8, seed=seed, B=100_000)
+
+
+# ------------------------------------------------------------------ draft vocabulary (d2t)
+def _d2t_case(V, Vd, seed):
+    """A one-to-one draft-to-target table: Vd distinct target ids, d2t[d] = id - d."""
+    g = W.rng(seed, 41)
+    ids = np.sort(g.choice(V, size=Vd, replace=False))
+    return (ids - np.arange(Vd)).astype(np.int32), ids
+
+
+def test_d2t_scatter_places_draft_probabilities_at_target_ids():
+    """p(t) over the target vocabulary is the draft softmax at t = d + d2t[d], 0 elsewhere."""
+    V, Vd = 11, 5
+    d2t, ids = _d2t_case(V, Vd, 1)
+    row = W.rng(1, 42).normal(0, 1, size=(2, 3, Vd)).astype(np.float32)
+    full = oracle.d2t_scatter(row, d2t, V)
+    for i in range(2):
+        for j in range(3):
+            pf = _softmax(full[i, j])
+            pd = _softmax(row[i, j])
+            assert np.allclose(pf[ids], pd, rtol=1e-14, atol=0)
+            mask = np.ones(V, bool)
+            mask[ids] = False
+            assert (pf[mask] == 0).all()
+
+
+def test_d2t_identity_table_is_the_full_vocabulary_walk():
+    B, n, V = 64, 9, 16
+    g = W.rng(9, 43)
+    parent = W.random_tree(n, 4, 9)
+    tgt = g.normal(0, 1.5, size=(B, n, V)).astype(np.float32)
+    drf = (tgt + g.normal(0, 1.0, size=(B, n, V))).astype(np.float32)
+    tok = np.broadcast_to(g.integers(0, V, size=n, dtype=np.int32), (B, n)).copy()
+    tok[:, 0] = -1
+    par = np.broadcast_to(parent, (B, n))
+    D = int(oracle.tree_check(parent)[1].max())
+    a = oracle.verify_accept(tgt, drf, tok, par, max_depth=D, T=1.0, seed=5)
+    b = oracle.verify_accept_d2t(tgt, drf, np.zeros(V, np.int32), tok, par, max_depth=D, T=1.0,
+                                 seed=5)
+    for key in ("accept_len", "path", "emit", "status"):
+        assert np.array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("seed", [4, 5])
+def test_d2t_tree_walk_exact_enumeration(seed):
+    """Draft rows over a draft vocabulary of 5 ids mapped into V = 8 target ids: every
+    drafted token is a draft id's target, p is zero on the 3 target ids outside the
+    table, and the (accepted path, final token) law is the exact recursion's with p in
+    target space (the rule stays lossless: the first emitted token is still ~ q)."""
+    V, Vd, B = 8, 5, 100_000
+    d2t, ids = _d2t_case(V, Vd, seed)
+    parent = W.random_tree(6, 3, seed)
+    n = len(parent)
+    g = W.rng(seed, 44)
+    tgt_rows = g.normal(0, 1.5, size=(n, V)).astype(np.float32)
+    drf_rows = g.normal(0, 1.5, size=(n, Vd)).astype(np.float32)
+    tokens = np.full(n, -1, np.int32)
+    for v in range(n):
+        kids = _children(parent, v)
+        if kids:
+            tokens[kids] = ids[g.choice(Vd, size=len(kids), replace=False)]
+    q_rows = [_softmax(r) for r in tgt_rows]
+    p_rows = [_softmax(r) for r in oracle.d2t_scatter(drf_rows, d2t, V)]
+    exact = exact_outcomes(q_rows, p_rows, tokens, parent)
+    assert abs(sum(exact.values()) - 1.0) < 1e-12
+    D = int(oracle.tree_check(parent)[1].max())
+    res = oracle.verify_accept_d2t(np.broadcast_to(tgt_rows, (B, n, V)),
+                                   np.broadcast_to(drf_rows, (B, n, Vd)), d2t,
+                                   np.broadcast_to(tokens, (B, n)), np.broadcast_to(parent, (B, n)),
+                                   max_depth=max(D, 1), T=1.0, seed=seed)
+    assert (res["status"] == 0).all()
+    keys = list(exact)
+    index = {k: i for i, k in enumerate(keys)}
+    counts = np.zeros(len(keys))
+    for b in range(B):
+        a = res["accept_len"][b]
+        key = (tuple(int(x) for x in res["path"][b, :a + 1]), int(res["emit"][b, a]))
+        assert key in index, key
+        counts[index[key]] += 1
+    probs = np.array([exact[k] for k in keys])
+    small = probs * B < 5
+    c = np.append(counts[~small], counts[small].sum())
+    pr = np.append(probs[~small], probs[small].sum())
+    assert _chisq_pvalue(c, pr) > 1e-4
+
+
+def test_d2t_leviathan_chisquare_v8():
+    """Losslessness with a draft vocabulary: drafts d ~ p over 5 draft ids, mapped to
+    target ids, 50,000 one-draft steps on V = 8; the emitted token is distributed as q
+    (including the 3 target ids p never proposes)."""
+    V, Vd, B = 8, 5, 50_000
+    d2t, ids = _d2t_case(V, Vd, 7)
+    g = W.rng(7, 45)
+    q = g.dirichlet(np.ones(V))
+    pd = g.dirichlet(np.ones(Vd))
+    tgt = np.broadcast_to(_logits(q), (B, 2, V))
+    drf = np.broadcast_to(_logits(pd), (B, 2, Vd))
+    tok = np.full((B, 2), -1, np.int32)
+    tok[:, 1] = ids[g.choice(Vd, size=B, p=pd)]
+    par = np.broadcast_to(W.chain_tree(2), (B, 2))
+    res = oracle.verify_accept_d2t(tgt, drf, d2t, tok, par, max_depth=1, T=1.0, seed=77)
+    assert (res["status"] == 0).all()
+    first = res["emit"][:, 0]
+    assert _chisq_pvalue(np.bincount(first, minlength=V), _softmax(_logits(q))) > 1e-3

@@ -99,16 +99,31 @@ def eagle_tree_attn(q, k_cache, v_cache, kv_len, parent, scale=None, out=None, w
     return out
 
 
+def eagle_d2t_inverse(d2t, V, t2d=None, dev_status=None, stream=None):
+    """t2d int32 [V]: the draft id of each target id (d + d2t[d] -> d), -1 where none."""
+    _dev(d2t, "d2t", torch.int32)
+    t2d = torch.empty(V, dtype=torch.int32, device=d2t.device) if t2d is None else t2d
+    _dev(t2d, "t2d", torch.int32)
+    _check("eagle_d2t_inverse", lib().eagle_d2t_inverse(
+        _ptr(d2t), d2t.numel(), int(V), _ptr(t2d), _ptr(_status(dev_status, d2t.device)),
+        _stream(stream)))
+    return t2d
+
+
 def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, temperature, seed,
                         draft_row=None, accept_len=None, path=None, emit=None, row_stats=None,
-                        dev_status=None, stream=None):
-    """Returns (accept_len [B], path [B,D+1], emit [B,D+1]) int32 tensors."""
+                        dev_status=None, stream=None, t2d=None):
+    """Returns (accept_len [B], path [B,D+1], emit [B,D+1]) int32 tensors.  With t2d
+    (from eagle_d2t_inverse) the draft rows are over the draft vocabulary
+    [B, R, Vd] and tokens are target ids."""
     _dev(target_logits, "target_logits", torch.float32)
     B, n, V = target_logits.shape
     R = n
+    Vd = V
     if draft_logits is not None:
         _dev(draft_logits, "draft_logits", torch.float32)
         R = draft_logits.shape[1]
+        Vd = draft_logits.shape[2]
     _dev(tokens, "tokens", torch.int32)
     _dev(parent, "parent", torch.int32)
     if draft_row is not None:
@@ -120,6 +135,16 @@ def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, 
     emit = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if emit is None else emit
     if row_stats is not None:
         _dev(row_stats, "row_stats", torch.float32)
+    if t2d is not None:
+        _dev(t2d, "t2d", torch.int32)
+        _check("eagle_verify_accept_d2t", lib().eagle_verify_accept_d2t(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_row), _ptr(tokens), _ptr(parent),
+            B, n, V, R, Vd, _ptr(t2d), D, float(temperature), int(seed) & (2**64 - 1),
+            _ptr(accept_len), _ptr(path), _ptr(emit), _ptr(row_stats),
+            _ptr(_status(dev_status, dev)), _stream(stream)))
+        return accept_len, path, emit
+    if draft_logits is not None and Vd != V:
+        raise ValueError("draft rows over another vocabulary need t2d")
     _check("eagle_verify_accept", lib().eagle_verify_accept(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_row), _ptr(tokens), _ptr(parent),
         B, n, V, R, D, float(temperature), int(seed) & (2**64 - 1),
@@ -149,12 +174,13 @@ def expand_scratch_size(B, V, top_k) -> int:
 
 def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=None,
                   lm_head_w=None, out_tokens=None, out_parent=None, out_draft_row=None,
-                  frontier_tokens=None, dev_status=None, stream=None, partials=None):
+                  frontier_tokens=None, dev_status=None, stream=None, partials=None, d2t=None):
     """One EAGLE-2 level over draft-logit storage logits [B, R, V] (f32).  With a
     partials buffer the level's statistics come from the GEMM epilogue's per-tile
     partials (written by this call's GEMM when hidden is given, else by a prior
     eagle_lmhead_gemm(..., partials=...) for the level's rows) and its top-k from a
-    rescan of the few tiles that can hold it."""
+    rescan of the few tiles that can hold it.  With d2t (int32 [V]) V is a draft
+    vocabulary and the tokens written are target ids d + d2t[d]."""
     _dev(logits, "logits", torch.float32)
     _dev(tree_state, "tree_state")
     B, R, V = logits.shape
@@ -172,6 +198,16 @@ def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=
     if partials is not None:
         _dev(partials, "partials", torch.float32)
         sbytes = partials.numel() * partials.element_size()
+    if d2t is not None:
+        _dev(d2t, "d2t", torch.int32)
+        if d2t.numel() != V:
+            raise ValueError("d2t needs one entry per draft id")
+        _check("eagle2_expand_d2t", lib().eagle2_expand_d2t(
+            int(level), int(final), _ptr(hidden), _ptr(lm_head_w), _ptr(logits), B, H, V, top_k,
+            depth, n_out, _ptr(tree_state), nbytes, _ptr(partials), sbytes, _ptr(d2t),
+            _ptr(out_tokens), _ptr(out_parent), _ptr(out_draft_row), _ptr(frontier_tokens),
+            _ptr(_status(dev_status, logits.device)), _stream(stream)))
+        return
     _check("eagle2_expand", lib().eagle2_expand(
         int(level), int(final), _ptr(hidden), _ptr(lm_head_w), _ptr(logits), B, H, V, top_k, depth,
         n_out, _ptr(tree_state), nbytes, _ptr(partials), sbytes, _ptr(out_tokens), _ptr(out_parent),

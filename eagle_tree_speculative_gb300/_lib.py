@@ -23,11 +23,16 @@ SIGNATURES = {
     "eagle_tree_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
     "eagle_verify_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _U64, _P, _P, _P, _P,
                                  _P, _P]),
+    "eagle_d2t_inverse": (_I, [_P, _I, _I, _P, _P, _P]),
+    "eagle_verify_accept_d2t": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _F, _U64, _P,
+                                     _P, _P, _P, _P, _P]),
     "eagle_kv_compact": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "eagle2_tree_state_size": (_SZ, [_I, _I, _I]),
     "eagle2_expand_scratch_size": (_SZ, [_I, _I, _I]),
     "eagle2_expand": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _SZ, _P, _P, _P,
                            _P, _P, _P]),
+    "eagle2_expand_d2t": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _SZ, _P, _P,
+                               _P, _P, _P, _P, _P]),
     "eagle2_expand_static_state": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _P, _P]),
     "eagle_softmax_stats": (_I, [_P, _I64, _I, _F, _P, _P, _P, _P, _P]),

@@ -505,7 +505,7 @@ constexpr int kSelectThreads = 256;
 
 __global__ void __launch_bounds__(kSelectThreads)
 select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t* frontier_tokens,
-              int32_t* dev_status) {
+              const int32_t* d2t, int32_t* dev_status) {
     __shared__ float s_val[kKMax * kKMax];
     __shared__ int s_id[kKMax * kKMax];
     __shared__ float s_conf[kKMax * kKMax];     // [row s][rank j]: confidence of the row's j-th best
@@ -566,7 +566,8 @@ select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t
         const float val = __fmul_rn(st.value[par], s_conf[s * kKMax + j]);
         st.value[id] = val;
         st.parent[id] = par;
-        st.token[id] = s_tok[s * kKMax + j];
+        const int tk = s_tok[s * kKMax + j];            // id in the logits' vocabulary
+        st.token[id] = d2t ? tk + d2t[tk] : tk;         // draft id -> target id
         st.depth[id] = level;
         st.row[id] = -1;
         s_val[e] = val;
@@ -680,13 +681,14 @@ extern "C" size_t eagle2_expand_scratch_size(int B, int V, int top_k) {
     return (size_t)B * top_k * tiles * 2 * 4u;
 }
 
-extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
-                                      const void* lm_head_w, float* logits, int B, int H, int V,
-                                      int top_k, int depth, int n_out, void* tree_state,
-                                      size_t state_bytes, float* partials, size_t partials_bytes,
-                                      int32_t* out_tokens, int32_t* out_parent,
-                                      int32_t* out_draft_row, int32_t* frontier_tokens,
-                                      int32_t* dev_status, eagle_stream_t stream) {
+namespace eagle {
+namespace {
+eagle_status expand_common(int level, int final, const void* hidden, const void* lm_head_w,
+                           float* logits, int B, int H, int V, int top_k, int depth, int n_out,
+                           void* tree_state, size_t state_bytes, float* partials,
+                           size_t partials_bytes, const int32_t* d2t, int32_t* out_tokens,
+                           int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
+                           int32_t* dev_status, eagle_stream_t stream) {
     if (B < 0 || V < 1 || top_k < 1 || depth < 1 || level < 1 || level > depth || !logits ||
         !tree_state)
         return EAGLE_ERR_INVALID_ARG;
@@ -731,7 +733,7 @@ extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
     }
     EAGLE_CHECK_LAUNCH();
     select_kernel<<<B, kSelectThreads, 0, s>>>(level, final, top_k, depth, nseg, tree_state,
-                                                 frontier_tokens, dev_status);
+                                                 frontier_tokens, d2t, dev_status);
     EAGLE_CHECK_LAUNCH();
     if (final) {
         const int Cl = StateView::cand_count(top_k, level);
@@ -747,6 +749,35 @@ extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden,
         EAGLE_CHECK_LAUNCH();
     }
     return EAGLE_OK;
+}
+
+}  // namespace
+}  // namespace eagle
+
+extern "C" eagle_status eagle2_expand(int level, int final, const void* hidden, const void* lm_head_w,
+                                      float* logits, int B, int H, int V, int top_k, int depth,
+                                      int n_out, void* tree_state, size_t state_bytes,
+                                      float* partials, size_t partials_bytes, int32_t* out_tokens,
+                                      int32_t* out_parent, int32_t* out_draft_row,
+                                      int32_t* frontier_tokens, int32_t* dev_status,
+                                      eagle_stream_t stream) {
+    return expand_common(level, final, hidden, lm_head_w, logits, B, H, V, top_k, depth, n_out,
+                         tree_state, state_bytes, partials, partials_bytes, nullptr, out_tokens,
+                         out_parent, out_draft_row, frontier_tokens, dev_status, stream);
+}
+
+extern "C" eagle_status eagle2_expand_d2t(int level, int final, const void* hidden,
+                                          const void* lm_head_w, float* logits, int B, int H, int V,
+                                          int top_k, int depth, int n_out, void* tree_state,
+                                          size_t state_bytes, float* partials,
+                                          size_t partials_bytes, const int32_t* d2t,
+                                          int32_t* out_tokens, int32_t* out_parent,
+                                          int32_t* out_draft_row, int32_t* frontier_tokens,
+                                          int32_t* dev_status, eagle_stream_t stream) {
+    if (!d2t) return EAGLE_ERR_INVALID_ARG;
+    return expand_common(level, final, hidden, lm_head_w, logits, B, H, V, top_k, depth, n_out,
+                         tree_state, state_bytes, partials, partials_bytes, d2t, out_tokens,
+                         out_parent, out_draft_row, frontier_tokens, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -40,6 +40,8 @@ struct VerifyArgs {
     int32_t* emit;
     float* row_stats;
     int32_t* dev_status;
+    int Vd;                // draft-row length (= V without a draft vocabulary)
+    const int32_t* t2d;    // target id -> draft id or -1 (draft vocabulary only)
 };
 
 // Softmax statistics of a row at temperature T, kept over the raw logits:
@@ -271,6 +273,62 @@ __device__ __forceinline__ int cta_rank_in_cluster(int cs) {
     return 0;
 }
 
+// The draft logit of target token t.  Without a draft vocabulary the draft row is
+// indexed by target id.  With one (the draft head ranks its own Vd ids, and draft id d
+// stands for target id d + d2t[d]), t2d[t] is the draft id of t or -1, and a target
+// id no draft id maps to has logit -inf: probability 0 under p.
+template <bool D2T>
+struct PRow {
+    const float* p;         // draft row, or nullptr (no draft distribution needed)
+    const int32_t* t2d;
+    __device__ __forceinline__ float at(int d) const { return d >= 0 ? __ldg(p + d) : -INFINITY; }
+    __device__ __forceinline__ float one(int t) const {
+        if (!p) return 0.f;
+        if constexpr (D2T) return at(__ldg(t2d + t));
+        else return __ldg(p + t);
+    }
+    __device__ __forceinline__ float4 four(int t) const {
+        if (!p) return make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (D2T) {
+            const int4 d = __ldg(reinterpret_cast<const int4*>(t2d + t));
+            return make_float4(at(d.x), at(d.y), at(d.z), at(d.w));
+        } else {
+            return __ldg(reinterpret_cast<const float4*>(p + t));
+        }
+    }
+};
+
+// (max, sum) of row[lo, hi) at c = log2(e) / T into S, non-finite entries into bad;
+// 4 float4 in flight per thread on the vector path.
+template <int NT>
+__device__ __forceinline__ void row_stats_slice(const float* row, int lo, int hi, bool vec4, float c,
+                                                RowStat& S, int& bad) {
+    if (vec4) {
+        int t = lo + 4 * (int)threadIdx.x;
+        for (; t + 12 * NT < hi; t += 16 * NT) {
+            float4 r4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) r4[u] = __ldg(reinterpret_cast<const float4*>(row + t + 4 * u * NT));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                bad |= bad4(r4[u]);
+                rs_push4(S, r4[u], c);
+            }
+        }
+        for (; t < hi; t += 4 * NT) {
+            const float4 r4 = __ldg(reinterpret_cast<const float4*>(row + t));
+            bad |= bad4(r4);
+            rs_push4(S, r4, c);
+        }
+    } else {
+        for (int t = lo + (int)threadIdx.x; t < hi; t += NT) {
+            const float l = row[t];
+            bad |= isnan(l) | (l == INFINITY);
+            rs_push1(S, l, c);
+        }
+    }
+}
+
 // E = -ln u' for the race uniform u' = (2 (w >> 9) + 1) 2^-24.  Near u' = 1 (where
 // the race is usually won: E is small) it uses the exact complement
 // v = 1 - u' = (2^24 - 2 (w >> 9) - 1) 2^-24 and the Taylor series of -ln(1 - v),
@@ -290,8 +348,8 @@ __device__ __forceinline__ float race_exponential(uint32_t w) {
 // Exponential race over the weights w_t (any positive scale): argmax_t w_t / E_t,
 // E_t = -ln u'_t.  `weight(lq, lp)` gives w_t from the two logits of token t; the
 // generator is only run for 4-token blocks with some positive weight.
-template <int NT, class Weight>
-__device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* prow, int lo, int hi,
+template <int NT, bool D2T, class Weight>
+__device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, int lo, int hi,
                                              bool vec4, uint32_t b, uint32_t k0, uint32_t k1,
                                              Weight weight) {
     KeyIdx best{-1.f, 0x7fffffff};
@@ -313,26 +371,24 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* pro
         }
     };
     if (vec4) {
-        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         int t = lo + 4 * (int)threadIdx.x;
         for (; t + 12 * NT < hi; t += 16 * NT) {          // 4 float4 of each row in flight
             float4 a4[4], b4[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 a4[u] = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * u * NT));
-                b4[u] = prow ? __ldg(reinterpret_cast<const float4*>(prow + t + 4 * u * NT)) : z;
+                b4[u] = prow.four(t + 4 * u * NT);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) block4(a4[u], b4[u], t + 4 * u * NT);
         }
         for (; t < hi; t += 4 * NT) {
             const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-            const float4 b4 = prow ? __ldg(reinterpret_cast<const float4*>(prow + t)) : z;
-            block4(a4, b4, t);
+            block4(a4, prow.four(t), t);
         }
     } else {
         for (int t = lo + (int)threadIdx.x; t < hi; t += NT) {
-            const float rr = weight(qrow[t], prow ? prow[t] : 0.f);
+            const float rr = weight(qrow[t], prow.one(t));
             if (rr > 0.f) {
                 const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
                 const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
@@ -345,7 +401,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, const float* pro
 }
 
 // ---------------------------------------------------------------------------
-template <int CS, int NT>
+template <int CS, int NT, bool D2T>
 __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
     using C = Cluster<CS, NT>;
     __shared__ VerifySmem<NT> sm;
@@ -355,6 +411,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
     const int n = a.n, V = a.V;
     const float c = a.c;
     const int64_t Vl = V;
+    const int64_t Vdl = D2T ? a.Vd : V;      // draft-row length
 
     // ---- load and validate the tree (identically in every CTA) ----
     if (tid < n) {
@@ -399,9 +456,14 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
     const int chunk = (((V + CS - 1) / CS) + 3) & ~3;
     const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
     const float* tgt_b = a.target + (int64_t)b * n * Vl;
-    const float* drf_b = a.draft ? a.draft + (int64_t)b * a.R * Vl : nullptr;
+    const float* drf_b = a.draft ? a.draft + (int64_t)b * a.R * Vdl : nullptr;
     const bool vec4 = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0) &&
-                      (a.draft == nullptr || (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0);
+                      (a.draft == nullptr || (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0) &&
+                      (!D2T || (((a.Vd & 3) == 0) && (reinterpret_cast<uintptr_t>(a.t2d) & 15) == 0));
+    // the CTA's slice of the draft row for its statistics (the target slice otherwise)
+    const int chunkd = D2T ? ((((a.Vd + CS - 1) / CS) + 3) & ~3) : chunk;
+    const int plo = D2T ? min(a.Vd, rank * chunkd) : lo;
+    const int phi = D2T ? min(a.Vd, plo + chunkd) : hi;
     const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
 
     int buf = 0;
@@ -413,11 +475,16 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
         const float* qrow = tgt_b + (int64_t)v * Vl;
         const bool kids = sm.nkids[v] > 0;
         if (a.T > 0.f) {
-            const float* prow = kids ? drf_b + (int64_t)sm.row[v] * Vl : nullptr;
+            const float* prow = kids ? drf_b + (int64_t)sm.row[v] * Vdl : nullptr;
+            const PRow<D2T> pr{prow, a.t2d};
             // ---------- pass: statistics of q(v) and p(v) ----------
             RowStat Q{-INFINITY, 0.f}, P{-INFINITY, 0.f};
             int bad = 0;
-            if (vec4) {
+            if constexpr (D2T) {
+                // q over the target slice, p over the draft slice
+                row_stats_slice<NT>(qrow, lo, hi, vec4, c, Q, bad);
+                if (prow) row_stats_slice<NT>(prow, plo, phi, vec4, c, P, bad);
+            } else if (vec4) {
                 int t = lo + 4 * tid;
                 // 4 float4 of each row in flight per thread
                 for (; t + 12 * NT < hi; t += 16 * NT) {
@@ -484,7 +551,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
             for (int ch = v + 1; ch < n && kids; ++ch) {
                 if (sm.parent[ch] != v) continue;
                 const int x = sm.tok[ch];
-                const float lq = qrow[x], lp = prow[x];
+                const float lq = qrow[x], lp = pr.one(x);
                 const float px = prob_of(lp, P.lmax, ip, c);
                 const float r = resid_weight(lq, lp, Q, iq, P, ip, c, rs);
                 const float u = accept_uniform(a.seed, (uint32_t)b, (uint32_t)ch);
@@ -512,7 +579,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             a4[u] = __ldg(reinterpret_cast<const float4*>(qrow + t + 4 * u * NT));
-                            b4[u] = __ldg(reinterpret_cast<const float4*>(prow + t + 4 * u * NT));
+                            b4[u] = pr.four(t + 4 * u * NT);
                         }
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
@@ -523,7 +590,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                     }
                     for (; t < hi; t += 4 * NT) {
                         const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
-                        const float4 b4 = __ldg(reinterpret_cast<const float4*>(prow + t));
+                        const float4 b4 = pr.four(t);
                         s += next_resid(a4.x, b4.x, Q, iq, P, ip, c, cnext) +
                              next_resid(a4.y, b4.y, Q, iq, P, ip, c, cnext) +
                              next_resid(a4.z, b4.z, Q, iq, P, ip, c, cnext) +
@@ -531,7 +598,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                     }
                 } else {
                     for (int t = lo + tid; t < hi; t += NT)
-                        s += next_resid(qrow[t], prow[t], Q, iq, P, ip, c, cnext);
+                        s += next_resid(qrow[t], pr.one(t), Q, iq, P, ip, c, cnext);
                 }
                 const float S = C::sum(sm, buf, s);
                 if (S > 0.f) rs = Residual{cnext, S, 1.f / S};   // else q_cur stays as it is
@@ -543,21 +610,21 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
             if (fused) {
                 // weights max(0, r_j - p), up to the positive factor 1 / D_j
                 const float cnext = rs.rc + rs.rD;
-                best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
+                best = race_slice<NT>(qrow, pr, lo, hi, vec4, (uint32_t)b, k0, k1,
                                       [&](float lq2, float lp2) {
                                           return next_resid(lq2, lp2, Q, iq, P, ip, c, cnext);
                                       });
                 best = C::argmax(sm, buf, best, bad2);
                 if (best.i == 0x7fffffff) {
                     // the clamped residual is all zero: keep q_cur (= r_j)
-                    best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
+                    best = race_slice<NT>(qrow, pr, lo, hi, vec4, (uint32_t)b, k0, k1,
                                           [&](float lq2, float lp2) {
                                               return resid_weight(lq2, lp2, Q, iq, P, ip, c, rs);
                                           });
                     best = C::argmax(sm, buf, best, bad2);
                 }
             } else {
-                best = race_slice<NT>(qrow, prow, lo, hi, vec4, (uint32_t)b, k0, k1,
+                best = race_slice<NT>(qrow, pr, lo, hi, vec4, (uint32_t)b, k0, k1,
                                       [&](float lq2, float lp2) {
                                           return resid_weight(lq2, lp2, Q, iq, P, ip, c, rs);
                                       });
@@ -742,18 +809,35 @@ int verify_cluster_size(int B) {
 
 constexpr int kVerifyThreads = 256;
 
-}  // namespace
-}  // namespace eagle
+template <bool D2T>
+cudaError_t launch_walk(const VerifyArgs& a, cudaStream_t s) {
+    constexpr int NT = kVerifyThreads;
+    switch (verify_cluster_size(a.B)) {
+        case 8: return launch_clustered(verify_walk_kernel<8, NT, D2T>, a.B, 8, NT, 0, s, a);
+        case 4: return launch_clustered(verify_walk_kernel<4, NT, D2T>, a.B, 4, NT, 0, s, a);
+        case 2: return launch_clustered(verify_walk_kernel<2, NT, D2T>, a.B, 2, NT, 0, s, a);
+        default: return launch_clustered(verify_walk_kernel<1, NT, D2T>, a.B, 1, NT, 0, s, a);
+    }
+}
 
-using namespace eagle;
+// t2d[t] = d for t = d + d2t[d], -1 for target ids no draft id maps to.  A draft id
+// mapped outside [0, V) or onto a target id another draft id already holds flags
+// EAGLE_DEV_BAD_TOKEN (and is left out of the table).
+__global__ void t2d_fill_kernel(int32_t* t2d, int V) {
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < V; t += gridDim.x * blockDim.x) t2d[t] = -1;
+}
+__global__ void t2d_scatter_kernel(const int32_t* d2t, int Vd, int32_t* t2d, int V, int32_t* dev_status) {
+    for (int d = blockIdx.x * blockDim.x + threadIdx.x; d < Vd; d += gridDim.x * blockDim.x) {
+        const int64_t t = (int64_t)d + d2t[d];
+        if (t < 0 || t >= V || atomicCAS(&t2d[t], -1, d) != -1) flag_error(dev_status, EAGLE_DEV_BAD_TOKEN);
+    }
+}
 
-extern "C" eagle_status eagle_verify_accept(const float* target_logits, const float* draft_logits,
-                                            const int32_t* draft_row, const int32_t* tokens,
-                                            const int32_t* parent, int B, int n, int V, int R,
-                                            int max_depth, float temperature, uint64_t seed,
-                                            int32_t* accept_len, int32_t* path, int32_t* emit,
-                                            float* row_stats, int32_t* dev_status,
-                                            eagle_stream_t stream) {
+eagle_status verify_common(const float* target_logits, const float* draft_logits, const int32_t* draft_row,
+                           const int32_t* tokens, const int32_t* parent, int B, int n, int V, int R,
+                           int Vd, const int32_t* t2d, int max_depth, float temperature, uint64_t seed,
+                           int32_t* accept_len, int32_t* path, int32_t* emit, float* row_stats,
+                           int32_t* dev_status, eagle_stream_t stream) {
     if (B < 0 || n < 1 || V < 1 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
     if (n > kMaxNodes || max_depth > kMaxNodes) return EAGLE_ERR_SHAPE;
     if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
@@ -766,17 +850,53 @@ extern "C" eagle_status eagle_verify_accept(const float* target_logits, const fl
     if (B == 0) return EAGLE_OK;
     const float c = temperature > 0.f ? kLog2e / temperature : 0.f;
     VerifyArgs a{target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, max_depth,
-                 temperature, c, seed, accept_len, path, emit, row_stats, dev_status};
+                 temperature, c, seed, accept_len, path, emit, row_stats, dev_status, Vd, t2d};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    constexpr int NT = kVerifyThreads;
-    cudaError_t e;
-    switch (verify_cluster_size(B)) {
-        case 8: e = launch_clustered(verify_walk_kernel<8, NT>, B, 8, NT, 0, s, a); break;
-        case 4: e = launch_clustered(verify_walk_kernel<4, NT>, B, 4, NT, 0, s, a); break;
-        case 2: e = launch_clustered(verify_walk_kernel<2, NT>, B, 2, NT, 0, s, a); break;
-        default: e = launch_clustered(verify_walk_kernel<1, NT>, B, 1, NT, 0, s, a); break;
-    }
+    const cudaError_t e = t2d ? launch_walk<true>(a, s) : launch_walk<false>(a, s);
     return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace eagle
+
+using namespace eagle;
+
+extern "C" eagle_status eagle_verify_accept(const float* target_logits, const float* draft_logits,
+                                            const int32_t* draft_row, const int32_t* tokens,
+                                            const int32_t* parent, int B, int n, int V, int R,
+                                            int max_depth, float temperature, uint64_t seed,
+                                            int32_t* accept_len, int32_t* path, int32_t* emit,
+                                            float* row_stats, int32_t* dev_status,
+                                            eagle_stream_t stream) {
+    return verify_common(target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, V,
+                         nullptr, max_depth, temperature, seed, accept_len, path, emit, row_stats,
+                         dev_status, stream);
+}
+
+extern "C" eagle_status eagle_verify_accept_d2t(const float* target_logits, const float* draft_logits,
+                                                const int32_t* draft_row, const int32_t* tokens,
+                                                const int32_t* parent, int B, int n, int V, int R,
+                                                int Vd, const int32_t* t2d, int max_depth,
+                                                float temperature, uint64_t seed,
+                                                int32_t* accept_len, int32_t* path, int32_t* emit,
+                                                float* row_stats, int32_t* dev_status,
+                                                eagle_stream_t stream) {
+    if (Vd < 1 || !t2d) return EAGLE_ERR_INVALID_ARG;
+    return verify_common(target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, Vd, t2d,
+                         max_depth, temperature, seed, accept_len, path, emit, row_stats, dev_status,
+                         stream);
+}
+
+extern "C" eagle_status eagle_d2t_inverse(const int32_t* d2t, int Vd, int V, int32_t* t2d,
+                                          int32_t* dev_status, eagle_stream_t stream) {
+    if (!d2t || !t2d || Vd < 1 || V < 1) return EAGLE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = device_sm_count() * 4;
+    t2d_fill_kernel<<<grid, 256, 0, s>>>(t2d, V);
+    EAGLE_CHECK_LAUNCH();
+    t2d_scatter_kernel<<<grid, 256, 0, s>>>(d2t, Vd, t2d, V, dev_status);
+    EAGLE_CHECK_LAUNCH();
+    return EAGLE_OK;
 }
 
 extern "C" eagle_status eagle_softmax_stats(const float* logits, int64_t rows, int V,

@@ -138,6 +138,36 @@ eagle_status eagle_verify_accept(const float* target_logits, const float* draft_
                                  float* row_stats, int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Draft vocabulary (EAGLE-3).  Guide "EAGLE-3：取消特征约束…": the draft head may
+ * have its own LM head over a smaller vocabulary of Vd ids, and a table d2t
+ * (int32 [Vd]) returns each draft id d to the target id d + d2t[d].
+ *
+ * eagle_d2t_inverse -- t2d[t] = d for t = d + d2t[d], -1 for every target id no
+ * draft id maps to.
+ *   d2t int32 [Vd] (device, read); t2d int32 [V] (device, written; caller-owned).
+ * A draft id mapped outside [0, V), or onto a target id that another draft id
+ * also maps to, sets EAGLE_DEV_BAD_TOKEN and is left out of t2d.
+ *
+ * eagle_verify_accept_d2t -- eagle_verify_accept when the draft rows are over
+ * the draft vocabulary: draft_logits f32 [B, R, Vd]; t2d int32 [V] from
+ * eagle_d2t_inverse; tokens are target ids.  p over the target vocabulary is
+ * softmax(draft row / T) at the ids d + d2t[d] and 0 at every other target id,
+ * so a target id p never proposes keeps its full q in every residual.  The
+ * walk, the uniforms, row_stats (the draft slot then over the Vd draft ids) and
+ * the errors are those of eagle_verify_accept.  Vd % 4 == 0 and 16-byte aligned
+ * rows take the vector path; other sizes are correct, slower.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_d2t_inverse(const int32_t* d2t, int Vd, int V, int32_t* t2d,
+                               int32_t* dev_status, eagle_stream_t stream);
+eagle_status eagle_verify_accept_d2t(const float* target_logits, const float* draft_logits,
+                                     const int32_t* draft_row, const int32_t* tokens,
+                                     const int32_t* parent, int B, int n, int V, int R, int Vd,
+                                     const int32_t* t2d, int max_depth, float temperature,
+                                     uint64_t seed, int32_t* accept_len, int32_t* path,
+                                     int32_t* emit, float* row_stats, int32_t* dev_status,
+                                     eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * eagle_kv_compact -- commit the accepted path into the KV cache.
  * Lesson "KV cache 回滚" and "第 4 步" (one physical cache plus a logical
  * length).  For t = 0 .. a (a = accept_len[b]): row L_b + path[b][t] moves to
@@ -202,6 +232,19 @@ eagle_status eagle2_expand(int level, int final, const void* hidden, const void*
                            void* tree_state, size_t state_bytes, float* partials, size_t partials_bytes,
                            int32_t* out_tokens, int32_t* out_parent, int32_t* out_draft_row,
                            int32_t* frontier_tokens, int32_t* dev_status, eagle_stream_t stream);
+
+/* eagle2_expand_d2t -- eagle2_expand with a draft vocabulary: V is the draft
+ * vocabulary size (the LM head's rows and the logits' width), the ranking is
+ * over draft ids (ties to the lower draft id), and each chosen draft id d enters
+ * the tree -- tree state, out_tokens, frontier_tokens -- as the target id
+ * d + d2t[d].  d2t int32 [V] (device) must not be NULL; the caller keeps the
+ * mapped ids inside the target vocabulary (eagle_d2t_inverse checks a table). */
+eagle_status eagle2_expand_d2t(int level, int final, const void* hidden, const void* lm_head_w,
+                               float* logits, int B, int H, int V, int top_k, int depth, int n_out,
+                               void* tree_state, size_t state_bytes, float* partials,
+                               size_t partials_bytes, const int32_t* d2t, int32_t* out_tokens,
+                               int32_t* out_parent, int32_t* out_draft_row,
+                               int32_t* frontier_tokens, int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * eagle2_expand_static_state -- eagle2_expand without caller-provided scratch.

@@ -233,3 +233,42 @@ def test_fused_expansion_tied_logits():
         assert len(kids) > 0
         assert all(t % 500 == kids[0] % 500 for t in kids)
     assert np.array_equal(t1, t0) and np.array_equal(p1, p0) and np.array_equal(r1, r0)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_expansion_with_d2t_matches_oracle(fused):
+    """A draft vocabulary of 8000 ids of a 32000-id target vocabulary: the GPU tree's
+    tokens are the mapped target ids, the tree is the oracle's.  Given logits
+    (one-pass top-k), or from hidden states through the GEMM (fused top-k; the oracle
+    then expands the very logits the GEMM wrote)."""
+    E = _E()
+    B, k, D, n_out, H, V, Vt = 4, 10, 4, 30, 512, 8000, 32000
+    d2t, ids = W.d2t_table(Vt, V, 5)
+    R = 1 + (D - 1) * k
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    state = torch.empty(E.tree_state_size(B, k, D), dtype=torch.uint8, device="cuda")
+    tok = torch.empty(B, n_out, dtype=torch.int32, device="cuda")
+    par, row = torch.empty_like(tok), torch.empty_like(tok)
+    front = torch.empty(B, k, dtype=torch.int32, device="cuda")
+    d2t_gpu = torch.from_numpy(d2t).cuda()
+    if fused:
+        w = W.lm_head(V, H, 0.02, 6, block=1000).cuda()
+        hid = [W.hidden_states(B, 1 if l == 1 else k, H, l, 6).cuda() for l in range(1, D + 1)]
+        lg = torch.zeros(B, R, V, device="cuda")
+        part = torch.empty(E.expand_scratch_size(B, V, k) // 4, device="cuda")
+    else:
+        cfg = W.CONFIGS["eagle3_b64"]
+        _, drows = W.tree_draft_rows(cfg, seed=6, B=B, V=V)
+        lg = torch.from_numpy(np.ascontiguousarray(drows[:, :R])).cuda()
+    for lvl in range(1, D + 1):
+        E.eagle2_expand(lvl, lvl == D, lg, k, D, n_out, state,
+                        hidden=hid[lvl - 1] if fused else None, lm_head_w=w if fused else None,
+                        out_tokens=tok, out_parent=par, out_draft_row=row, frontier_tokens=front,
+                        dev_status=st, partials=part if fused else None, d2t=d2t_gpu)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle.eagle2_from_logits(lg.cpu().numpy(), k, D, n_out, d2t=d2t)
+    assert _compare_trees(ref, tok.cpu().numpy(), par.cpu().numpy(), row.cpu().numpy()) <= 1
+    t = tok.cpu().numpy()[:, 1:]
+    assert np.isin(t, ids).all()
+    assert np.isin(front.cpu().numpy(), ids).all()

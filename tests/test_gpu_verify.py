@@ -206,3 +206,72 @@ def test_softmax_stats_full_size_sampled_rows():
     np.testing.assert_allclose(gm.reshape(-1).cpu().numpy()[rows], m, rtol=1e-6)
     np.testing.assert_allclose(gz.reshape(-1).cpu().numpy()[rows], Z, rtol=1e-5)
     assert np.array_equal(ga.reshape(-1).cpu().numpy()[rows], am)
+
+
+# ---------------------------------------------------------------- draft vocabulary (d2t)
+def _d2t_case(cfg, B, seed, V, Vd, sigma=None):
+    d2t, ids = W.d2t_table(V, Vd, seed)
+    trow, drows = W.tree_draft_rows_d2t(cfg, seed, ids, B=B, V=V, sigma=sigma)
+    tree = oracle.eagle2_from_logits(drows, cfg.top_k, cfg.depth, cfg.n, d2t=d2t)
+    tgt = W.assemble_target(trow, tree["draft_row"], tree["cand"], cfg.target_std, seed)
+    return tgt, drows, tree, d2t
+
+
+def test_d2t_inverse_table_and_bad_tables():
+    E = _gpu()
+    V, Vd = 1000, 250
+    d2t, ids = W.d2t_table(V, Vd, 3)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2d = E.eagle_d2t_inverse(_cuda(d2t), V, dev_status=st).cpu().numpy()
+    torch.cuda.synchronize()
+    ref = np.full(V, -1, np.int32)
+    ref[ids] = np.arange(Vd)
+    assert int(st.item()) == 0 and np.array_equal(t2d, ref)
+    bad = d2t.copy()
+    bad[7] = ids[3] - 7                      # draft id 7 onto draft id 3's target id
+    st.zero_()
+    E.eagle_d2t_inverse(_cuda(bad), V, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 2                 # EAGLE_DEV_BAD_TOKEN
+    out = d2t.copy()
+    out[-1] = V - (Vd - 1)                    # last draft id -> target id V
+    st.zero_()
+    E.eagle_d2t_inverse(_cuda(out), V, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & 2
+
+
+@pytest.mark.parametrize("V,Vd,T", [(128256, 32000, 1.0), (128256, 32000, 0.0), (1000, 252, 1.0),
+                                    (1003, 257, 1.0)])
+def test_d2t_trees_match_oracle(V, Vd, T):
+    """Draft rows over a draft vocabulary of Vd ids mapped to target ids (EAGLE-3's
+    32000 of 128256, and ragged small sizes that take the scalar path), 48-node depth-6
+    trees built from those rows, B = 8."""
+    E = _gpu()
+    cfg = W.CONFIGS["sweep_70b"]
+    tgt, drows, tree, d2t = _d2t_case(cfg, 8, seed=17, V=V, Vd=Vd)
+    ref = oracle.verify_accept_d2t(tgt, drows, d2t, tree["tokens"], tree["parent"], cfg.depth, T,
+                                   seed=21, draft_row=tree["draft_row"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t2d = E.eagle_d2t_inverse(_cuda(d2t), V, dev_status=st)
+    rs = torch.full((2, 8, cfg.n, 2), float("nan"), device="cuda")
+    acc, path, emit = E.eagle_verify_accept(
+        _cuda(tgt), _cuda(drows), _cuda(tree["tokens"]), _cuda(tree["parent"]), cfg.depth, T, 21,
+        draft_row=_cuda(tree["draft_row"]), row_stats=rs, dev_status=st, t2d=t2d)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and (ref["status"] == 0).all()
+    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(),
+                              exact=(T == 0.0))
+    assert_tie_budget(dec, ties)
+    # a random quarter of the target ids leaves most of q's mass outside the draft
+    # vocabulary, so acceptance is low; some drafts are still accepted
+    assert (ref["accept_len"] > 0).any()
+    if T > 0:
+        # draft statistics of the visited rows are over the Vd draft ids
+        r = rs.cpu().numpy()
+        rows = tree["draft_row"]
+        seen = ~np.isnan(r[1, :, :, 0])
+        assert seen.any()
+        m, Z, _, _ = oracle.softmax_rows(drows, T)
+        b_i, n_i = np.nonzero(seen)
+        np.testing.assert_allclose(r[1, b_i, n_i, 1], Z[b_i, rows[b_i, n_i]], rtol=1e-5)

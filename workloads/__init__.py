@@ -34,6 +34,7 @@ TAG_W = 10
 TAG_TREE = 11
 TAG_CACHE = 12
 TAG_CHAIN = 13
+TAG_D2T = 14          # which target ids a draft vocabulary holds
 
 
 @dataclass(frozen=True)
@@ -158,6 +159,25 @@ def tree_draft_rows(cfg: Config, seed: int, B: int | None = None, V: int | None 
     trow = per_seq_normal(B, (cfg.R, V), cfg.target_std, seed, TAG_TARGET)
     drows = trow + per_seq_normal(B, (cfg.R, V), sigma, seed, TAG_DRAFT_NOISE)
     return trow, drows
+
+
+def d2t_table(V: int, Vd: int, seed: int):
+    """A draft vocabulary of Vd target ids, a sorted seeded subset of [0, V), as the
+    table d2t (int32 [Vd], draft id d -> target id d + d2t[d]) and the ids themselves."""
+    ids = np.sort(rng(seed, TAG_D2T, V, Vd).choice(V, size=Vd, replace=False))
+    return (ids - np.arange(Vd)).astype(np.int32), ids.astype(np.int64)
+
+
+def tree_draft_rows_d2t(cfg: Config, seed: int, ids: np.ndarray, B: int | None = None,
+                        V: int | None = None, sigma: float | None = None):
+    """Per draft row r: the target row T_r over V ids, and the draft row over the draft
+    vocabulary (the entries of T_r at the vocabulary's ids, plus sigma * noise)."""
+    B = cfg.B if B is None else B
+    V = cfg.V if V is None else V
+    sigma = cfg.sigma if sigma is None else sigma
+    trow = per_seq_normal(B, (cfg.R, V), cfg.target_std, seed, TAG_TARGET)
+    drows = trow[..., ids] + per_seq_normal(B, (cfg.R, len(ids)), sigma, seed, TAG_DRAFT_NOISE)
+    return trow, drows.astype(np.float32)
 
 
 def assemble_target(trow: np.ndarray, draft_row: np.ndarray, cand: np.ndarray,

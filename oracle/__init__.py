@@ -378,3 +378,63 @@ def eagle2_from_logits(logits, top_k: int, depth: int, n_out: int, root_tokens=N
     res = {key: np.stack([o[key] for o in outs]) for key in outs[0]}
     res["trees"] = trees
     return res
+
+
+# ---------------------------------------------------------------- static trees
+def static_tree_from_choices(choices):
+    """A static draft tree (EAGLE-1 / Medusa style) from its list of choices: each choice
+    is a path of child ranks from the root, (r_1, ..., r_d), naming the node reached by
+    taking, at each depth, the r-th best token of the parent's draft distribution.
+    Guide, "EAGLE-2：草稿树的 Expansion 与 Reranking" (the static trees EAGLE-2 replaces
+    add a fixed k candidates per step) and the file layout it points to (choices.py).
+
+    Readings where the pages are silent: every proper prefix of a choice must itself
+    be a choice (a node's parent is in the tree); choices are distinct and ranks are
+    >= 0.  Node order: the root (node 0), then the choices sorted by (length,
+    lexicographic) -- a topological order.  The children of a node are drafted from
+    one draft row: internal nodes (nodes with children) are numbered 0, 1, ... in node
+    order, and that number is the node's draft row.
+    Returns dict(parent, rank, depth, draft_row) int32 [n] (root: parent -1, rank -1)."""
+    paths = [tuple(int(r) for r in c) for c in choices]
+    if len(set(paths)) != len(paths):
+        raise ValueError("duplicate choice")
+    if any(len(c) == 0 or min(c) < 0 for c in paths):
+        raise ValueError("empty choice or negative rank")
+    have = set(paths)
+    for c in paths:
+        if len(c) > 1 and c[:-1] not in have:
+            raise ValueError(f"choice {c} without its parent {c[:-1]}")
+    order = sorted(paths, key=lambda c: (len(c), c))
+    index = {(): 0}
+    for i, c in enumerate(order):
+        index[c] = i + 1
+    n = len(order) + 1
+    parent = np.full(n, -1, np.int32)
+    rank = np.full(n, -1, np.int32)
+    depth = np.zeros(n, np.int32)
+    for c in order:
+        i = index[c]
+        parent[i] = index[c[:-1]]
+        rank[i] = c[-1]
+        depth[i] = len(c)
+    has_kids = np.zeros(n, bool)
+    has_kids[parent[1:]] = True
+    draft_row = np.full(n, -1, np.int32)
+    draft_row[has_kids] = np.arange(int(has_kids.sum()), dtype=np.int32)
+    return dict(parent=parent, rank=rank, depth=depth, draft_row=draft_row)
+
+
+def static_tree_tokens(logits, tree):
+    """Tokens of a static tree's nodes from the draft rows of its internal nodes,
+    f32 [B, R, V] (row draft_row[v] holds the distribution after node v): node i takes
+    the rank[i]-th best token (logit desc, token asc) of its parent's row.  The root's
+    token is -1 (it is the last committed token, known to the caller)."""
+    x = _c(logits, np.float32)
+    B, R, V = x.shape
+    par, rank, drow = tree["parent"], tree["rank"], tree["draft_row"]
+    K = int(rank.max()) + 1 if len(rank) > 1 else 1
+    tok, _, st = row_topk(x, K)
+    out = np.full((B, len(par)), -1, np.int32)
+    for i in range(1, len(par)):
+        out[:, i] = tok[:, drow[par[i]], rank[i]]
+    return out

@@ -165,3 +165,62 @@ def test_eagle2_with_d2t_maps_tokens_and_keeps_the_tree():
         assert np.array_equal(plain[key], mapped[key])
     assert (mapped["tokens"][:, 0] == -1).all()
     assert np.array_equal(mapped["tokens"][:, 1:], ids[plain["tokens"][:, 1:]])
+
+
+# ------------------------------------------------------------------ static trees
+def test_static_tree_hand_worked_example():
+    """Choices (0), (1), (0,0), (0,1), (1,0), (0,0,0), worked out by hand: nodes in
+    (length, lexicographic) order after the root."""
+    t = oracle.static_tree_from_choices([(1, 0), (0,), (0, 0, 0), (1,), (0, 1), (0, 0)])
+    #            root (0)  (1)  (0,0) (0,1) (1,0) (0,0,0)
+    assert t["parent"].tolist() == [-1, 0, 0, 1, 1, 2, 3]
+    assert t["rank"].tolist() == [-1, 0, 1, 0, 1, 0, 0]
+    assert t["depth"].tolist() == [0, 1, 1, 2, 2, 2, 3]
+    # internal nodes: root, (0), (1), (0,0) -> rows 0..3
+    assert t["draft_row"].tolist() == [0, 1, 2, 3, -1, -1, -1]
+
+
+def test_static_tree_round_trip_and_errors():
+    g = W.rng(8, 47)
+    # a random prefix-closed set of choices: grow from the root
+    choices = set()
+    frontier = [()]
+    while frontier and len(choices) < 40:
+        c = frontier.pop(0)
+        for r in range(int(g.integers(0, 4))):
+            choices.add(c + (r,))
+            frontier.append(c + (r,))
+    choices = sorted(choices, key=lambda c: g.random())           # any input order
+    t = oracle.static_tree_from_choices(choices)
+    par, rank = t["parent"], t["rank"]
+    assert all(0 <= par[i] < i for i in range(1, len(par)))
+    paths = set()
+    for i in range(1, len(par)):
+        p, v = [], i
+        while v > 0:
+            p.append(int(rank[v]))
+            v = par[v]
+        paths.add(tuple(reversed(p)))
+        assert len(p) == t["depth"][i]
+    assert paths == set(choices)
+    kids = set(par[1:].tolist())
+    assert [i for i in range(len(par)) if t["draft_row"][i] >= 0] == sorted(kids)
+    for bad in ([(0,), (0,)], [(1, 0)], [(0,), (-1,)], [()]):
+        with pytest.raises(ValueError):
+            oracle.static_tree_from_choices(bad)
+
+
+def test_static_tree_tokens_are_ranked_tokens_of_the_parent_row():
+    t = oracle.static_tree_from_choices([(0,), (1,), (2,), (0, 0), (0, 1), (1, 0), (0, 0, 0)])
+    R = int(t["draft_row"].max()) + 1
+    B, V = 3, 50
+    x = W.rng(9, 48).normal(0, 1, size=(B, R, V)).astype(np.float32)
+    x[1, 0, 7] = x[1, 0, 3] = x[1, 0].max() + 1        # a tie at the top: lower token first
+    tok = oracle.static_tree_tokens(x, t)
+    for b in range(B):
+        assert tok[b, 0] == -1
+        for i in range(1, len(t["parent"])):
+            row = x[b, t["draft_row"][t["parent"][i]]].astype(np.float64)
+            order = sorted(range(V), key=lambda c: (-row[c], c))
+            assert tok[b, i] == order[t["rank"][i]]
+    assert tok[1, 1] == 3 and tok[1, 2] == 7

@@ -9,6 +9,7 @@ the optional ``dev_status`` int32 tensor (bits EAGLE_DEV_*).
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import torch
@@ -212,6 +213,43 @@ def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=
         int(level), int(final), _ptr(hidden), _ptr(lm_head_w), _ptr(logits), B, H, V, top_k, depth,
         n_out, _ptr(tree_state), nbytes, _ptr(partials), sbytes, _ptr(out_tokens), _ptr(out_parent),
         _ptr(out_draft_row), _ptr(frontier_tokens), _ptr(_status(dev_status, logits.device)),
+        _stream(stream)))
+
+
+def eagle_static_tree(choices):
+    """Plan a static draft tree from its choices (rank paths from the root) on the host.
+    Returns dict(parent, rank, depth, draft_row) of int32 numpy arrays [n]."""
+    import numpy as np
+    n_choices = len(choices)
+    max_len = max((len(c) for c in choices), default=1)
+    ranks = np.zeros((max(n_choices, 1), max_len), np.int32)
+    lens = np.zeros(max(n_choices, 1), np.int32)
+    for i, c in enumerate(choices):
+        ranks[i, :len(c)] = c
+        lens[i] = len(c)
+    n_max = n_choices + 1
+    out = {k: np.zeros(n_max, np.int32) for k in ("parent", "rank", "depth", "draft_row")}
+    n_nodes = np.zeros(1, np.int32)
+    adr = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    _check("eagle_static_tree", lib().eagle_static_tree(
+        adr(ranks), adr(lens), n_choices, max_len, n_max, adr(out["parent"]), adr(out["rank"]),
+        adr(out["depth"]), adr(out["draft_row"]), adr(n_nodes)))
+    n = int(n_nodes[0])
+    return {k: v[:n] for k, v in out.items()}
+
+
+def eagle_static_tree_level(level, logits, parent, rank, depth, draft_row, tokens,
+                            dev_status=None, stream=None):
+    """Tokens of the nodes at depth `level` of a static tree (device int32 arrays [n]),
+    from the internal nodes' draft rows logits [B, R, V] (f32), into tokens [B, n]."""
+    _dev(logits, "logits", torch.float32)
+    for name, t in (("parent", parent), ("rank", rank), ("depth", depth),
+                    ("draft_row", draft_row), ("tokens", tokens)):
+        _dev(t, name, torch.int32)
+    B, R, V = logits.shape
+    _check("eagle_static_tree_level", lib().eagle_static_tree_level(
+        int(level), _ptr(logits), _ptr(parent), _ptr(rank), _ptr(depth), _ptr(draft_row),
+        parent.numel(), B, R, V, _ptr(tokens), _ptr(_status(dev_status, logits.device)),
         _stream(stream)))
 
 

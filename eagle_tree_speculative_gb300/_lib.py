@@ -33,6 +33,8 @@ SIGNATURES = {
                            _P, _P, _P]),
     "eagle2_expand_d2t": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _SZ, _P, _P,
                                _P, _P, _P, _P, _P]),
+    "eagle_static_tree": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "eagle_static_tree_level": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "eagle2_expand_static_state": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                         _P, _P]),
     "eagle_softmax_stats": (_I, [_P, _I64, _I, _F, _P, _P, _P, _P, _P]),

@@ -22,6 +22,9 @@
 //                    sort those by (depth asc, V desc, id asc) and re-index parents.
 // The draft LM-head GEMM (lmhead_gemm.cu) writes the level's logits rows first
 // when hidden states are given.
+#include <algorithm>
+#include <map>
+#include <vector>
 #include <cstdlib>
 #include <mutex>
 
@@ -834,4 +837,153 @@ extern "C" eagle_status eagle2_expand_static_state(int level, int final, const v
     return eagle2_expand(level, final, hidden, lm_head_w, logits, B, H, V, top_k, depth, n_out,
                          state, kStaticStateBytes, nullptr, 0, out_tokens, out_parent,
                          out_draft_row, frontier_tokens, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Static draft trees (EAGLE-1 / Medusa style): the tree is fixed by a list of
+// rank paths ("choices"); node (r_1..r_d) takes the r_d-th best token of its
+// parent's draft row.  Guide "EAGLE-2：草稿树的 Expansion 与 Reranking" (the static
+// trees that EAGLE-2 replaces add a fixed number of candidates per step).
+// ---------------------------------------------------------------------------
+namespace eagle {
+namespace {
+
+// One CTA per (internal node v at depth level-1, sequence b): the top K = (largest
+// child rank + 1) of v's draft row, then each child c of v gets token top[rank[c]].
+__global__ void __launch_bounds__(kTopkThreads)
+static_tree_level_kernel(int level, const float* __restrict__ logits, const int32_t* parent,
+                         const int32_t* rank, const int32_t* depth, const int32_t* draft_row,
+                         int n, int R, int V, int32_t* tokens, int32_t* dev_status) {
+    __shared__ float s_v[kTopkWarps * kKMax];
+    __shared__ int s_i[kTopkWarps * kKMax];
+    __shared__ int s_tok[kKMax];
+    __shared__ int s_K, s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int v = blockIdx.x, b = blockIdx.y;
+    if (depth[v] != level - 1 || draft_row[v] < 0) return;      // block-uniform
+    if (tid == 0) {
+        int K = 0;
+        for (int c = v + 1; c < n; ++c)
+            if (parent[c] == v) K = max(K, rank[c] + 1);
+        s_K = K;
+        s_bad = 0;
+    }
+    __syncthreads();
+    const int K = s_K;
+    if (K == 0) return;
+    const int row = draft_row[v];
+    if (row >= R || K > kKMax || K > V) {
+        if (tid == 0) flag_error(dev_status, EAGLE_DEV_BAD_TREE);
+        return;
+    }
+    const float* x = logits + ((int64_t)b * R + row) * (int64_t)V;
+    float lv = -INFINITY, tv = -INFINITY;
+    int li = 0x7fffffff, ti = 0x7fffffff, bad = 0;
+    for (int base = 0; base < V; base += kTopkThreads) {            // block-uniform trips
+        const int t = base + tid;
+        const bool ok = t < V;
+        const float l = ok ? x[t] : -INFINITY;
+        bad |= ok && (l != l || l == INFINITY);
+        unsigned ball = __ballot_sync(0xffffffffu, ok && topk_better(l, t, tv, ti));
+        while (ball) {
+            const int src = __ffs(ball) - 1;
+            ball &= ball - 1;
+            const float cv = __shfl_sync(0xffffffffu, l, src);
+            const int ci = __shfl_sync(0xffffffffu, t, src);
+            if (topk_better(cv, ci, tv, ti)) {
+                warp_list_insert(lv, li, cv, ci);
+                tv = __shfl_sync(0xffffffffu, lv, K - 1);
+                ti = __shfl_sync(0xffffffffu, li, K - 1);
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&s_bad, 1);
+    if (lane < K) { s_v[warp * kKMax + lane] = lv; s_i[warp * kKMax + lane] = li; }
+    __syncthreads();
+    if (tid < kTopkWarps * K) {
+        const int w = tid / K, j = tid % K;
+        const float val = s_v[w * kKMax + j];
+        const int id = s_i[w * kKMax + j];
+        int r = 0;
+        for (int w2 = 0; w2 < kTopkWarps; ++w2)
+            for (int j2 = 0; j2 < K; ++j2)
+                r += topk_better(s_v[w2 * kKMax + j2], s_i[w2 * kKMax + j2], val, id);
+        if (r < K) s_tok[r] = id;
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) flag_error(dev_status, EAGLE_DEV_NONFINITE);
+        return;
+    }
+    for (int c = v + 1 + tid; c < n; c += kTopkThreads)
+        if (parent[c] == v) tokens[(int64_t)b * n + c] = s_tok[rank[c]];
+}
+
+}  // namespace
+}  // namespace eagle
+
+extern "C" eagle_status eagle_static_tree(const int32_t* ranks, const int32_t* lens, int n_choices,
+                                          int max_len, int n_max, int32_t* parent, int32_t* rank,
+                                          int32_t* depth, int32_t* draft_row, int32_t* n_nodes) {
+    if (!ranks || !lens || !parent || !rank || !depth || !draft_row || !n_nodes || n_choices < 0 ||
+        max_len < 1)
+        return EAGLE_ERR_INVALID_ARG;
+    const int n = n_choices + 1;
+    if (n > n_max || n > kMaxNodes) return EAGLE_ERR_CAPACITY;
+    std::vector<std::vector<int>> paths((size_t)n_choices);
+    for (int c = 0; c < n_choices; ++c) {
+        const int len = lens[c];
+        if (len < 1 || len > max_len) return EAGLE_ERR_SHAPE;
+        for (int j = 0; j < len; ++j) {
+            const int r = ranks[(size_t)c * max_len + j];
+            if (r < 0 || r >= kKMax) return EAGLE_ERR_SHAPE;
+            paths[c].push_back(r);
+        }
+    }
+    // node order: (length, lexicographic); the root is node 0
+    std::sort(paths.begin(), paths.end(), [](const std::vector<int>& a, const std::vector<int>& b) {
+        return a.size() != b.size() ? a.size() < b.size() : a < b;
+    });
+    std::map<std::vector<int>, int> index;
+    index[std::vector<int>()] = 0;
+    for (int c = 0; c < n_choices; ++c) {
+        if (!index.emplace(paths[c], c + 1).second) return EAGLE_ERR_SHAPE;   // duplicate
+    }
+    std::vector<int> par(n, -1), rk(n, -1), dep(n, 0);
+    for (int c = 0; c < n_choices; ++c) {
+        const std::vector<int> pre(paths[c].begin(), paths[c].end() - 1);
+        const auto it = index.find(pre);
+        if (it == index.end()) return EAGLE_ERR_SHAPE;                         // parent missing
+        par[c + 1] = it->second;
+        rk[c + 1] = paths[c].back();
+        dep[c + 1] = (int)paths[c].size();
+    }
+    std::vector<char> kids(n, 0);
+    for (int i = 1; i < n; ++i) kids[par[i]] = 1;
+    int rows = 0;
+    for (int i = 0; i < n; ++i) {
+        parent[i] = par[i];
+        rank[i] = rk[i];
+        depth[i] = dep[i];
+        draft_row[i] = kids[i] ? rows++ : -1;
+    }
+    *n_nodes = n;
+    return EAGLE_OK;
+}
+
+extern "C" eagle_status eagle_static_tree_level(int level, const float* logits, const int32_t* parent,
+                                                const int32_t* rank, const int32_t* depth,
+                                                const int32_t* draft_row, int n, int B, int R, int V,
+                                                int32_t* tokens, int32_t* dev_status,
+                                                eagle_stream_t stream) {
+    if (!logits || !parent || !rank || !depth || !draft_row || !tokens || level < 1 || B < 0 ||
+        R < 1 || V < 1 || n < 1)
+        return EAGLE_ERR_INVALID_ARG;
+    if (n > kMaxNodes) return EAGLE_ERR_SHAPE;
+    if (B == 0) return EAGLE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    static_tree_level_kernel<<<dim3((unsigned)n, (unsigned)B), kTopkThreads, 0, s>>>(
+        level, logits, parent, rank, depth, draft_row, n, R, V, tokens, dev_status);
+    EAGLE_CHECK_LAUNCH();
+    return EAGLE_OK;
 }

@@ -247,6 +247,41 @@ eagle_status eagle2_expand_d2t(int level, int final, const void* hidden, const v
                                int32_t* frontier_tokens, int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Static draft trees (EAGLE-1 / Medusa style).  Guide "EAGLE-2：草稿树的 Expansion
+ * 与 Reranking": the static trees EAGLE-2 replaces add a fixed number of
+ * candidates per step, whatever the context.  A static tree is a list of
+ * choices, each a path of child ranks (r_1, ..., r_d) from the root: the node it
+ * names takes the r_d-th best token (logit desc, lower token on ties) of its
+ * parent's draft row.  The tree then feeds eagle_tree_attn and
+ * eagle_verify_accept through its parent and draft_row arrays, like an EAGLE-2
+ * tree.
+ *
+ * eagle_static_tree -- HOST planner (host pointers, no GPU work, no allocation
+ * visible to the caller).  ranks int32 [n_choices, max_len] row-major, choice c
+ * being ranks[c][0 .. lens[c]-1]; lens int32 [n_choices].  Writes n = n_choices
+ * + 1 nodes: the root, then the choices sorted by (length, lexicographic), into
+ * parent, rank (root: -1), depth and draft_row (internal nodes numbered 0, 1, ...
+ * in node order; leaves -1), each int32 [n_max]; *n_nodes = n.
+ * Errors: EAGLE_ERR_CAPACITY when n > n_max or n > 64; EAGLE_ERR_SHAPE for an
+ * empty or too long choice, a rank outside [0, 16), a duplicate, or a choice
+ * whose parent path is not itself a choice.
+ *
+ * eagle_static_tree_level -- one level's tokens on the GPU: for every node c at
+ * depth `level`, tokens[b][c] = the rank[c]-th best token of row draft_row[parent
+ * [c]] of logits f32 [B, R, V] (the draft rows of the internal nodes).  parent,
+ * rank, depth, draft_row: int32 [n], device.  Other entries of tokens are left
+ * as they are (the root's is the caller's).  A non-finite row sets
+ * EAGLE_DEV_NONFINITE; a draft row >= R sets EAGLE_DEV_BAD_TREE.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_static_tree(const int32_t* ranks, const int32_t* lens, int n_choices, int max_len,
+                               int n_max, int32_t* parent, int32_t* rank, int32_t* depth,
+                               int32_t* draft_row, int32_t* n_nodes);
+eagle_status eagle_static_tree_level(int level, const float* logits, const int32_t* parent,
+                                     const int32_t* rank, const int32_t* depth,
+                                     const int32_t* draft_row, int n, int B, int R, int V,
+                                     int32_t* tokens, int32_t* dev_status, eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * eagle2_expand_static_state -- eagle2_expand without caller-provided scratch.
  * No counterpart in the paper: this is a deployment convenience of this library.
  * It is for callers that cannot allocate device memory themselves: a serving

@@ -49,6 +49,18 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
     return t
 
 
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    """A CUDA tensor, or a page-locked host tensor, which the GPU reads in place over
+    unified addressing (the kernel then moves only the bytes it touches)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return t
+    return _dev(t, name, dtype)
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -116,8 +128,9 @@ def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, 
                         dev_status=None, stream=None, t2d=None):
     """Returns (accept_len [B], path [B,D+1], emit [B,D+1]) int32 tensors.  With t2d
     (from eagle_d2t_inverse) the draft rows are over the draft vocabulary
-    [B, R, Vd] and tokens are target ids."""
-    _dev(target_logits, "target_logits", torch.float32)
+    [B, R, Vd] and tokens are target ids.  target_logits may be a pinned host tensor:
+    the walk then reads only the rows it visits, in place."""
+    _dev_or_pinned(target_logits, "target_logits", torch.float32)
     B, n, V = target_logits.shape
     R = n
     Vd = V
@@ -129,7 +142,7 @@ def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, 
     _dev(parent, "parent", torch.int32)
     if draft_row is not None:
         _dev(draft_row, "draft_row", torch.int32)
-    dev = target_logits.device
+    dev = tokens.device
     D = int(max_depth)
     accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
     path = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if path is None else path

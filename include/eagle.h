@@ -112,7 +112,10 @@ eagle_status eagle_tree_attn(const void* q, const void* k_cache, const void* v_c
  * Philox(seed; t >> 2, 0, b, 1).  At temperature 0 a child is accepted iff
  * its token is the argmax of target row v (lowest index on ties) and the
  * final token is that argmax.
- *   target_logits f32 [B, n, V]  row i: target logits after node i
+ *   target_logits f32 [B, n, V]  row i: target logits after node i.  Device
+ *                 memory, or page-locked host memory the GPU addresses directly
+ *                 (unified addressing): the walk then reads in place only the
+ *                 rows it visits.
  *   draft_logits  f32 [B, R, V]  draft logits rows (only rows of nodes with
  *                 children are read; unused at T = 0, may then be NULL)
  *   draft_row     int32 [B, n] or NULL: row of draft_logits holding the draft

@@ -275,3 +275,21 @@ def test_d2t_trees_match_oracle(V, Vd, T):
         m, Z, _, _ = oracle.softmax_rows(drows, T)
         b_i, n_i = np.nonzero(seen)
         np.testing.assert_allclose(r[1, b_i, n_i, 1], Z[b_i, rows[b_i, n_i]], rtol=1e-5)
+
+
+def test_target_logits_in_pinned_host_memory_give_the_same_walk():
+    """target_logits may live in page-locked host memory, read in place by the walk:
+    the outputs equal those of the same call on a device copy, bit for bit."""
+    E = _gpu()
+    cfg = W.CONFIGS["sweep_70b"]
+    tgt, drows, tree = _tree_case(cfg, 8, seed=41, V=32000)
+    args = (_cuda(drows), _cuda(tree["tokens"]), _cuda(tree["parent"]), cfg.depth, 1.0, 17)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev_out = E.eagle_verify_accept(_cuda(tgt), *args, draft_row=_cuda(tree["draft_row"]),
+                                    dev_status=st)
+    host = torch.from_numpy(np.ascontiguousarray(tgt)).pin_memory()
+    host_out = E.eagle_verify_accept(host, *args, draft_row=_cuda(tree["draft_row"]), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for a, b in zip(dev_out, host_out):
+        assert torch.equal(a, b)

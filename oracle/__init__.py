@@ -199,6 +199,45 @@ def verify_accept_d2t(target, draft, d2t, tokens, parent, max_depth: int, T: flo
                          draft_row=draft_row, u_override=u_override)
 
 
+def filter_logits(logits, T: float, top_k: int = 0, top_p: float = 0.0):
+    """Top-k then top-p filtering of rows of logits at temperature T > 0, as logits:
+    kept entries unchanged, the others -inf (probability 0 after the softmax).
+
+    Guide, "一次 eagenerate 调用的完整流转": eagenerate takes temperature, top_p and
+    top_k (0 = off).  Reading, where the pages are silent: rank a row's tokens by
+    probability (logit desc, lower token first on ties); top-k keeps the first k;
+    top-p then keeps the shortest prefix of that order whose probability, renormalised
+    over what top-k kept, reaches top_p (at least one token; top_p <= 0 or >= 1 keeps
+    all).  Applied the same way to the target rows (q) and the draft rows (p)."""
+    x = np.asarray(logits, np.float32)
+    V = x.shape[-1]
+    flat = x.reshape(-1, V)
+    out = np.full_like(flat, -np.inf)
+    for r in range(flat.shape[0]):
+        row = flat[r].astype(np.float64)
+        order = sorted(range(V), key=lambda t: (-row[t], t))
+        keep = V if top_k <= 0 else min(int(top_k), V)
+        if 0.0 < top_p < 1.0:
+            z = row[order[:keep]] / T
+            pr = np.exp(z - z.max())
+            cum = np.cumsum(pr) / pr.sum()
+            keep = min(keep, int(np.searchsorted(cum, top_p, side="left")) + 1)
+        idx = np.array(order[:keep])
+        out[r, idx] = flat[r, idx]
+    return out.reshape(x.shape)
+
+
+def verify_accept_filtered(target, draft, tokens, parent, max_depth: int, T: float, seed: int,
+                           top_k: int = 0, top_p: float = 0.0, draft_row=None, u_override=None):
+    """verify_accept with q and p replaced by their top-k / top-p filtered versions
+    (filter_logits, the same filter for both); the walk itself is unchanged."""
+    if T > 0:
+        target = filter_logits(target, T, top_k, top_p)
+        draft = filter_logits(draft, T, top_k, top_p)
+    return verify_accept(target, draft, tokens, parent, max_depth, T, seed, draft_row=draft_row,
+                         u_override=u_override)
+
+
 def sample_rows(logits, T: float, seed: int):
     """One token per row of logits [B, rows, V] from softmax(row / T) (argmax at T = 0)."""
     x = _c(logits, np.float32)

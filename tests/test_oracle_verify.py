@@ -404,3 +404,49 @@ def test_d2t_leviathan_chisquare_v8():
     assert (res["status"] == 0).all()
     first = res["emit"][:, 0]
     assert _chisq_pvalue(np.bincount(first, minlength=V), _softmax(_logits(q))) > 1e-3
+
+
+# ------------------------------------------------------------------ top-k / top-p filtering
+def test_filter_keeps_top_k_then_nucleus_and_renormalises():
+    """Hand-checked row: probabilities 0.4, 0.3, 0.2, 0.1 (tokens 2, 0, 3, 1)."""
+    p = np.array([0.3, 0.1, 0.4, 0.2])
+    row = _logits(p)[None]
+    keep = lambda k, tp: np.isfinite(oracle.filter_logits(row, 1.0, k, tp))[0]  # noqa: E731
+    assert keep(0, 0.0).tolist() == [True, True, True, True]
+    assert keep(2, 0.0).tolist() == [True, False, True, False]          # tokens 2 and 0
+    assert keep(0, 0.5).tolist() == [True, False, True, False]          # 0.4 < 0.5 <= 0.7
+    assert keep(0, 0.39).tolist() == [False, False, True, False]        # 0.4 reaches 0.39
+    assert keep(0, 0.75).tolist() == [True, False, True, True]          # 0.9 >= 0.75
+    assert keep(3, 0.95).tolist() == [True, False, True, True]          # top-3 mass 0.9: all 3
+    # top-p over what top-k kept: 0.4 / 0.7 = 0.571 < 0.6 <= 1.0
+    assert keep(2, 0.6).tolist() == [True, False, True, False]
+    assert keep(2, 0.5).tolist() == [False, False, True, False]         # 0.571 >= 0.5
+    # ties: lower token first
+    tie = np.log(np.array([0.25, 0.25, 0.25, 0.25]))[None].astype(np.float32)
+    assert np.isfinite(oracle.filter_logits(tie, 1.0, 2, 0.0))[0].tolist() == [True, True, False,
+                                                                               False]
+    # temperature enters before the nucleus: at T = 4 the row is flatter
+    assert keep(0, 0.5).sum() == 2
+    assert np.isfinite(oracle.filter_logits(row, 4.0, 0, 0.5))[0].sum() == 2
+
+
+def test_filtered_walk_is_lossless_for_the_filtered_target():
+    """One-draft chains, drafts from the filtered p: the emitted token is distributed as the
+    filtered q (top-k = 5 and top-p = 0.8 on V = 8), 50,000 steps."""
+    V, B = 8, 50_000
+    g = W.rng(11, 51)
+    q = g.dirichlet(np.ones(V))
+    p = g.dirichlet(np.ones(V))
+    k, tp = 5, 0.8
+    qf = _softmax(oracle.filter_logits(_logits(q)[None], 1.0, k, tp)[0])
+    pf = _softmax(oracle.filter_logits(_logits(p)[None], 1.0, k, tp)[0])
+    tgt = np.broadcast_to(_logits(q), (B, 2, V))
+    drf = np.broadcast_to(_logits(p), (B, 2, V))
+    tok = np.full((B, 2), -1, np.int32)
+    tok[:, 1] = g.choice(V, size=B, p=pf)
+    par = np.broadcast_to(W.chain_tree(2), (B, 2))
+    res = oracle.verify_accept_filtered(tgt, drf, tok, par, 1, 1.0, 91, top_k=k, top_p=tp)
+    assert (res["status"] == 0).all()
+    first = res["emit"][:, 0]
+    assert _chisq_pvalue(np.bincount(first, minlength=V), qf) > 1e-3
+    assert (qf > 0).sum() < V          # the filter removed something

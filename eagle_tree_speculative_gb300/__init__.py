@@ -125,7 +125,8 @@ def eagle_d2t_inverse(d2t, V, t2d=None, dev_status=None, stream=None):
 
 def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, temperature, seed,
                         draft_row=None, accept_len=None, path=None, emit=None, row_stats=None,
-                        dev_status=None, stream=None, t2d=None):
+                        dev_status=None, stream=None, t2d=None, top_k=0, top_p=0.0,
+                        workspace=None):
     """Returns (accept_len [B], path [B,D+1], emit [B,D+1]) int32 tensors.  With t2d
     (from eagle_d2t_inverse) the draft rows are over the draft vocabulary
     [B, R, Vd] and tokens are target ids.  target_logits may be a pinned host tensor:
@@ -149,6 +150,20 @@ def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, 
     emit = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if emit is None else emit
     if row_stats is not None:
         _dev(row_stats, "row_stats", torch.float32)
+    if (top_k or top_p) and temperature > 0:
+        if t2d is not None:
+            raise ValueError("top-k / top-p filtering with a draft vocabulary is not offered")
+        need = int(lib().eagle_verify_filter_workspace_size(B, n, R))
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        _dev(workspace, "workspace")
+        _check("eagle_verify_accept_filtered", lib().eagle_verify_accept_filtered(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_row), _ptr(tokens), _ptr(parent),
+            B, n, V, R, D, float(temperature), int(seed) & (2**64 - 1), int(top_k), float(top_p),
+            _ptr(accept_len), _ptr(path), _ptr(emit), _ptr(row_stats), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(_status(dev_status, dev)),
+            _stream(stream)))
+        return accept_len, path, emit
     if t2d is not None:
         _dev(t2d, "t2d", torch.int32)
         _check("eagle_verify_accept_d2t", lib().eagle_verify_accept_d2t(

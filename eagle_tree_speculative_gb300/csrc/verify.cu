@@ -25,6 +25,29 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Top-k / top-p filter of one row at temperature T > 0 (reading of eagenerate's top_k and
+// top_p arguments: rank the row's tokens by probability, lower token first on ties; top-k
+// keeps the first k; top-p keeps the shortest prefix of what top-k kept whose probability,
+// renormalised over that set, reaches top_p).  The kept set is {t : key(l_t) > key, or
+// key(l_t) == key and t <= idx}, key() the order-preserving integer image of a float; S is
+// sum 2^((l - lmax) c) over the kept set.  bad != 0: the row holds NaN or +inf.
+struct FilterParam {
+    float lmax, S;
+    uint32_t key;
+    int32_t idx;
+    int32_t bad, pad0, pad1, pad2;
+};
+
+__device__ __forceinline__ uint32_t order_key(float l) {
+    const uint32_t u = __float_as_uint(l);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ bool filter_keeps(const FilterParam& f, int t, float l) {
+    const uint32_t k = order_key(l);
+    return k > f.key || (k == f.key && t <= f.idx);
+}
+
 struct VerifyArgs {
     const float* target;
     const float* draft;
@@ -42,6 +65,8 @@ struct VerifyArgs {
     int32_t* dev_status;
     int Vd;                // draft-row length (= V without a draft vocabulary)
     const int32_t* t2d;    // target id -> draft id or -1 (draft vocabulary only)
+    const FilterParam* fq; // per target row [B * n], filtered walk only
+    const FilterParam* fp; // per draft row [B * R], filtered walk only
 };
 
 // Softmax statistics of a row at temperature T, kept over the raw logits:
@@ -346,7 +371,7 @@ __device__ __forceinline__ float race_exponential(uint32_t w) {
 }
 
 // Exponential race over the weights w_t (any positive scale): argmax_t w_t / E_t,
-// E_t = -ln u'_t.  `weight(lq, lp)` gives w_t from the two logits of token t; the
+// E_t = -ln u'_t.  `weight(lq, lp, t)` gives w_t from the two logits of token t; the
 // generator is only run for 4-token blocks with some positive weight.
 template <int NT, bool D2T, class Weight>
 __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, int lo, int hi,
@@ -357,7 +382,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
         const float ax[4] = {a4.x, a4.y, a4.z, a4.w}, bx[4] = {b4.x, b4.y, b4.z, b4.w};
         float rr[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) rr[e] = weight(ax[e], bx[e]);
+        for (int e = 0; e < 4; ++e) rr[e] = weight(ax[e], bx[e], t + e);
         if (rr[0] > 0.f || rr[1] > 0.f || rr[2] > 0.f || rr[3] > 0.f) {
             const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
             const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
@@ -388,7 +413,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
         }
     } else {
         for (int t = lo + (int)threadIdx.x; t < hi; t += NT) {
-            const float rr = weight(qrow[t], prow.one(t));
+            const float rr = weight(qrow[t], prow.one(t), t);
             if (rr > 0.f) {
                 const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
                 const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
@@ -401,7 +426,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
 }
 
 // ---------------------------------------------------------------------------
-template <int CS, int NT, bool D2T>
+template <int CS, int NT, bool D2T, bool FILT>
 __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
     using C = Cluster<CS, NT>;
     __shared__ VerifySmem<NT> sm;
@@ -477,10 +502,32 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
         if (a.T > 0.f) {
             const float* prow = kids ? drf_b + (int64_t)sm.row[v] * Vdl : nullptr;
             const PRow<D2T> pr{prow, a.t2d};
+            // filtered walk: this node's row filters; logits outside them read as -inf
+            FilterParam fqv{}, fpv{};
+            if constexpr (FILT) {
+                fqv = a.fq[(int64_t)b * n + v];
+                if (prow) fpv = a.fp[(int64_t)b * a.R + sm.row[v]];
+            }
+            auto mq = [&](int t, float l) -> float {
+                if constexpr (FILT) return filter_keeps(fqv, t, l) ? l : -INFINITY;
+                else return l;
+            };
+            auto mp = [&](int t, float l) -> float {
+                if constexpr (FILT) return filter_keeps(fpv, t, l) ? l : -INFINITY;
+                else return l;
+            };
             // ---------- pass: statistics of q(v) and p(v) ----------
             RowStat Q{-INFINITY, 0.f}, P{-INFINITY, 0.f};
             int bad = 0;
-            if constexpr (D2T) {
+            if constexpr (FILT) {
+                // statistics of the filtered rows come with the filters
+                Q = RowStat{fqv.lmax, fqv.S};
+                bad = fqv.bad;
+                if (prow) {
+                    P = RowStat{fpv.lmax, fpv.S};
+                    bad |= fpv.bad;
+                }
+            } else if constexpr (D2T) {
                 // q over the target slice, p over the draft slice
                 row_stats_slice<NT>(qrow, lo, hi, vec4, c, Q, bad);
                 if (prow) row_stats_slice<NT>(prow, plo, phi, vec4, c, P, bad);
@@ -530,7 +577,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                     }
                 }
             }
-            C::stats(sm, buf, Q, P, bad, c);
+            if constexpr (!FILT) C::stats(sm, buf, Q, P, bad, c);
             if (bad || Q.lmax == -INFINITY || (prow && P.lmax == -INFINITY)) {
                 err = EAGLE_DEV_NONFINITE;
                 break;
@@ -551,7 +598,7 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
             for (int ch = v + 1; ch < n && kids; ++ch) {
                 if (sm.parent[ch] != v) continue;
                 const int x = sm.tok[ch];
-                const float lq = qrow[x], lp = pr.one(x);
+                const float lq = mq(x, qrow[x]), lp = mp(x, pr.one(x));
                 const float px = prob_of(lp, P.lmax, ip, c);
                 const float r = resid_weight(lq, lp, Q, iq, P, ip, c, rs);
                 const float u = accept_uniform(a.seed, (uint32_t)b, (uint32_t)ch);
@@ -571,6 +618,9 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                 }
                 // ---------- pass: the next residual's normaliser ----------
                 const float cnext = rs.rc + rs.rD;
+                auto nr = [&](float lq2, float lp2, int t2) {
+                    return next_resid(mq(t2, lq2), mp(t2, lp2), Q, iq, P, ip, c, cnext);
+                };
                 float s = 0.f;
                 if (vec4) {
                     int t = lo + 4 * tid;
@@ -583,22 +633,20 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                         }
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
-                            s += next_resid(a4[u].x, b4[u].x, Q, iq, P, ip, c, cnext) +
-                                 next_resid(a4[u].y, b4[u].y, Q, iq, P, ip, c, cnext) +
-                                 next_resid(a4[u].z, b4[u].z, Q, iq, P, ip, c, cnext) +
-                                 next_resid(a4[u].w, b4[u].w, Q, iq, P, ip, c, cnext);
+                            s += nr(a4[u].x, b4[u].x, t + 4 * u * NT) +
+                                 nr(a4[u].y, b4[u].y, t + 4 * u * NT + 1) +
+                                 nr(a4[u].z, b4[u].z, t + 4 * u * NT + 2) +
+                                 nr(a4[u].w, b4[u].w, t + 4 * u * NT + 3);
                     }
                     for (; t < hi; t += 4 * NT) {
                         const float4 a4 = __ldg(reinterpret_cast<const float4*>(qrow + t));
                         const float4 b4 = pr.four(t);
-                        s += next_resid(a4.x, b4.x, Q, iq, P, ip, c, cnext) +
-                             next_resid(a4.y, b4.y, Q, iq, P, ip, c, cnext) +
-                             next_resid(a4.z, b4.z, Q, iq, P, ip, c, cnext) +
-                             next_resid(a4.w, b4.w, Q, iq, P, ip, c, cnext);
+                        s += nr(a4.x, b4.x, t) + nr(a4.y, b4.y, t + 1) + nr(a4.z, b4.z, t + 2) +
+                             nr(a4.w, b4.w, t + 3);
                     }
                 } else {
                     for (int t = lo + tid; t < hi; t += NT)
-                        s += next_resid(qrow[t], pr.one(t), Q, iq, P, ip, c, cnext);
+                        s += nr(qrow[t], pr.one(t), t);
                 }
                 const float S = C::sum(sm, buf, s);
                 if (S > 0.f) rs = Residual{cnext, S, 1.f / S};   // else q_cur stays as it is
@@ -611,22 +659,25 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                 // weights max(0, r_j - p), up to the positive factor 1 / D_j
                 const float cnext = rs.rc + rs.rD;
                 best = race_slice<NT>(qrow, pr, lo, hi, vec4, (uint32_t)b, k0, k1,
-                                      [&](float lq2, float lp2) {
-                                          return next_resid(lq2, lp2, Q, iq, P, ip, c, cnext);
+                                      [&](float lq2, float lp2, int t2) {
+                                          return next_resid(mq(t2, lq2), mp(t2, lp2), Q, iq, P, ip,
+                                                            c, cnext);
                                       });
                 best = C::argmax(sm, buf, best, bad2);
                 if (best.i == 0x7fffffff) {
                     // the clamped residual is all zero: keep q_cur (= r_j)
                     best = race_slice<NT>(qrow, pr, lo, hi, vec4, (uint32_t)b, k0, k1,
-                                          [&](float lq2, float lp2) {
-                                              return resid_weight(lq2, lp2, Q, iq, P, ip, c, rs);
+                                          [&](float lq2, float lp2, int t2) {
+                                              return resid_weight(mq(t2, lq2), mp(t2, lp2), Q, iq, P,
+                                                                  ip, c, rs);
                                           });
                     best = C::argmax(sm, buf, best, bad2);
                 }
             } else {
                 best = race_slice<NT>(qrow, pr, lo, hi, vec4, (uint32_t)b, k0, k1,
-                                      [&](float lq2, float lp2) {
-                                          return resid_weight(lq2, lp2, Q, iq, P, ip, c, rs);
+                                      [&](float lq2, float lp2, int t2) {
+                                          return resid_weight(mq(t2, lq2), mp(t2, lp2), Q, iq, P, ip,
+                                                              c, rs);
                                       });
                 best = C::argmax(sm, buf, best, bad2);
             }
@@ -793,6 +844,237 @@ softmax_stats_kernel(const float* __restrict__ logits, int64_t rows, int V, floa
     }
 }
 
+// ---------------------------------------------------------------------------
+// Row filters for the filtered walk (top-k, then top-p over what top-k kept): one CTA
+// per row.  The cut is found by a radix select over the rows' order keys (11-bit
+// digits, most significant first), with per-bin counts and fixed-point masses
+// (2^((l - max) c) scaled by 2^40, integer sums, so the decisions do not depend on
+// the order of the atomics); ties at the cut go to the lower token.
+// ---------------------------------------------------------------------------
+constexpr int kFiltThreads = 256;
+constexpr int kFiltBins = 2048;
+constexpr int kFiltMaxV = 1 << 22;              // the index select uses two 11-bit digits
+
+struct FiltSmem {
+    unsigned int cnt[kFiltBins];
+    unsigned long long mass[kFiltBins];
+    unsigned int wcnt[kFiltThreads / 32];
+    unsigned long long wmass[kFiltThreads / 32];
+    float redf[kFiltThreads / 32];
+    int redi[kFiltThreads / 32];
+    int found_bin;
+    unsigned int found_cnt;
+    unsigned long long found_mass;
+    int imax;
+};
+
+__device__ __forceinline__ unsigned long long fixed_mass(float l, float lmax, float c) {
+    return __float2ull_rz(exp2f((l - lmax) * c) * 0x1p40f);     // exact: <= 2^40, 24-bit mantissa
+}
+
+__device__ __forceinline__ bool elig(uint32_t k, int t, uint32_t k0, int i0) {
+    return k > k0 || (k == k0 && t <= i0);
+}
+
+// Scan the bins in rank order (descending when DESC) for the bin where the running metric
+// (count, or mass when MASS) first reaches `remaining` (>= 1, <= the bins' total).  Writes
+// found_bin and the count and mass of the bins before it.
+template <bool MASS, bool DESC>
+__device__ void scan_bins(FiltSmem& sm, int nb, unsigned long long remaining) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = nb / kFiltThreads;
+    const int first = DESC ? nb - 1 - tid * per : tid * per;
+    if (tid == 0) { sm.found_bin = 0; sm.found_cnt = 0u; sm.found_mass = 0ull; }
+    unsigned int lc = 0;
+    unsigned long long lm = 0;
+    for (int j = 0; j < per; ++j) {
+        const int bin = DESC ? first - j : first + j;
+        lc += sm.cnt[bin];
+        lm += sm.mass[bin];
+    }
+    unsigned int ic = lc;
+    unsigned long long im = lm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int yc = __shfl_up_sync(0xffffffffu, ic, o);
+        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
+        if (lane >= o) { ic += yc; im += ym; }
+    }
+    if (lane == 31) { sm.wcnt[warp] = ic; sm.wmass[warp] = im; }
+    __syncthreads();
+    unsigned int rc = ic - lc;
+    unsigned long long rm = im - lm;
+    for (int w = 0; w < warp; ++w) { rc += sm.wcnt[w]; rm += sm.wmass[w]; }
+    const unsigned long long before = MASS ? rm : rc, mine = MASS ? lm : lc;
+    if (before < remaining && before + mine >= remaining) {
+        for (int j = 0; j < per; ++j) {
+            const int bin = DESC ? first - j : first + j;
+            const unsigned long long v = MASS ? sm.mass[bin] : sm.cnt[bin];
+            if ((MASS ? rm : rc) + v >= remaining) {
+                sm.found_bin = bin;
+                sm.found_cnt = rc;
+                sm.found_mass = rm;
+                break;
+            }
+            rc += sm.cnt[bin];
+            rm += sm.mass[bin];
+        }
+    }
+    __syncthreads();
+}
+
+struct Cut {
+    uint32_t key;
+    int idx;
+    unsigned long long mass_upto;     // mass of the elements up to and including the cut
+};
+
+// Among the row's elements eligible under (k0, i0), in rank order (key desc, index asc),
+// the element at which the running count (MASS false) or fixed-point mass (MASS true)
+// first reaches `target` (1 <= target <= the eligible total).
+template <bool MASS>
+__device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, float c,
+                            unsigned long long target, uint32_t k0, int i0) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0u, pmask = 0u;
+    unsigned long long mb = 0ull, remaining = target, m_eq_total = 0ull;
+    unsigned int n_eq = 0u;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        for (int i = tid; i < nb; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+        __syncthreads();
+        for (int t = tid; t < V; t += kFiltThreads) {
+            const float l = x[t];
+            const uint32_t k = order_key(l);
+            if ((k & pmask) != prefix || !elig(k, t, k0, i0)) continue;
+            const int bin = (int)((k >> shift) & (uint32_t)(nb - 1));
+            atomicAdd(&sm.cnt[bin], 1u);
+            atomicAdd(&sm.mass[bin], fixed_mass(l, lmax, c));
+        }
+        __syncthreads();
+        scan_bins<MASS, true>(sm, nb, remaining);
+        const int bin = sm.found_bin;
+        remaining -= MASS ? sm.found_mass : (unsigned long long)sm.found_cnt;
+        mb += sm.found_mass;
+        if (pass == 2) { n_eq = sm.cnt[bin]; m_eq_total = sm.mass[bin]; }
+        prefix |= (uint32_t)bin << shift;
+        pmask |= (uint32_t)(nb - 1) << shift;
+        __syncthreads();
+    }
+    // the elements whose key is the cut's: they share one value, so one mass each; the
+    // cut keeps the first `need` of them by index
+    if (n_eq == 0u) n_eq = 1u;                         // (cannot happen: the cut's bin is not empty)
+    const unsigned long long m_eq = m_eq_total / n_eq;
+    unsigned long long need = MASS ? (remaining + m_eq - 1ull) / m_eq : remaining;
+    if (need > n_eq) need = n_eq;
+    int idx;
+    if (need == n_eq) {
+        if (tid == 0) sm.imax = -1;
+        __syncthreads();
+        for (int t = tid; t < V; t += kFiltThreads)
+            if (order_key(x[t]) == prefix && elig(prefix, t, k0, i0)) atomicMax(&sm.imax, t);
+        __syncthreads();
+        idx = sm.imax;
+        __syncthreads();
+    } else {
+        uint32_t iprefix = 0u, imask = 0u;
+        unsigned long long rem = need;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int shift = pass == 0 ? 11 : 0;
+            for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+            __syncthreads();
+            for (int t = tid; t < V; t += kFiltThreads) {
+                if (((uint32_t)t & imask) != iprefix) continue;
+                const uint32_t k = order_key(x[t]);
+                if (k != prefix || !elig(k, t, k0, i0)) continue;
+                atomicAdd(&sm.cnt[((uint32_t)t >> shift) & (kFiltBins - 1)], 1u);
+            }
+            __syncthreads();
+            scan_bins<false, false>(sm, kFiltBins, rem);
+            rem -= sm.found_cnt;
+            iprefix |= (uint32_t)sm.found_bin << shift;
+            imask |= (uint32_t)(kFiltBins - 1) << shift;
+            __syncthreads();
+        }
+        idx = (int)iprefix;
+    }
+    return Cut{prefix, idx, mb + need * m_eq};
+}
+
+__global__ void __launch_bounds__(kFiltThreads)
+row_filter_kernel(const float* __restrict__ target, int nq, const float* __restrict__ draft, int V,
+                  float c, int top_k, float top_p, FilterParam* fq, FilterParam* fp) {
+    __shared__ FiltSmem sm;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t r = blockIdx.x;
+    const bool isq = r < nq;
+    const float* x = isq ? target + r * (int64_t)V : draft + (r - nq) * (int64_t)V;
+    FilterParam* out = isq ? fq + r : fp + (r - nq);
+    float mx = -INFINITY;
+    int bad = 0;
+    for (int t = tid; t < V; t += kFiltThreads) {
+        const float l = x[t];
+        bad |= (l != l) | (l == INFINITY);
+        mx = fmaxf(mx, l);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) { sm.redf[warp] = mx; sm.redi[warp] = bad; }
+    __syncthreads();
+    float lmax = -INFINITY;
+    int bd = 0;
+    for (int w = 0; w < kFiltThreads / 32; ++w) { lmax = fmaxf(lmax, sm.redf[w]); bd |= sm.redi[w]; }
+    __syncthreads();
+    if (bd || lmax == -INFINITY) {
+        if (tid == 0) *out = FilterParam{lmax, 0.f, 0u, 0, 1, 0, 0, 0};
+        return;
+    }
+    uint32_t key = 0u;                 // keep everything
+    int idx = 0x7fffffff;
+    unsigned long long total = 0ull;
+    bool have_total = false;
+    if (top_k > 0 && top_k < V) {
+        const Cut k = block_select<false>(sm, x, V, lmax, c, (unsigned long long)top_k, 0u, 0x7fffffff);
+        key = k.key;
+        idx = k.idx;
+        total = k.mass_upto;
+        have_total = true;
+    }
+    if (top_p > 0.f && top_p < 1.f) {
+        if (!have_total) {
+            unsigned long long m = 0ull;
+            for (int t = tid; t < V; t += kFiltThreads) m += fixed_mass(x[t], lmax, c);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+            if (lane == 0) sm.wmass[warp] = m;
+            __syncthreads();
+            for (int w = 0; w < kFiltThreads / 32; ++w) total += sm.wmass[w];
+            __syncthreads();
+        }
+        unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
+        tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
+        const Cut p = block_select<true>(sm, x, V, lmax, c, tgt, key, idx);
+        idx = p.key == key ? min(p.idx, idx) : p.idx;
+        key = p.key;
+    }
+    // S over the kept set; per-thread sums combined in a fixed order
+    float s = 0.f;
+    for (int t = tid; t < V; t += kFiltThreads) {
+        const float l = x[t];
+        if (elig(order_key(l), t, key, idx)) s += exp2f((l - lmax) * c);
+    }
+    s = warp_sum(s);
+    if (lane == 0) sm.redf[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        float S = 0.f;
+        for (int w = 0; w < kFiltThreads / 32; ++w) S += sm.redf[w];
+        *out = FilterParam{lmax, S, key, idx, 0, 0, 0, 0};
+    }
+}
+
 int verify_cluster_size(int B) {
     static int forced = -1;
     if (forced < 0) {
@@ -809,14 +1091,14 @@ int verify_cluster_size(int B) {
 
 constexpr int kVerifyThreads = 256;
 
-template <bool D2T>
+template <bool D2T, bool FILT>
 cudaError_t launch_walk(const VerifyArgs& a, cudaStream_t s) {
     constexpr int NT = kVerifyThreads;
     switch (verify_cluster_size(a.B)) {
-        case 8: return launch_clustered(verify_walk_kernel<8, NT, D2T>, a.B, 8, NT, 0, s, a);
-        case 4: return launch_clustered(verify_walk_kernel<4, NT, D2T>, a.B, 4, NT, 0, s, a);
-        case 2: return launch_clustered(verify_walk_kernel<2, NT, D2T>, a.B, 2, NT, 0, s, a);
-        default: return launch_clustered(verify_walk_kernel<1, NT, D2T>, a.B, 1, NT, 0, s, a);
+        case 8: return launch_clustered(verify_walk_kernel<8, NT, D2T, FILT>, a.B, 8, NT, 0, s, a);
+        case 4: return launch_clustered(verify_walk_kernel<4, NT, D2T, FILT>, a.B, 4, NT, 0, s, a);
+        case 2: return launch_clustered(verify_walk_kernel<2, NT, D2T, FILT>, a.B, 2, NT, 0, s, a);
+        default: return launch_clustered(verify_walk_kernel<1, NT, D2T, FILT>, a.B, 1, NT, 0, s, a);
     }
 }
 
@@ -837,7 +1119,8 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
                            const int32_t* tokens, const int32_t* parent, int B, int n, int V, int R,
                            int Vd, const int32_t* t2d, int max_depth, float temperature, uint64_t seed,
                            int32_t* accept_len, int32_t* path, int32_t* emit, float* row_stats,
-                           int32_t* dev_status, eagle_stream_t stream) {
+                           int32_t* dev_status, eagle_stream_t stream, int top_k = 0,
+                           float top_p = 0.f, void* workspace = nullptr, size_t ws_bytes = 0) {
     if (B < 0 || n < 1 || V < 1 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
     if (n > kMaxNodes || max_depth > kMaxNodes) return EAGLE_ERR_SHAPE;
     if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
@@ -850,9 +1133,28 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
     if (B == 0) return EAGLE_OK;
     const float c = temperature > 0.f ? kLog2e / temperature : 0.f;
     VerifyArgs a{target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, max_depth,
-                 temperature, c, seed, accept_len, path, emit, row_stats, dev_status, Vd, t2d};
+                 temperature, c, seed, accept_len, path, emit, row_stats, dev_status, Vd, t2d,
+                 nullptr, nullptr};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = t2d ? launch_walk<true>(a, s) : launch_walk<false>(a, s);
+    const bool filt = temperature > 0.f && ((top_k > 0 && top_k < V) || (top_p > 0.f && top_p < 1.f));
+    cudaError_t e;
+    if (filt) {
+        if (t2d) return EAGLE_ERR_INVALID_ARG;             // filtering with a draft vocabulary: not offered
+        if (V > kFiltMaxV) return EAGLE_ERR_SHAPE;
+        const size_t need = (size_t)B * (n + R) * sizeof(FilterParam);
+        if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+            return EAGLE_ERR_CAPACITY;
+        FilterParam* fq = static_cast<FilterParam*>(workspace);
+        FilterParam* fp = fq + (size_t)B * n;
+        row_filter_kernel<<<(unsigned)(B * (n + R)), kFiltThreads, 0, s>>>(
+            target_logits, B * n, draft_logits, V, c, top_k, top_p, fq, fp);
+        EAGLE_CHECK_LAUNCH();
+        a.fq = fq;
+        a.fp = fp;
+        e = launch_walk<false, true>(a, s);
+    } else {
+        e = t2d ? launch_walk<true, false>(a, s) : launch_walk<false, false>(a, s);
+    }
     return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
@@ -885,6 +1187,27 @@ extern "C" eagle_status eagle_verify_accept_d2t(const float* target_logits, cons
     return verify_common(target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, Vd, t2d,
                          max_depth, temperature, seed, accept_len, path, emit, row_stats, dev_status,
                          stream);
+}
+
+extern "C" size_t eagle_verify_filter_workspace_size(int B, int n, int R) {
+    if (B < 0 || n < 1 || R < 1) return 0;
+    return (size_t)B * (n + R) * sizeof(FilterParam);
+}
+
+extern "C" eagle_status eagle_verify_accept_filtered(const float* target_logits,
+                                                     const float* draft_logits,
+                                                     const int32_t* draft_row, const int32_t* tokens,
+                                                     const int32_t* parent, int B, int n, int V,
+                                                     int R, int max_depth, float temperature,
+                                                     uint64_t seed, int top_k, float top_p,
+                                                     int32_t* accept_len, int32_t* path,
+                                                     int32_t* emit, float* row_stats,
+                                                     void* workspace, size_t ws_bytes,
+                                                     int32_t* dev_status, eagle_stream_t stream) {
+    if (top_k < 0 || !(top_p >= 0.f) || !(top_p < INFINITY)) return EAGLE_ERR_INVALID_ARG;
+    return verify_common(target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, V,
+                         nullptr, max_depth, temperature, seed, accept_len, path, emit, row_stats,
+                         dev_status, stream, top_k, top_p, workspace, ws_bytes);
 }
 
 extern "C" eagle_status eagle_d2t_inverse(const int32_t* d2t, int Vd, int V, int32_t* t2d,

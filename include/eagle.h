@@ -141,6 +141,37 @@ eagle_status eagle_verify_accept(const float* target_logits, const float* draft_
                                  float* row_stats, int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * eagle_verify_accept_filtered -- eagle_verify_accept with top-k / top-p
+ * filtering.  Guide "一次 eagenerate 调用的完整流转": eagenerate takes
+ * temperature, top_p and top_k (0 = off); the pages give no further rule.
+ * Reading: at T > 0, each row's tokens are ranked by probability (logit desc,
+ * lower token first on ties); top-k keeps the first top_k; top-p then keeps the
+ * shortest prefix of that order whose probability, renormalised over what top-k
+ * kept, reaches top_p (at least one token).  q and p are each filtered this way
+ * and renormalised, and the walk, uniforms and outputs are those of
+ * eagle_verify_accept on the filtered distributions (row_stats then hold the
+ * filtered sums).  top_k = 0 or >= V and top_p = 0 or >= 1 switch a filter off;
+ * at T = 0 (greedy) both are ignored.
+ *   workspace  device, >= eagle_verify_filter_workspace_size(B, n, R) bytes,
+ *              16-byte aligned; needed only when a filter is on (one 32-byte
+ *              filter per target and draft row, computed for every row first).
+ * Errors: EAGLE_ERR_INVALID_ARG for top_k < 0 or top_p < 0 / not finite;
+ * EAGLE_ERR_CAPACITY for a missing or small workspace; EAGLE_ERR_SHAPE for
+ * V > 4194304.  The filter decisions use the probability mass in 2^-40 fixed
+ * point, so a top-p cut within ~1e-7 of top_p may fall one token apart from an
+ * exact computation.
+ * ------------------------------------------------------------------------- */
+size_t eagle_verify_filter_workspace_size(int B, int n, int R);
+eagle_status eagle_verify_accept_filtered(const float* target_logits, const float* draft_logits,
+                                          const int32_t* draft_row, const int32_t* tokens,
+                                          const int32_t* parent, int B, int n, int V, int R,
+                                          int max_depth, float temperature, uint64_t seed,
+                                          int top_k, float top_p, int32_t* accept_len,
+                                          int32_t* path, int32_t* emit, float* row_stats,
+                                          void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                          eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Draft vocabulary (EAGLE-3).  Guide "EAGLE-3：取消特征约束…": the draft head may
  * have its own LM head over a smaller vocabulary of Vd ids, and a table d2t
  * (int32 [Vd]) returns each draft id d to the target id d + d2t[d].

@@ -215,7 +215,7 @@ def filter_logits(logits, T: float, top_k: int = 0, top_p: float = 0.0):
     out = np.full_like(flat, -np.inf)
     for r in range(flat.shape[0]):
         row = flat[r].astype(np.float64)
-        order = sorted(range(V), key=lambda t: (-row[t], t))
+        order = np.lexsort((np.arange(V), -row))          # logit desc, then token asc
         keep = V if top_k <= 0 else min(int(top_k), V)
         if 0.0 < top_p < 1.0:
             z = row[order[:keep]] / T

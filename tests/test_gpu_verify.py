@@ -293,3 +293,44 @@ def test_target_logits_in_pinned_host_memory_give_the_same_walk():
     assert int(st.item()) == 0
     for a, b in zip(dev_out, host_out):
         assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- top-k / top-p filtering
+@pytest.mark.parametrize("V,top_k,top_p,quant", [(32000, 50, 0.0, 0.0), (32000, 0, 0.9, 0.0),
+                                                 (32000, 20, 0.8, 0.0), (1003, 7, 0.0, 0.5),
+                                                 (1003, 0, 0.7, 0.5), (1003, 30, 0.95, 0.25)])
+def test_filtered_trees_match_oracle(V, top_k, top_p, quant):
+    """Top-k / top-p filtered walk on 48-node depth-6 trees, B = 8, against
+    oracle.verify_accept_filtered.  quant > 0 rounds every logit to a multiple of quant,
+    so cuts fall inside runs of equal logits (the lower token is kept first).  The
+    visited rows' filtered sums (row_stats) are checked to 1e-5."""
+    E = _gpu()
+    cfg = W.CONFIGS["sweep_70b"]
+    tgt, drows, tree = _tree_case(cfg, 8, seed=53, V=V)
+    if quant:
+        tgt = (np.round(tgt / quant) * quant).astype(np.float32)
+        drows = (np.round(drows / quant) * quant).astype(np.float32)
+    ref = oracle.verify_accept_filtered(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, 1.0,
+                                        seed=29, top_k=top_k, top_p=top_p,
+                                        draft_row=tree["draft_row"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs = torch.full((2, 8, cfg.n, 2), float("nan"), device="cuda")
+    acc, path, emit = E.eagle_verify_accept(
+        _cuda(tgt), _cuda(drows), _cuda(tree["tokens"]), _cuda(tree["parent"]), cfg.depth, 1.0, 29,
+        draft_row=_cuda(tree["draft_row"]), row_stats=rs, dev_status=st, top_k=top_k, top_p=top_p)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and (ref["status"] == 0).all()
+    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy())
+    assert_tie_budget(dec, ties)
+    r = rs.cpu().numpy()
+    ft = oracle.filter_logits(tgt, 1.0, top_k, top_p)
+    m, Z, _, _ = oracle.softmax_rows(ft, 1.0)
+    seen = ~np.isnan(r[0, :, :, 0])
+    assert seen.sum() >= 8
+    np.testing.assert_allclose(r[0][..., 1][seen], Z[seen], rtol=1e-5)
+    fd = oracle.filter_logits(drows, 1.0, top_k, top_p)
+    _, Zd, _, _ = oracle.softmax_rows(fd, 1.0)
+    rows = tree["draft_row"]
+    seen = ~np.isnan(r[1, :, :, 0])
+    b_i, n_i = np.nonzero(seen)
+    np.testing.assert_allclose(r[1, b_i, n_i, 1], Zd[b_i, rows[b_i, n_i]], rtol=1e-5)

@@ -630,7 +630,8 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
-KERNEL_CASES = ("gemm", "topk", "fused", "attn", "verify", "compact", "softmax")
+KERNEL_CASES = ("gemm", "topk", "fused", "attn", "verify", "verify_filtered", "compact",
+                "softmax")
 
 
 def kernel_case(name, reps):
@@ -645,6 +646,7 @@ def kernel_case(name, reps):
                only the tiles able to hold a row's top-10
       attn     tree attention, one layer, B=64, 32/8 heads, KV 4096, 60 nodes
       verify   verify-and-accept, B=32, 60 nodes, V=128256, T=1
+      verify_filtered  the same with top-k 50 and top-p 0.9 (row filters, then the walk)
       compact  KV compaction, 32 layers, B=4 (8 kv heads, Lmax 4156)
       softmax  softmax statistics of [32, 60, 128256] target logits
     """
@@ -710,13 +712,19 @@ def kernel_case(name, reps):
         wsb = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
         fn = lambda: E.eagle_tree_attn(q, kc, vc, kv_len, parent, out=out,  # noqa: E731
                                        workspace=wsb, dev_status=st)
-    elif name in ("verify", "softmax"):
+    elif name in ("verify", "verify_filtered", "softmax"):
         B = 32
         logits, _, tok, par, row = expanded(B)
         target = synth_target(torch, logits, row, c.sigma, leaf_std, g)
         if name == "verify":
             fn = lambda: E.eagle_verify_accept(target, logits, tok, par, c.depth, 1.0, 7,  # noqa
                                                draft_row=row, dev_status=st)
+        elif name == "verify_filtered":
+            ws = torch.empty(E.verify_filter_workspace_size(B, c.n, c.R), dtype=torch.uint8,
+                             device=dev)
+            fn = lambda: E.eagle_verify_accept(target, logits, tok, par, c.depth, 1.0, 7,  # noqa
+                                               draft_row=row, dev_status=st, top_k=50, top_p=0.9,
+                                               workspace=ws)
         else:
             fn = lambda: E.eagle_softmax_stats(target, 1.0, dev_status=st)  # noqa: E731
     elif name == "compact":

@@ -112,6 +112,10 @@ def eagle_tree_attn(q, k_cache, v_cache, kv_len, parent, scale=None, out=None, w
     return out
 
 
+def verify_filter_workspace_size(B, n, R) -> int:
+    return int(lib().eagle_verify_filter_workspace_size(B, n, R))
+
+
 def eagle_d2t_inverse(d2t, V, t2d=None, dev_status=None, stream=None):
     """t2d int32 [V]: the draft id of each target id (d + d2t[d] -> d), -1 where none."""
     _dev(d2t, "d2t", torch.int32)

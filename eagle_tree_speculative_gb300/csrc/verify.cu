@@ -855,9 +855,13 @@ constexpr int kFiltThreads = 256;
 constexpr int kFiltBins = 2048;
 constexpr int kFiltMaxV = 1 << 22;              // the index select uses two 11-bit digits
 
+constexpr int kCand = 2048;                    // largest bin the sorted path takes
+
 struct FiltSmem {
     unsigned int cnt[kFiltBins];
     unsigned long long mass[kFiltBins];
+    unsigned long long sk[kCand];              // a bin's elements: (key << 32) | ~index, sorted
+    int ncand;
     unsigned int wcnt[kFiltThreads / 32];
     unsigned long long wmass[kFiltThreads / 32];
     float redf[kFiltThreads / 32];
@@ -870,6 +874,61 @@ struct FiltSmem {
 
 __device__ __forceinline__ unsigned long long fixed_mass(float l, float lmax, float c) {
     return __float2ull_rz(exp2f((l - lmax) * c) * 0x1p40f);     // exact: <= 2^40, 24-bit mantissa
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Distance bin of a logit: (max - l) c in 1/64 of a log2 unit, the far tail (mass below
+// 2^-31.98 of the maximum's) in the last bin.  Monotone: a larger logit never has a
+// larger bin, and equal logits share one.
+__device__ __forceinline__ int dist_bin(float l, float lmax, float c) {
+    const float d = (lmax - l) * c;
+    return d < (float)(kFiltBins - 1) / 64.f ? (int)(d * 64.f) : kFiltBins - 1;
+}
+
+// Gather the elements of distance bin b (at most kCand of them) and sort them by (key
+// desc, index asc) into sm.sk[0 .. ncand).
+__device__ void gather_sort(FiltSmem& sm, const float* x, int V, int b, float lmax, float c) {
+    const int tid = threadIdx.x;
+    if (tid == 0) sm.ncand = 0;
+    __syncthreads();
+    for (int t = tid; t < V; t += kFiltThreads) {
+        const float l = x[t];
+        if (dist_bin(l, lmax, c) == b) {
+            const int pos = atomicAdd(&sm.ncand, 1);
+            if (pos < kCand)
+                sm.sk[pos] = ((unsigned long long)order_key(l) << 32) | (unsigned long long)(~(uint32_t)t);
+        }
+    }
+    __syncthreads();
+    const int n = min(sm.ncand, kCand);
+    int n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (int j = n + tid; j < n2; j += kFiltThreads) sm.sk[j] = 0ull;     // sorts last
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < n2; i += kFiltThreads) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long a = sm.sk[i], bb = sm.sk[j];
+                    if (desc ? (a < bb) : (a > bb)) { sm.sk[i] = bb; sm.sk[j] = a; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Add one element (count 1, mass m) to bin `bin` of the block histogram; bin < 0 adds
+// nothing, and a zero mass skips the 64-bit atomic.
+__device__ __forceinline__ void hist_add(FiltSmem& sm, int bin, unsigned long long m) {
+    if (bin < 0) return;
+    atomicAdd(&sm.cnt[bin], 1u);
+    if (m) atomicAdd(&sm.mass[bin], m);
 }
 
 __device__ __forceinline__ bool elig(uint32_t k, int t, uint32_t k0, int i0) {
@@ -944,13 +1003,13 @@ __device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, flo
         const int nb = pass == 2 ? 1024 : 2048;
         for (int i = tid; i < nb; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
         __syncthreads();
-        for (int t = tid; t < V; t += kFiltThreads) {
-            const float l = x[t];
+        for (int base = 0; base < V; base += kFiltThreads) {          // warp-uniform trips
+            const int t = base + tid;
+            const float l = t < V ? x[t] : -INFINITY;
             const uint32_t k = order_key(l);
-            if ((k & pmask) != prefix || !elig(k, t, k0, i0)) continue;
-            const int bin = (int)((k >> shift) & (uint32_t)(nb - 1));
-            atomicAdd(&sm.cnt[bin], 1u);
-            atomicAdd(&sm.mass[bin], fixed_mass(l, lmax, c));
+            const bool in = t < V && (k & pmask) == prefix && elig(k, t, k0, i0);
+            hist_add(sm, in ? (int)((k >> shift) & (uint32_t)(nb - 1)) : -1,
+                     in ? fixed_mass(l, lmax, c) : 0ull);
         }
         __syncthreads();
         scan_bins<MASS, true>(sm, nb, remaining);
@@ -984,11 +1043,14 @@ __device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, flo
             const int shift = pass == 0 ? 11 : 0;
             for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
             __syncthreads();
-            for (int t = tid; t < V; t += kFiltThreads) {
-                if (((uint32_t)t & imask) != iprefix) continue;
-                const uint32_t k = order_key(x[t]);
-                if (k != prefix || !elig(k, t, k0, i0)) continue;
-                atomicAdd(&sm.cnt[((uint32_t)t >> shift) & (kFiltBins - 1)], 1u);
+            for (int base = 0; base < V; base += kFiltThreads) {      // warp-uniform trips
+                const int t = base + tid;
+                bool in = t < V && ((uint32_t)t & imask) == iprefix;
+                if (in) {
+                    const uint32_t k = order_key(x[t]);
+                    in = k == prefix && elig(k, t, k0, i0);
+                }
+                hist_add(sm, in ? (int)(((uint32_t)t >> shift) & (kFiltBins - 1)) : -1, 0ull);
             }
             __syncthreads();
             scan_bins<false, false>(sm, kFiltBins, rem);
@@ -1004,11 +1066,26 @@ __device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, flo
 
 __global__ void __launch_bounds__(kFiltThreads)
 row_filter_kernel(const float* __restrict__ target, int nq, const float* __restrict__ draft, int V,
-                  float c, int top_k, float top_p, FilterParam* fq, FilterParam* fp) {
+                  float c, int top_k, float top_p, FilterParam* fq, FilterParam* fp,
+                  const int32_t* __restrict__ parent, const int32_t* __restrict__ draft_row, int n,
+                  int R) {
     __shared__ FiltSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t r = blockIdx.x;
     const bool isq = r < nq;
+    if (!isq) {
+        // a draft row is read only as the distribution after a node with children
+        const int b = (int)((r - nq) / R), row = (int)((r - nq) % R);
+        if (tid == 0) sm.imax = 0;
+        __syncthreads();
+        if (tid < n && tid > 0) {
+            const int p = parent[(int64_t)b * n + tid];
+            if (p >= 0 && p < n && (draft_row ? draft_row[(int64_t)b * n + p] : p) == row) sm.imax = 1;
+        }
+        __syncthreads();
+        if (!sm.imax) return;          // never read by the walk: left unwritten
+        __syncthreads();
+    }
     const float* x = isq ? target + r * (int64_t)V : draft + (r - nq) * (int64_t)V;
     FilterParam* out = isq ? fq + r : fp + (r - nq);
     float mx = -INFINITY;
@@ -1033,31 +1110,97 @@ row_filter_kernel(const float* __restrict__ target, int nq, const float* __restr
     }
     uint32_t key = 0u;                 // keep everything
     int idx = 0x7fffffff;
-    unsigned long long total = 0ull;
-    bool have_total = false;
-    if (top_k > 0 && top_k < V) {
-        const Cut k = block_select<false>(sm, x, V, lmax, c, (unsigned long long)top_k, 0u, 0x7fffffff);
-        key = k.key;
-        idx = k.idx;
-        total = k.mass_upto;
-        have_total = true;
-    }
-    if (top_p > 0.f && top_p < 1.f) {
-        if (!have_total) {
-            unsigned long long m = 0ull;
-            for (int t = tid; t < V; t += kFiltThreads) m += fixed_mass(x[t], lmax, c);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
-            if (lane == 0) sm.wmass[warp] = m;
-            __syncthreads();
-            for (int w = 0; w < kFiltThreads / 32; ++w) total += sm.wmass[w];
-            __syncthreads();
+    const bool do_k = top_k > 0 && top_k < V;
+    const bool do_p = top_p > 0.f && top_p < 1.f;
+    auto fm = [&](unsigned long long e) { return fixed_mass(key_float((uint32_t)(e >> 32)), lmax, c); };
+    if (do_k || do_p) {
+        // Fast path: a histogram over distance bins (fine where the probability mass is),
+        // then an exact sort of the one bin the cut falls in.  The radix select takes over
+        // when that bin is the far tail or holds more than kCand elements.
+        for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+        __syncthreads();
+        for (int base = 0; base < V; base += kFiltThreads) {          // warp-uniform trips
+            const int t = base + tid;
+            const bool in = t < V;
+            const float l = in ? x[t] : -INFINITY;
+            hist_add(sm, in ? dist_bin(l, lmax, c) : -1, in && do_p ? fixed_mass(l, lmax, c) : 0ull);
         }
-        unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
-        tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
-        const Cut p = block_select<true>(sm, x, V, lmax, c, tgt, key, idx);
-        idx = p.key == key ? min(p.idx, idx) : p.idx;
-        key = p.key;
+        __syncthreads();
+        bool hist = true;                 // the histogram is still intact
+        int bk = -1, nk = 0;              // top-k cut: its bin, and how many of its sorted elements stay
+        unsigned long long mk = 0ull;     // mass of the bins before bk
+        unsigned long long total = 0ull;  // mass of what top-k keeps
+        if (do_k) {
+            scan_bins<false, false>(sm, kFiltBins, (unsigned long long)top_k);
+            const int bin = sm.found_bin;
+            const unsigned int cb = sm.found_cnt;
+            mk = sm.found_mass;
+            if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
+                gather_sort(sm, x, V, bin, lmax, c);
+                nk = top_k - (int)cb;
+                const unsigned long long e = sm.sk[nk - 1];
+                key = (uint32_t)(e >> 32);
+                idx = (int)(~(uint32_t)e);
+                total = mk;
+                for (int j = 0; j < nk; ++j) total += fm(sm.sk[j]);
+                bk = bin;
+            } else {
+                const Cut k = block_select<false>(sm, x, V, lmax, c, (unsigned long long)top_k, 0u,
+                                                  0x7fffffff);
+                key = k.key;
+                idx = k.idx;
+                total = k.mass_upto;
+                hist = false;
+            }
+        }
+        if (do_p) {
+            if (!do_k)
+                for (int i = 0; i < kFiltBins; ++i) total += sm.mass[i];
+            unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
+            tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
+            bool done = false;
+            if (hist && bk >= 0 && tgt > mk) {
+                // the cut lies among the elements of bk that top-k keeps (already sorted)
+                unsigned long long acc = mk;
+                int j = 0;
+                for (; j < nk - 1; ++j) {
+                    acc += fm(sm.sk[j]);
+                    if (acc >= tgt) break;
+                }
+                key = (uint32_t)(sm.sk[j] >> 32);
+                idx = (int)(~(uint32_t)sm.sk[j]);
+                done = true;
+            } else if (hist) {
+                if (bk >= 0) {            // only the bins before top-k's cut bin remain eligible
+                    __syncthreads();
+                    for (int i = bk + tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+                    __syncthreads();
+                }
+                scan_bins<true, false>(sm, kFiltBins, tgt);
+                const int bin = sm.found_bin;
+                const unsigned long long mb = sm.found_mass;
+                if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
+                    gather_sort(sm, x, V, bin, lmax, c);
+                    const int n = min(sm.ncand, kCand);
+                    unsigned long long acc = mb;
+                    int j = 0;
+                    for (; j < n - 1; ++j) {
+                        acc += fm(sm.sk[j]);
+                        if (acc >= tgt) break;
+                    }
+                    key = (uint32_t)(sm.sk[j] >> 32);
+                    idx = (int)(~(uint32_t)sm.sk[j]);
+                    done = true;
+                }
+            }
+            if (!done) {
+                __syncthreads();
+                const Cut pc = block_select<true>(sm, x, V, lmax, c, tgt, key, idx);
+                idx = pc.key == key ? min(pc.idx, idx) : pc.idx;
+                key = pc.key;
+            }
+        }
+        __syncthreads();
     }
     // S over the kept set; per-thread sums combined in a fixed order
     float s = 0.f;
@@ -1147,7 +1290,7 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
         FilterParam* fq = static_cast<FilterParam*>(workspace);
         FilterParam* fp = fq + (size_t)B * n;
         row_filter_kernel<<<(unsigned)(B * (n + R)), kFiltThreads, 0, s>>>(
-            target_logits, B * n, draft_logits, V, c, top_k, top_p, fq, fp);
+            target_logits, B * n, draft_logits, V, c, top_k, top_p, fq, fp, parent, draft_row, n, R);
         EAGLE_CHECK_LAUNCH();
         a.fq = fq;
         a.fp = fp;

@@ -298,11 +298,15 @@ def test_target_logits_in_pinned_host_memory_give_the_same_walk():
 # ---------------------------------------------------------------- top-k / top-p filtering
 @pytest.mark.parametrize("V,top_k,top_p,quant", [(32000, 50, 0.0, 0.0), (32000, 0, 0.9, 0.0),
                                                  (32000, 20, 0.8, 0.0), (1003, 7, 0.0, 0.5),
-                                                 (1003, 0, 0.7, 0.5), (1003, 30, 0.95, 0.25)])
+                                                 (1003, 0, 0.7, 0.5), (1003, 30, 0.95, 0.25),
+                                                 (32000, 100, 0.0, 2.0), (32000, 0, 0.9, 2.0),
+                                                 (32000, 3000, 0.99, 0.0)])
 def test_filtered_trees_match_oracle(V, top_k, top_p, quant):
     """Top-k / top-p filtered walk on 48-node depth-6 trees, B = 8, against
     oracle.verify_accept_filtered.  quant > 0 rounds every logit to a multiple of quant,
-    so cuts fall inside runs of equal logits (the lower token is kept first).  The
+    so cuts fall inside runs of equal logits (the lower token is kept first); at quant 2
+    the runs hold thousands of tokens, more than the sorted path takes, so the radix
+    select decides.  The
     visited rows' filtered sums (row_stats) are checked to 1e-5."""
     E = _gpu()
     cfg = W.CONFIGS["sweep_70b"]

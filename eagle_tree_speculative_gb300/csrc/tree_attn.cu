@@ -358,15 +358,17 @@ PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
     return fn;
 }
 
-// K or V cache viewed as a 2-D [B * Hkv * Lmax, 128] bf16 matrix; 64 x 64 boxes.
-bool kv_map(CUtensorMap* map, const void* base, int64_t rows) {
+// K or V cache viewed as a 3-D tensor: head_dim (128, innermost), Lmax rows of one
+// (sequence, kv head), then B * Hkv of those; 64 x TBN x 1 boxes.  Rows outside 0 .. Lmax - 1
+// of a (sequence, head) read as zeros, never as the neighbouring head's rows.
+bool kv_map(CUtensorMap* map, const void* base, int Lmax, int64_t heads) {
     auto fn = attn_encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)attn_tc::TBN};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Lmax, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Lmax * kHeadDim * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)attn_tc::TBN, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -439,9 +441,9 @@ extern "C" eagle_status eagle_tree_attn(const void* q, const void* k_cache, cons
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!v1) {
         CUtensorMap mk, mv;
-        const int64_t kv_rows = (int64_t)B * Hkv * Lmax;
-        if (kv_rows > 0x7fffffffLL) return EAGLE_ERR_SHAPE;
-        if (!kv_map(&mk, k_cache, kv_rows) || !kv_map(&mv, v_cache, kv_rows)) return EAGLE_ERR_CUDA;
+        const int64_t heads = (int64_t)B * Hkv;
+        if (heads > 0x7fffffffLL) return EAGLE_ERR_SHAPE;
+        if (!kv_map(&mk, k_cache, Lmax, heads) || !kv_map(&mv, v_cache, Lmax, heads)) return EAGLE_ERR_CUDA;
         attn_tc::Args t;
         t.q = a.q; t.out = a.out; t.ws_o = a.ws_o; t.ws_ml = a.ws_ml; t.kv_len = kv_len;
         t.parent = parent; t.B = B; t.n = n; t.Hq = Hq; t.Hkv = Hkv; t.G = G; t.Lmax = Lmax;

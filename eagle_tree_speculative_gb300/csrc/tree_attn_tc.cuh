@@ -191,7 +191,13 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int kb = err ? 0 : min(L, split * chunk);
     const int ke = err ? 0 : ((split == a.splits - 1) ? L + n : min(L, kb + chunk));
     const int T = err ? 0 : (ke - kb + TBN - 1) / TBN;
-    const int kvrow0 = (b * a.Hkv + kvh) * a.Lmax;
+    const int kvz = b * a.Hkv + kvh;                               // (sequence, kv head) slab
+    // A partial last tile is loaded ending at the last key (keys ke - TBN .. ke - 1), so it
+    // reads no cache row past the keys: rows nobody wrote may hold NaN, and P = 0 does not
+    // cancel NaN in the PV product.  Its keys below last_fresh are masked in the softmax:
+    // they belong to the tile before, or lie before row 0 and arrive from TMA as zeros.
+    const int last_fresh = T > 0 ? kb + (T - 1) * TBN : 0;         // first key the last tile adds
+    const int last0 = (T > 0 && ke - last_fresh < TBN) ? ke - TBN : last_fresh;
 
     // ---- Q -> TMEM (softmax warps, one lane = one row), while K/V already stream ----
     if (warp >= 4) {
@@ -227,19 +233,19 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 // L2 prefetch kPrefetch tiles beyond the ring, paced with the loads
                 if (t == 0) {
                     for (int jp = NS; jp < min(T, NS + kPrefetch); ++jp) {
-                        tma_prefetch_2d(map, 0, kvrow0 + kb + jp * TBN);
-                        tma_prefetch_2d(map, 64, kvrow0 + kb + jp * TBN);
+                        tma_prefetch_3d(map, 0, kb + jp * TBN, kvz);
+                        tma_prefetch_3d(map, 64, kb + jp * TBN, kvz);
                     }
                 } else if (t + NS + kPrefetch - 1 < T) {
-                    const int yp = kvrow0 + kb + (t + NS + kPrefetch - 1) * TBN;
-                    tma_prefetch_2d(map, 0, yp);
-                    tma_prefetch_2d(map, 64, yp);
+                    const int yp = kb + (t + NS + kPrefetch - 1) * TBN;
+                    tma_prefetch_3d(map, 0, yp, kvz);
+                    tma_prefetch_3d(map, 64, yp, kvz);
                 }
                 const uint32_t fb = s32(&full[st]);
                 mbar_expect_tx(fb, K_BYTES);
-                const int y = kvrow0 + kb + t * TBN;
-                tma_load_2d(s32(ring + st * K_BYTES), map, fb, 0, y);
-                tma_load_2d(s32(ring + st * K_BYTES + KV_BOX_BYTES), map, fb, 64, y);
+                const int y = t == T - 1 ? last0 : kb + t * TBN;
+                tma_load_3d(s32(ring + st * K_BYTES), map, fb, 0, y, kvz);
+                tma_load_3d(s32(ring + st * K_BYTES + KV_BOX_BYTES), map, fb, 64, y, kvz);
             }
         }
     } else if (warp == 1) {
@@ -352,8 +358,8 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     x[96 + c] = __uint_as_float(u3[c]);
                 }
             }
-            const int key0 = kb + j * TBN;
-            if (key0 + TBN > L || key0 + TBN > ke || !valid) {
+            const int key0 = j == T - 1 ? last0 : kb + j * TBN;
+            if (key0 + TBN > L || key0 + TBN > ke || !valid || key0 < last_fresh && j == T - 1) {
                 // visibility of the tile's keys as a 128-bit map: committed keys below L,
                 // tree key L + t visible iff bit t of the ancestor mask, nothing from ke on
                 uint64_t vis[2];
@@ -366,7 +372,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const int sh = L - k0;                     // tree key t sits at bit t + sh
                     const uint64_t tree = (sh >= 64 || sh <= -64) ? 0ull
                                           : (sh >= 0 ? anc << sh : anc >> (-sh));
-                    vis[w] = valid ? ((committed | tree) & upto) : 0ull;
+                    const int seen = last_fresh - k0;                 // keys below were counted
+                    const uint64_t fresh = (j < T - 1 || seen <= 0) ? ~0ull
+                                           : (seen >= 64 ? 0ull : ~((1ull << seen) - 1ull));
+                    vis[w] = valid ? ((committed | tree) & upto & fresh) : 0ull;
                 }
 #pragma unroll
                 for (int c = 0; c < TBN; ++c)

@@ -92,3 +92,30 @@ def test_capacity_and_tree_errors_set_status_and_zero_output():
     got, st = _run(q, k, v, kv_len, parent, 0.1)
     assert st & E.EAGLE_DEV_CAPACITY and st & E.EAGLE_DEV_BAD_TREE   # 10 + 4 > 13 in seq 0
     assert np.all(got == 0)
+
+
+@pytest.mark.parametrize("Hq,Hkv,n,L,Lmax", [(32, 8, 60, [200, 77, 333], 512),
+                                             (8, 8, 13, [200, 77, 333], 512),
+                                             (32, 8, 30, [1000], 2048)])
+def test_unwritten_cache_rows_past_the_tree_do_not_leak(Hq, Hkv, n, L, Lmax):
+    """Cache rows at and beyond L + n are not part of the attention; a cache that was
+    never written there may hold anything.  Those rows are set to NaN and +inf here (K
+    and V); the output must still match the oracle, which never reads them.  The last
+    key tile is partial in every case; 77 + 13 keys fit in less than one tile; one
+    sequence at 2048 rows splits its keys across CTAs."""
+    B, d = len(L), 128
+    q, k, v, kv_len = W.attn_inputs(B, n, Hq, Hkv, d, L, Lmax, seed=21)
+    k, v = k.clone(), v.clone()
+    for b in range(B):
+        k[b, :, L[b] + n:] = float("nan")
+        v[b, :, L[b] + n:] = float("nan")
+        v[b, :, L[b] + n + 1::3] = float("inf")
+    parent = np.stack([W.random_tree(n, 6, 21, b) for b in range(B)])
+    scale = d ** -0.5
+    got, st = _run(q, k, v, kv_len, parent, scale)
+    assert st == 0
+    assert np.isfinite(got).all()
+    for b in range(B):
+        ref = oracle.tree_attn(q[b:b + 1], k[b:b + 1], v[b:b + 1], kv_len[b:b + 1],
+                               parent[b:b + 1], scale)
+        assert attn_row_rel_err(got[b:b + 1], ref).max() <= TOL

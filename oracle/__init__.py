@@ -11,7 +11,8 @@ Pages cited (by title and section):
            "KV cache 回滚", "动手构建" steps 1-6, "练习".
   [Guide]  "EAGLE-1/2/3 拆解" (txtmix.com) -- "无损性的来源与它的证明位置",
            "EAGLE-2：草稿树的 Expansion 与 Reranking", "一次 eagenerate 调用的完整流转".
-  [TTT]    "EAGLE-3 完全拆解：Training-Time Test" -- "EAGLE-3 和 EAGLE-2 动态树如何拼在一起".
+  [TTT]    "EAGLE-3 完全拆解：Training-Time Test" -- "EAGLE-3 和 EAGLE-2 动态树如何拼在一起",
+           "训练时的 attention mask 为什么要特殊处理".
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 something other than itself (published Philox known-answer vectors, the
@@ -61,6 +62,8 @@ def lib():
         L.orc_sample_rows.argtypes = [_P, _I, _I, _I, _D, _U64, _P]
         L.orc_tree_attn.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _D, _P]
         L.orc_tree_attn.restype = _I
+        L.orc_ttt_attn.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _D, _P]
+        L.orc_ttt_attn.restype = _I
         L.orc_kv_compact.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I]
         L.orc_kv_compact.restype = _I
         L.orc_lmhead_rows.argtypes = [_P, _P, _I, _I, _I, _P, _I, _P]
@@ -260,6 +263,22 @@ def tree_attn(q, k, v, kv_len, parent, scale: float):
                              Lmax, float(scale), _ptr(out))
     if st != ORC_OK:
         raise ValueError(f"tree_attn: invalid input (status {st})")
+    return out
+
+
+def ttt_attn(q, k, v, r: int, scale: float):
+    """Training-time-test attention of the queries of round r in double (see oracle.c,
+    orc_ttt_attn).  q [B,S,Hq,d], k/v [B,Hkv,R1,S,d] (bf16; round 0 = original tokens)."""
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    B, S, Hq, d = qb.shape
+    Hkv, R1 = kb.shape[1], kb.shape[2]
+    if kb.shape != (B, Hkv, R1, S, d) or vb.shape != kb.shape:
+        raise ValueError("ttt_attn: k / v must be [B, Hkv, R1, S, d]")
+    out = np.zeros((B, S, Hq, d))
+    st = lib().orc_ttt_attn(_ptr(qb), _ptr(kb), _ptr(vb), B, S, Hq, Hkv, d, R1, int(r),
+                            float(scale), _ptr(out))
+    if st != ORC_OK:
+        raise ValueError(f"ttt_attn: invalid input (status {st})")
     return out
 
 

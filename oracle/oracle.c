@@ -476,6 +476,65 @@ int orc_tree_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 }
 
 /* ------------------------------------------------------------------------
+ * Training-time-test attention (TTT page, section
+ * "训练时的 attention mask 为什么要特殊处理").  Round 0 runs on the original tokens with the ordinary causal mask.
+ * Round r >= 1 feeds back, at every position i, the token the previous round
+ * predicted there; a simulated token may see only its own ancestors: the
+ * original tokens up to its position (0..i) and the tokens of rounds 1..r at
+ * the same position (its own chain, itself included), never another
+ * position's simulated tokens.  For the queries of round r, query head h,
+ * kv head h / (Hq / Hkv): plain softmax(scale * q.k) . v over that key list,
+ * all in double.
+ *   q bf16 [B, S, Hq, d] (the queries of round r);
+ *   k, v bf16 [B, Hkv, R1, S, d] (round 0 = original tokens, rounds 1..R1-1);
+ *   out f64 [B, S, Hq, d]
+ * ---------------------------------------------------------------------- */
+int orc_ttt_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int S, int Hq,
+                 int Hkv, int d, int R1, int r, double scale, double* out)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || r < 0 || r >= R1) return ORC_BAD_TREE;
+    const int G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hq; ++h) {
+            const int kvh = h / G;
+            const int64_t slab = ((int64_t)b * Hkv + kvh) * R1 * S;   /* row (round, pos) */
+            double* s = (double*)malloc(sizeof(double) * (S + R1));
+            int64_t* key = (int64_t*)malloc(sizeof(int64_t) * (S + R1));
+            double* qd = (double*)malloc(sizeof(double) * d);
+            for (int i = 0; i < S; ++i) {
+                const uint16_t* Q = q + (((int64_t)b * S + i) * Hq + h) * d;
+                for (int e = 0; e < d; ++e) qd[e] = bf16_to_double(Q[e]);
+                int nk = 0;
+                for (int j = 0; j <= i; ++j) key[nk++] = slab + j;                     /* round 0 */
+                for (int rr = 1; rr <= r; ++rr) key[nk++] = slab + (int64_t)rr * S + i;  /* chain */
+                double mx = -INFINITY;
+                for (int t = 0; t < nk; ++t) {
+                    const uint16_t* Kr = k + key[t] * d;
+                    double acc = 0.0;
+                    for (int e = 0; e < d; ++e) acc += qd[e] * bf16_to_double(Kr[e]);
+                    s[t] = acc * scale;
+                    if (s[t] > mx) mx = s[t];
+                }
+                double den = 0.0;
+                for (int t = 0; t < nk; ++t) { s[t] = exp(s[t] - mx); den += s[t]; }
+                double* O = out + (((int64_t)b * S + i) * Hq + h) * d;
+                for (int e = 0; e < d; ++e) O[e] = 0.0;
+                for (int t = 0; t < nk; ++t) {
+                    const uint16_t* Vr = v + key[t] * d;
+                    double w = s[t] / den;
+                    for (int e = 0; e < d; ++e) O[e] += w * bf16_to_double(Vr[e]);
+                }
+            }
+            free(s);
+            free(key);
+            free(qd);
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
  * KV compaction and logical-length update (Lesson "KV cache 回滚" and
  * "第 4 步": keep one physical cache plus a logical length).  The tree's
  * K/V rows sit at L_b + j.  After acceptance the rows of the accepted path

@@ -35,6 +35,7 @@ TAG_TREE = 11
 TAG_CACHE = 12
 TAG_CHAIN = 13
 TAG_D2T = 14          # which target ids a draft vocabulary holds
+TAG_TTT_Q, TAG_TTT_K, TAG_TTT_V = 15, 16, 17   # training-time-test attention
 
 
 @dataclass(frozen=True)
@@ -205,6 +206,16 @@ def attn_inputs(B: int, n: int, Hq: int, Hkv: int, d: int, kv_len, Lmax: int, se
     k = to_bf16(per_seq_normal(B, (Hkv, Lmax, d), 1.0, seed, TAG_K))
     v = to_bf16(per_seq_normal(B, (Hkv, Lmax, d), 1.0, seed, TAG_V))
     return q, k, v, kv_len
+
+
+def ttt_inputs(B: int, S: int, Hq: int, Hkv: int, d: int, R1: int, seed: int):
+    """Training-time-test attention inputs: q [B,S,Hq,d] (the queries of one round) and
+    k / v [B,Hkv,R1,S,d] (round 0 = the original tokens, then the simulated rounds), bf16
+    ~N(0,1)."""
+    q = to_bf16(per_seq_normal(B, (S, Hq, d), 1.0, seed, TAG_TTT_Q))
+    k = to_bf16(per_seq_normal(B, (Hkv, R1, S, d), 1.0, seed, TAG_TTT_K))
+    v = to_bf16(per_seq_normal(B, (Hkv, R1, S, d), 1.0, seed, TAG_TTT_V))
+    return q, k, v
 
 
 def kv_cache(n_layers: int, B: int, Hkv: int, Lmax: int, d: int, seed: int):

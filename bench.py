@@ -310,6 +310,7 @@ def run_ours(args, rank, world, dist):
 
     # -------- per-call breakdown (separate short timing) --------
     br = breakdown(st, torch)
+    ttt = ttt_attn_figures(torch, dev, peaks)
 
     # -------- end to end through the public API with host buffers --------
     e2e = run_e2e(st, torch, max(5, min(args.steps, 20)), graph)
@@ -357,6 +358,7 @@ def run_ours(args, rank, world, dist):
                      "gemm_flops_per_step_all_levels": gemm_flops / eager_steps,
                      "timed": f"{eager_steps} eager steps, events around each launch"},
         "breakdown_ms": br,
+        "ttt_attn": ttt,
         "e2e": e2e,
         "e2e_target_in_place": e2e_in_place,
         "gpu_launches": st.launches_per_step() * args.steps,
@@ -366,6 +368,51 @@ def run_ours(args, rank, world, dist):
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     return out
+
+
+TTT_SHAPE = dict(B=8, S=2048, Hq=32, Hkv=8, R1=8, r=7)
+
+
+def ttt_inputs(torch, dev, B, S, Hq, Hkv, R1, g):
+    d = 128
+    q = torch.empty(B, S, Hq, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    k = torch.empty(B, Hkv, R1, S, d, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+    v = torch.empty_like(k).normal_(generator=g)
+    return q, k, v
+
+
+def ttt_attn_figures(torch, dev, peaks, reps=20):
+    """Training-time-test attention of one layer, timed alone: Llama-3-8B heads (32 q /
+    8 kv), 8 sequences of 2048 positions, the queries of round 7 of 8 and of round 0.
+    FLOPs count the visible keys only (causal part + r diagonal keys per row)."""
+    import eagle_tree_speculative_gb300 as E
+    c = TTT_SHAPE
+    B, S, Hq, Hkv, R1, d = c["B"], c["S"], c["Hq"], c["Hkv"], c["R1"], 128
+    g = torch.Generator(device=dev).manual_seed(SEED + 23)
+    q, k, v = ttt_inputs(torch, dev, B, S, Hq, Hkv, R1, g)
+    out = torch.empty_like(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {"shape": "B=8, S=2048, 32 q / 8 kv heads, d=128, 8 rounds stored",
+           "l2": "inputs larger than L2 (q 134 MB, K and V 268 MB each)"}
+    peak = peaks["bf16_tflops"]
+    for r in (c["r"], 0):
+        fn = lambda: E.eagle_ttt_attn(q, k, v, r, out=out, dev_status=st)  # noqa: E731
+        for _ in range(3):
+            fn()
+        ms = time_region(lambda i: fn(), reps, torch) / reps
+        flops = 4.0 * d * Hq * B * S * (S + 1) / 2 + 4.0 * d * Hq * B * S * r
+        hbm = 2 * (2 * B * S * Hq * d) + 2 * (2 * B * Hkv * (1 + r) * S * d)
+        tf = flops / (ms * 1e-3) / 1e12
+        res[f"round{r}"] = {"ms": round(ms, 4), "TFLOPs": round(tf, 1),
+                            "frac_of_bf16_peak": round(tf / peak, 4),
+                            "GBps_algorithmic": round(hbm / (ms * 1e-3) / 1e9, 1),
+                            "flops": flops, "hbm_bytes": hbm}
+    res["peak_source"] = f"{peaks['source']} bf16_tflops (burst: the kernel is timed alone)"
+    if int(st.item()) != 0:
+        raise RuntimeError(f"ttt attention device status {int(st.item())}")
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def breakdown(st, torch, reps=20):
@@ -631,7 +678,7 @@ def run_reference(args, rank, world):
 
 
 KERNEL_CASES = ("gemm", "topk", "fused", "attn", "verify", "verify_filtered", "compact",
-                "softmax")
+                "softmax", "ttt")
 
 
 def kernel_case(name, reps):
@@ -649,6 +696,7 @@ def kernel_case(name, reps):
       verify_filtered  the same with top-k 50 and top-p 0.9 (row filters, then the walk)
       compact  KV compaction, 32 layers, B=4 (8 kv heads, Lmax 4156)
       softmax  softmax statistics of [32, 60, 128256] target logits
+      ttt      training-time-test attention, B=8, S=2048, 32/8 heads, round 7 of 8
     """
     import torch
 
@@ -742,6 +790,11 @@ def kernel_case(name, reps):
         def fn():
             E.eagle_kv_compact(kc, vc, kv_len, path, acc, c.depth, dev_status=st)
             kv_len.copy_(kv_len0)
+    elif name == "ttt":
+        t = TTT_SHAPE
+        q, k, v = ttt_inputs(torch, dev, t["B"], t["S"], t["Hq"], t["Hkv"], t["R1"], g)
+        out = torch.empty_like(q)
+        fn = lambda: E.eagle_ttt_attn(q, k, v, t["r"], out=out, dev_status=st)  # noqa: E731
     else:
         raise ValueError(name)
     fn()                                   # warm-up (first-call set-up stays untimed)

@@ -112,6 +112,28 @@ def eagle_tree_attn(q, k_cache, v_cache, kv_len, parent, scale=None, out=None, w
     return out
 
 
+def eagle_ttt_attn(q, k, v, r, scale=None, out=None, dev_status=None, stream=None):
+    """Training-time-test attention of the queries of round r.  q [B,S,Hq,d] and
+    k / v [B,Hkv,R1,S,d] bf16 (round 0 = the original tokens); returns out [B,S,Hq,d]."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(k, "k", torch.bfloat16)
+    _dev(v, "v", torch.bfloat16)
+    B, S, Hq, d = q.shape
+    if k.dim() != 5 or tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != S \
+            or k.shape[4] != d:
+        raise ValueError("eagle_ttt_attn: k / v must be [B, Hkv, R1, S, d] matching q")
+    Hkv, R1 = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.bfloat16)
+    _check("eagle_ttt_attn", lib().eagle_ttt_attn(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, Hq, Hkv, d, R1, int(r), float(scale),
+        _ptr(_status(dev_status, q.device)), _stream(stream)))
+    return out
+
+
 def verify_filter_workspace_size(B, n, R) -> int:
     return int(lib().eagle_verify_filter_workspace_size(B, n, R))
 

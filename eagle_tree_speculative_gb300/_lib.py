@@ -21,6 +21,7 @@ _SZ = ctypes.c_size_t
 SIGNATURES = {
     "eagle_tree_attn_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "eagle_tree_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P]),
+    "eagle_ttt_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
     "eagle_verify_accept": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _U64, _P, _P, _P, _P,
                                  _P, _P]),
     "eagle_verify_filter_workspace_size": (_SZ, [_I, _I, _I]),

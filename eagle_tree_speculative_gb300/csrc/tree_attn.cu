@@ -343,26 +343,11 @@ int attn_splits(int B, int n, int Hq, int Hkv, int Lmax) {
     return splits < 1 ? 1 : splits;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // K or V cache viewed as a 3-D tensor: head_dim (128, innermost), Lmax rows of one
 // (sequence, kv head), then B * Hkv of those; 64 x TBN x 1 boxes.  Rows outside 0 .. Lmax - 1
 // of a (sequence, head) read as zeros, never as the neighbouring head's rows.
 bool kv_map(CUtensorMap* map, const void* base, int Lmax, int64_t heads) {
-    auto fn = attn_encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Lmax, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)Lmax * kHeadDim * 2};

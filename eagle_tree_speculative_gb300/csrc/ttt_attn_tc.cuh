@@ -1,0 +1,527 @@
+// Training-time-test attention on the 5th-generation tensor cores.
+//
+// Method (TTT page, section "训练时的 attention mask 为什么要特殊处理"): round 0 runs
+// on the original tokens with the causal mask; in round r >= 1 every position i
+// holds the token the previous round predicted there, and that token may see only
+// its ancestors: the original tokens 0..i and the round-1..r tokens at position i.
+// The original-token part is a dense causal attention; the part between simulated
+// rounds is one key per earlier round on the diagonal, which the page says to
+// compute as per-position dot products rather than as a mostly-masked matrix
+// product.  This kernel does exactly that split.
+//
+// One CTA owns 128 query rows (row = position * G + head-in-group, G = Hq / Hkv)
+// of one (sequence, kv head); its positions are imin .. imin + PB - 1 at most.
+//   - The causal part runs like the tree-attention kernel: 128-key K and V tiles of
+//     round 0 stream by TMA through two 3-stage rings; S = Q K^T and O += P V are
+//     tcgen05 MMAs with Q, S, P and O in TMEM; one thread per row runs the online
+//     softmax with the causal mask on the tiles that cross the diagonal.
+//   - Diagonal tiles follow the causal tiles through the same rings, so they load
+//     while the last causal tiles are computed.  The rows of rounds 1..r at the
+//     tile's positions are contiguous per round, so one 4-D TMA box (64 dims x PB
+//     positions x RB rounds) brings PB * RB <= 128 of them into a K stage, and the
+//     same box of V into the V stage.  After the last PV, each softmax thread takes
+//     O into registers and, per diagonal key of its position, the dot product with
+//     its query (read back from TMEM) on the CUDA cores, one more online-softmax
+//     step and the weighted value row; the four softmax warps then release the
+//     stage on `drel`.
+// The row tiles nearest the end of the sequence have the most keys, so the grid
+// runs them first.  Every wait is bounded.
+//
+// Barriers (each completes once per use; a waiter is never more than one
+// completion behind):
+//   k_full/v_full[s]     stage s landed (TMA): causal tiles -> MMA, diagonal tiles ->
+//                        softmax warps, which poll them only after the last PV, when
+//                        every earlier completion of the barrier has happened
+//   k_empty/v_empty[s]   causal tile in stage s consumed (MMA)  MMA -> producer
+//   drel[s]              diagonal tile in stage s consumed (4 softmax warps)
+//   q_full, s_full/p_full/pv_done[tile % 2]  as in the tree-attention kernel.
+#pragma once
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace eagle {
+namespace ttt_tc {
+
+constexpr int TBN = 128;                          // keys per causal tile
+constexpr int NSTAGES = 3;                        // K ring and V ring
+constexpr int kPrefetch = 3;
+constexpr int NSBUF = 2;
+constexpr int ROWS_PER_CTA = 128;
+constexpr int KV_BOX_BYTES = TBN * 64 * 2;        // 16 KB: 128 rows x 64 dims
+constexpr int K_BYTES = 2 * KV_BOX_BYTES;         // 32 KB per K or V stage
+constexpr int SMEM_BYTES = 2 * NSTAGES * K_BYTES + 2048;
+constexpr int kThreads = 256;                     // warps 0-3 roles, 4-7 softmax
+constexpr int kMaxRounds = 16;                    // rounds stored (original + simulated)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL0 = 0, O_COL0 = 256, Q_COL0 = 384;
+constexpr float kRescaleThreshold = 8.f;          // log2 units
+
+constexpr uint32_t kIdescQK = idesc_bf16(128, TBN, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, 0, 1);
+
+struct Args {
+    const uint16_t* q;        // [B, S, Hq, 128], the queries of round r
+    uint16_t* out;            // [B, S, Hq, 128]
+    int B, S, Hq, Hkv, G, R1, r;
+    int PB;                   // positions per diagonal box (>= positions of any row tile)
+    int RB;                   // rounds per diagonal box (PB * RB <= 128)
+    int ND;                   // diagonal tiles: ceil(r / RB)
+    float scale_log2;
+    int32_t* dev_status;
+};
+
+struct Bars {
+    uint64_t k_full[NSTAGES];
+    uint64_t k_empty[NSTAGES];
+    uint64_t v_full[NSTAGES];
+    uint64_t v_empty[NSTAGES];
+    uint64_t drel[NSTAGES];
+    uint64_t s_full[NSBUF];
+    uint64_t q_full;
+    uint64_t p_full[NSBUF];
+    uint64_t pv_done[NSBUF];
+    uint64_t drain;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+// 16 bytes (8 dims) of row `row` of a 64-dim half-box staged with the 128-byte
+// swizzle: chunk c of a 128-byte row sits at chunk c ^ (row % 8).
+__device__ __forceinline__ uint4 swz_chunk(const uint8_t* half_box, int row, int c) {
+    return *reinterpret_cast<const uint4*>(half_box + row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-D
+                   const __grid_constant__ CUtensorMap tmap_v,
+                   const __grid_constant__ CUtensorMap tmap_kd,   // all rounds, 4-D
+                   const __grid_constant__ CUtensorMap tmap_vd, Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* sK = smem;                                   // [NSTAGES][32 KB]
+    uint8_t* sV = sK + NSTAGES * K_BYTES;                 // [NSTAGES][32 KB]
+    Bars* bars = reinterpret_cast<Bars*>(sV + NSTAGES * K_BYTES);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kvz = blockIdx.x;                           // (sequence, kv head) slab
+    const int b = kvz / a.Hkv, kvh = kvz % a.Hkv;
+    const int rg = (int)gridDim.y - 1 - (int)blockIdx.y;  // row tiles with the most keys first
+    const int G = a.G, S = a.S, rows = S * G;
+    const int row0 = rg * ROWS_PER_CTA;
+    const int row_end = min(row0 + ROWS_PER_CTA, rows);
+    const int imin = row0 / G;                            // first position of the tile
+    const int ke = (row_end - 1) / G + 1;                 // round-0 keys 0 .. ke-1 reach the tile
+    const int T = (ke + TBN - 1) / TBN;                   // causal tiles
+    const int ND = a.ND;                                  // diagonal tiles, loaded last
+    const bool has_diag = ND > 0;
+
+    uint4 qrow[kHeadDim / 8];
+    if (warp >= 4) {
+        const int r = row0 + (warp & 3) * 32 + lane;
+#pragma unroll
+        for (int u = 0; u < kHeadDim / 8; ++u) qrow[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + (((int64_t)b * S + r / G) * a.Hq + kvh * G + r % G) * kHeadDim);
+#pragma unroll
+            for (int u = 0; u < kHeadDim / 8; ++u) qrow[u] = __ldg(src + u);
+        }
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGES; ++s) {
+            mbar_init(s32(&bars->k_full[s]), 1);
+            mbar_init(s32(&bars->k_empty[s]), 1);
+            mbar_init(s32(&bars->v_full[s]), 1);
+            mbar_init(s32(&bars->v_empty[s]), 1);
+            mbar_init(s32(&bars->drel[s]), 4);
+        }
+        for (int p = 0; p < NSBUF; ++p) {
+            mbar_init(s32(&bars->s_full[p]), 1);
+            mbar_init(s32(&bars->p_full[p]), 4);
+            mbar_init(s32(&bars->pv_done[p]), 1);
+        }
+        mbar_init(s32(&bars->drain), 1);
+        mbar_init(s32(&bars->q_full), 4);
+        bars->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        for (const CUtensorMap* m : {&tmap_k, &tmap_v, &tmap_kd, &tmap_vd})
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+    }
+    if (warp == 1) tmem_alloc(s32(&bars->tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+
+    // ---- Q -> TMEM (softmax warps, one lane = one row) ----
+    if (warp >= 4) {
+        const uint32_t qaddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + Q_COL0;
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint4 v = qrow[8 * h + u];
+                w[4 * u] = v.x; w[4 * u + 1] = v.y; w[4 * u + 2] = v.z; w[4 * u + 3] = v.w;
+            }
+            tmem_st32(qaddr + 32 * h, w);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s32(&bars->q_full));
+    }
+
+    if (warp == 0 || warp == 2) {
+        if (lane == 0) {
+            // ---------------- TMA producers: K (warp 0) and V (warp 2) ----------------
+            // Ring tiles 0 .. T-1 are the causal tiles, T .. T+ND-1 the diagonal boxes,
+            // which so stream in while the last causal tiles are computed.
+            const bool isK = warp == 0;
+            const CUtensorMap* map = isK ? &tmap_k : &tmap_v;
+            const CUtensorMap* dmap = isK ? &tmap_kd : &tmap_vd;
+            uint8_t* ring = isK ? sK : sV;
+            uint64_t* full = isK ? bars->k_full : bars->v_full;
+            uint64_t* empty = isK ? bars->k_empty : bars->v_empty;
+            // first diagonal ring tile of each stage
+            const int d0s[NSTAGES] = {T + (NSTAGES - T % NSTAGES) % NSTAGES,
+                                      T + (NSTAGES + 1 - T % NSTAGES) % NSTAGES,
+                                      T + (NSTAGES + 2 - T % NSTAGES) % NSTAGES};
+            for (int jp = NSTAGES; jp < min(T, NSTAGES + kPrefetch); ++jp) {
+                tma_prefetch_3d(map, 0, jp * TBN, kvz);
+                tma_prefetch_3d(map, 64, jp * TBN, kvz);
+            }
+            for (int t = 0; t < T + ND; ++t) {
+                const int st = t % NSTAGES;
+                if (t >= NSTAGES) {
+                    // wait until the stage's previous tile was consumed: a causal tile by
+                    // the MMA commit, a diagonal one by the softmax warps
+                    const int tp = t - NSTAGES;
+                    const bool okw =
+                        tp < T ? mbar_wait(s32(&empty[st]), (uint32_t)(tp / NSTAGES) & 1u, abort_flag)
+                               : mbar_wait(s32(&bars->drel[st]), (uint32_t)((tp - d0s[st]) / NSTAGES) & 1u,
+                                           abort_flag);
+                    if (!okw) break;
+                }
+                const uint32_t fb = s32(&full[st]);
+                uint8_t* dst = ring + st * K_BYTES;
+                if (t < T) {
+                    if (t >= 1 && t + NSTAGES + kPrefetch - 1 < T) {
+                        const int yp = (t + NSTAGES + kPrefetch - 1) * TBN;
+                        tma_prefetch_3d(map, 0, yp, kvz);
+                        tma_prefetch_3d(map, 64, yp, kvz);
+                    }
+                    mbar_expect_tx(fb, K_BYTES);
+                    tma_load_3d(s32(dst), map, fb, 0, t * TBN, kvz);
+                    tma_load_3d(s32(dst + KV_BOX_BYTES), map, fb, 64, t * TBN, kvz);
+                } else {
+                    mbar_expect_tx(fb, (uint32_t)(2 * 128 * a.PB * a.RB));
+                    const int u0 = 1 + (t - T) * a.RB;            // first round of the box
+                    tma_load_4d(s32(dst), dmap, fb, 0, imin, u0, kvz);
+                    tma_load_4d(s32(dst + KV_BOX_BYTES), dmap, fb, 64, imin, u0, kvz);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: causal tiles (ring tiles 0 .. T-1) ----------------
+            const uint64_t dK0 = sw128_desc(s32(sK));
+            const uint64_t dV0 = sw128_desc_mn(s32(sV), KV_BOX_BYTES, 1024);
+            const uint32_t ocol = tmem + O_COL0;
+            auto issue_qk = [&](int j) {     // S[j % 2] = Q K_j^T; frees K stage of tile j
+                const int st = j % NSTAGES;
+                const uint64_t dk = dK0 + (uint64_t)((st * K_BYTES) >> 4);
+                const uint32_t scol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
+#pragma unroll
+                for (int k = 0; k < kHeadDim / 16; ++k)
+                    umma_f16_ts(scol, tmem + Q_COL0 + k * 8,
+                                dk + (uint64_t)((((k >> 2) * KV_BOX_BYTES) + (k & 3) * 32) >> 4),
+                                kIdescQK, k > 0 ? 1u : 0u);
+                umma_commit(s32(&bars->s_full[j % NSBUF]));
+                umma_commit(s32(&bars->k_empty[st]));
+            };
+            auto issue_pv = [&](int j) {     // O += P[j % 2] V_j; frees V stage of tile j
+                const int st = j % NSTAGES;
+                const uint64_t dv = dV0 + (uint64_t)((st * K_BYTES) >> 4);
+                const uint32_t pcol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+                for (int k = 0; k < TBN / 16; ++k)
+                    umma_f16_ts(ocol, pcol + k * 8, dv + (uint64_t)((k * 16 * 128) >> 4), kIdescPV,
+                                k > 0 ? 1u : acc0);
+                umma_commit(s32(&bars->pv_done[j % NSBUF]));
+                umma_commit(s32(&bars->v_empty[st]));
+            };
+            auto kfull_ready = [&](int j) -> bool {
+                return mbar_try_wait(s32(&bars->k_full[j % NSTAGES]), ((uint32_t)j / NSTAGES) & 1u);
+            };
+            auto vfull_ready = [&](int j) -> bool {
+                return mbar_try_wait(s32(&bars->v_full[j % NSTAGES]), ((uint32_t)j / NSTAGES) & 1u);
+            };
+            bool ok = mbar_wait(s32(&bars->q_full), 0u, abort_flag);
+            tc_fence_after();
+            int js = 0, jp = 0;
+            long long t_last = clock64();
+            uint32_t idle = 0;
+            while (ok && jp < T) {
+                bool progressed = false;
+                // QK^T of tile js: its S buffer's previous P (tile js-2) consumed, K landed
+                if (js < T &&
+                    (js < NSBUF ||
+                     mbar_try_wait(s32(&bars->pv_done[js % NSBUF]), ((uint32_t)(js - NSBUF) / NSBUF) & 1u)) &&
+                    kfull_ready(js)) {
+                    tc_fence_after();
+                    issue_qk(js++);
+                    progressed = true;
+                }
+                if (jp < js &&
+                    mbar_try_wait(s32(&bars->p_full[jp % NSBUF]), ((uint32_t)jp / NSBUF) & 1u) &&
+                    vfull_ready(jp)) {
+                    tc_fence_after();
+                    issue_pv(jp++);
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = clock64();
+                } else if ((++idle & 63u) == 0u) {
+                    if (*abort_flag) ok = false;
+                    else if (clock64() - t_last > kTimeoutCycles) { *abort_flag = 1; ok = false; }
+                }
+            }
+            umma_commit(s32(&bars->drain));
+            mbar_wait(s32(&bars->drain), 0u, abort_flag, /*honour_abort=*/false);
+        }
+    } else if (warp >= 4) {
+        // ---------------- softmax: one thread per query row ----------------
+        const int q4 = warp & 3;                         // TMEM lane quadrant
+        const int r = row0 + q4 * 32 + lane;
+        const bool valid = r < rows;
+        const int i = valid ? r / G : imin;              // position
+        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        const uint32_t s_addr0 = tmem + lane_base + S_COL0;
+        const uint32_t o_addr = tmem + lane_base + O_COL0;
+        const uint32_t q_addr = tmem + lane_base + Q_COL0;
+        const float sc = a.scale_log2;
+        float mref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; ok && j < T; ++j) {
+            bool got = mbar_wait(s32(&bars->s_full[j % NSBUF]), ((uint32_t)j / NSBUF) & 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t s_addr = s_addr0 + (uint32_t)((j % NSBUF) * TBN);
+            float x[TBN];
+            {
+                uint32_t u0[32], u1[32], u2[32], u3[32];
+                tmem_ld32_nowait(s_addr, u0);
+                tmem_ld32_nowait(s_addr + 32, u1);
+                tmem_ld32_nowait(s_addr + 64, u2);
+                tmem_ld32_nowait(s_addr + 96, u3);
+                asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    x[c] = __uint_as_float(u0[c]);
+                    x[32 + c] = __uint_as_float(u1[c]);
+                    x[64 + c] = __uint_as_float(u2[c]);
+                    x[96 + c] = __uint_as_float(u3[c]);
+                }
+            }
+            const int key0 = j * TBN;
+            if (key0 + TBN - 1 > imin || !valid) {
+                // causal mask: key k visible iff k <= i (keys past the sequence arrive as
+                // zeros from TMA and are masked too)
+                uint64_t vis[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int ne = min(max(i + 1 - (key0 + 64 * w), 0), 64);
+                    vis[w] = valid ? (ne >= 64 ? ~0ull : ((1ull << ne) - 1ull)) : 0ull;
+                }
+#pragma unroll
+                for (int c = 0; c < TBN; ++c)
+                    if (!((vis[c >> 6] >> (c & 63)) & 1ull)) x[c] = -INFINITY;
+            }
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = x[e];
+#pragma unroll
+            for (int c = 8; c < TBN; c += 8)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], x[c + e]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            mx *= sc;
+            float alpha = 1.f;
+            if (mx > mref + kRescaleThreshold || (mref == -INFINITY && mx > -INFINITY)) {
+                alpha = mref == -INFINITY ? 0.f : exp2f(mref - mx);
+                mref = mx;
+                l *= alpha;
+            }
+            // O holds data to rescale once a PV ran: wait for the last one
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                got = mbar_wait(s32(&bars->pv_done[(j - 1) % NSBUF]), ((uint32_t)(j - 1) / NSBUF) & 1u,
+                                abort_flag);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < kHeadDim / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + cc * 32, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(o_addr + cc * 32, o);
+                }
+            }
+            const float base = mref == -INFINITY ? 0.f : mref;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(x[64 * h + 2 * e], sc, -base));
+                    const float p1 = ex2_approx(fmaf(x[64 * h + 2 * e + 1], sc, -base));
+                    ps[e & 3] += p0 + p1;
+                    pk[e] = pack2(p0, p1);
+                }
+                tmem_st32(s_addr + (uint32_t)(32 * h), pk);
+            }
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s32(&bars->p_full[j % NSBUF]));
+        }
+        bool got = ok && T > 0 ? mbar_wait(s32(&bars->pv_done[(T - 1) % NSBUF]),
+                                           ((uint32_t)(T - 1) / NSBUF) & 1u, abort_flag)
+                               : false;
+        got = __all_sync(0xffffffffu, got);
+        tc_fence_after();
+        const int h = kvh * G + (valid ? r % G : 0);
+        uint16_t* dst0 = a.out + (((int64_t)b * S + i) * a.Hq + h) * kHeadDim;
+        if (!has_diag) {
+            const float inv = (got && l > 0.f) ? 1.f / l : 0.f;
+            for (int cc = 0; cc < kHeadDim / 32; ++cc) {
+                uint32_t o[32];
+                if (got) tmem_ld32(o_addr + cc * 32, o);
+                else
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                if (!valid) continue;
+                uint16_t* dst = dst0 + cc * 32;
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    const uint4 w = make_uint4(
+                        pack2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                        pack2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                        pack2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                        pack2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                    *reinterpret_cast<uint4*>(dst + e) = w;
+                }
+            }
+        } else {
+            // ---- diagonal: rounds 1..r at this position, folded into O last ----
+            // O comes into registers; each diagonal key is one more online-softmax step.
+            float oacc[kHeadDim];
+#pragma unroll
+            for (int cc = 0; cc < kHeadDim / 32; ++cc) {
+                uint32_t o[32];
+                if (got) tmem_ld32(o_addr + cc * 32, o);
+                else
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) oacc[32 * cc + e] = __uint_as_float(o[e]);
+            }
+            const int pl = i - imin;                     // position within the boxes
+            // The last PV has completed, so every causal tile's K and V landed and each
+            // stage's next full-barrier completion is the diagonal tile's.
+            for (int t = 0; got && t < ND; ++t) {
+                const int ring_t = T + t;
+                const int st = ring_t % NSTAGES;
+                const uint32_t par = ((uint32_t)ring_t / NSTAGES) & 1u;
+                const bool okw = mbar_wait(s32(&bars->k_full[st]), par, abort_flag) &&
+                                 mbar_wait(s32(&bars->v_full[st]), par, abort_flag);
+                if (!__all_sync(0xffffffffu, okw)) { got = false; break; }
+                const uint8_t* kst = sK + st * K_BYTES;
+                const uint8_t* vst = sV + st * K_BYTES;
+                // rounds of this box in use; the same for every lane, because the loop
+                // holds warp-collective TMEM loads (rows past the tile compute on row
+                // pl = 0 and are never written out)
+                const int nr = min(a.RB, a.r - t * a.RB);
+                for (int ub = 0; ub < nr; ++ub) {
+                    const int row = ub * a.PB + pl;
+                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        // this row's query, dims 64hh .. 64hh+63, read back from TMEM
+                        uint32_t qa[32];
+                        tmem_ld32(q_addr + 32 * hh, qa);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 kw = swz_chunk(kst + hh * KV_BOX_BYTES, row, c);
+                            const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 kf = bf2(ka[e]), qf = bf2(qa[4 * c + e]);
+                                acc[2 * e] = fmaf(qf.x, kf.x, acc[2 * e]);
+                                acc[2 * e + 1] = fmaf(qf.y, kf.y, acc[2 * e + 1]);
+                            }
+                        }
+                    }
+                    const float sd = (((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                                      ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * sc;
+                    if (sd > mref + kRescaleThreshold || mref == -INFINITY) {
+                        const float alpha = mref == -INFINITY ? 0.f : exp2f(mref - sd);
+#pragma unroll
+                        for (int e = 0; e < kHeadDim; ++e) oacc[e] *= alpha;
+                        l *= alpha;
+                        mref = sd;
+                    }
+                    const float p = ex2_approx(sd - mref);
+                    l += p;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 vw = swz_chunk(vst + hh * KV_BOX_BYTES, row, c);
+                            const uint32_t va[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 vf = bf2(va[e]);
+                                const int d0 = 64 * hh + 8 * c + 2 * e;
+                                oacc[d0] = fmaf(p, vf.x, oacc[d0]);
+                                oacc[d0 + 1] = fmaf(p, vf.y, oacc[d0 + 1]);
+                            }
+                        }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s32(&bars->drel[st]));
+            }
+            const float inv = (got && l > 0.f) ? 1.f / l : 0.f;
+            if (valid) {
+#pragma unroll
+                for (int e = 0; e < kHeadDim; e += 8) {
+                    const uint4 w = make_uint4(pack2(oacc[e] * inv, oacc[e + 1] * inv),
+                                               pack2(oacc[e + 2] * inv, oacc[e + 3] * inv),
+                                               pack2(oacc[e + 4] * inv, oacc[e + 5] * inv),
+                                               pack2(oacc[e + 6] * inv, oacc[e + 7] * inv));
+                    *reinterpret_cast<uint4*>(dst0 + e) = w;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && *abort_flag) flag_error(a.dev_status, EAGLE_DEV_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace ttt_tc
+}  // namespace eagle

@@ -11,7 +11,8 @@
  *   eagle_kv_compact     move the accepted path's K/V rows behind the committed
  *                        prefix and advance the logical length
  * plus two building blocks exposed for measurement and testing
- * (eagle_softmax_stats, eagle_lmhead_gemm).
+ * (eagle_softmax_stats, eagle_lmhead_gemm), and the draft head's
+ * training-time-test attention (eagle_ttt_attn).
  *
  * Pages (cited by title and section):
  *   Lesson: "推测解码与 EAGLE-3" -- "不变量：Leviathan 拒绝采样", "KV cache 回滚",
@@ -20,7 +21,8 @@
  *           "无损性的来源与它的证明位置", "EAGLE-2：草稿树的 Expansion 与 Reranking",
  *           "EAGLE-3：取消特征约束..." (the draft head's own lm_head),
  *           "一次 eagenerate 调用的完整流转".
- *   TTT:    "EAGLE-3 完全拆解：Training-Time Test ..." -- "EAGLE-3 和 EAGLE-2 动态树如何拼在一起".
+ *   TTT:    "EAGLE-3 完全拆解：Training-Time Test ..." -- "EAGLE-3 和 EAGLE-2 动态树如何拼在一起",
+ *           "训练时的 attention mask 为什么要特殊处理".
  *
  * Conventions shared by every call
  *   - Every pointer is caller-owned DEVICE memory unless stated otherwise; the
@@ -216,6 +218,32 @@ eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, con
                               const int32_t* accept_len, int n_layers, int B, int Hkv,
                               int head_dim, int Lmax, int max_depth, int32_t* dev_status,
                               eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * eagle_ttt_attn -- training-time-test attention for one layer and one round.
+ * TTT page, section "训练时的 attention mask 为什么要特殊处理": round 0 runs on
+ * the original tokens with the causal mask; in round r >= 1 position i holds the
+ * token the previous round predicted there, and it may see only its ancestors.
+ * For sequence b, position i, query head h (kv head h / (Hq/Hkv)), queries of
+ * round r:
+ *   keys  = round-0 rows 0 .. i (the original tokens up to i) plus the rows of
+ *           rounds 1 .. r at position i (its own chain, itself included);
+ *   out   = softmax(scale * q . k) . v, fp32 accumulation, bf16 result.
+ * The causal part runs on the tensor cores; the diagonal part (at most R1 - 1
+ * keys per query) as per-position dot products, as the page suggests.
+ *   q    bf16 [B, S, Hq, head_dim]        (the queries of round r)
+ *   k, v bf16 [B, Hkv, R1, S, head_dim]   (round 0 = original tokens; rounds
+ *        1 .. R1-1 simulated; only rounds 0 .. r are read)
+ *   out  bf16 [B, S, Hq, head_dim]
+ * Sizes: S >= 1, 1 <= R1 <= 16, 0 <= r < R1, head_dim == 128, Hq % Hkv == 0,
+ * ceil(S * Hq / Hkv / 128) <= 65535.  Every row of round 0 must be finite (rows
+ * past a query's position are read and masked).  All pointers 16-byte aligned;
+ * with B == 0 nothing is read or written and they may be NULL.
+ * Device errors: a wait that exceeds its limit sets EAGLE_DEV_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_ttt_attn(const void* q, const void* k, const void* v, void* out, int B, int S,
+                            int Hq, int Hkv, int head_dim, int R1, int r, float scale,
+                            int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * eagle2_expand -- one level of EAGLE-2 expansion; optionally the rerank.

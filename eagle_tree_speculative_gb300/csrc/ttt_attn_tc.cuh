@@ -198,6 +198,9 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
                 tma_prefetch_3d(map, 0, jp * TBN, kvz);
                 tma_prefetch_3d(map, 64, jp * TBN, kvz);
             }
+            // round-0 K/V tiles are read by every row tile of the (sequence, kv head):
+            // keep them in L2; each diagonal row is read once: let it go first
+            const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
             for (int t = 0; t < T + ND; ++t) {
                 const int st = t % NSTAGES;
                 if (t >= NSTAGES) {
@@ -219,13 +222,13 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
                         tma_prefetch_3d(map, 64, yp, kvz);
                     }
                     mbar_expect_tx(fb, K_BYTES);
-                    tma_load_3d(s32(dst), map, fb, 0, t * TBN, kvz);
-                    tma_load_3d(s32(dst + KV_BOX_BYTES), map, fb, 64, t * TBN, kvz);
+                    tma_load_3d_hint(s32(dst), map, fb, 0, t * TBN, kvz, keep);
+                    tma_load_3d_hint(s32(dst + KV_BOX_BYTES), map, fb, 64, t * TBN, kvz, keep);
                 } else {
                     mbar_expect_tx(fb, (uint32_t)(2 * 128 * a.PB * a.RB));
                     const int u0 = 1 + (t - T) * a.RB;            // first round of the box
-                    tma_load_4d(s32(dst), dmap, fb, 0, imin, u0, kvz);
-                    tma_load_4d(s32(dst + KV_BOX_BYTES), dmap, fb, 64, imin, u0, kvz);
+                    tma_load_4d_hint(s32(dst), dmap, fb, 0, imin, u0, kvz, once);
+                    tma_load_4d_hint(s32(dst + KV_BOX_BYTES), dmap, fb, 64, imin, u0, kvz, once);
                 }
             }
         }

@@ -43,6 +43,17 @@ __device__ __forceinline__ uint32_t order_key(float l) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// A filter written by another CTA of the cluster: read at L2, past this SM's L1.
+__device__ __forceinline__ FilterParam load_filter(const FilterParam* f) {
+    static_assert(sizeof(FilterParam) == 32, "two 16-byte words");
+    const uint4 w0 = __ldcg(reinterpret_cast<const uint4*>(f));
+    const uint4 w1 = __ldcg(reinterpret_cast<const uint4*>(f) + 1);
+    FilterParam r;
+    memcpy(&r, &w0, 16);
+    memcpy(reinterpret_cast<char*>(&r) + 16, &w1, 16);
+    return r;
+}
+
 __device__ __forceinline__ bool filter_keeps(const FilterParam& f, int t, float l) {
     const uint32_t k = order_key(l);
     return k > f.key || (k == f.key && t <= f.idx);
@@ -65,8 +76,10 @@ struct VerifyArgs {
     int32_t* dev_status;
     int Vd;                // draft-row length (= V without a draft vocabulary)
     const int32_t* t2d;    // target id -> draft id or -1 (draft vocabulary only)
-    const FilterParam* fq; // per target row [B * n], filtered walk only
-    const FilterParam* fp; // per draft row [B * R], filtered walk only
+    FilterParam* fq;       // per target row [B * n], filtered walk only (written on visit)
+    FilterParam* fp;       // per draft row [B * R], filtered walk only (written on visit)
+    int top_k;             // filtered walk only
+    float top_p;
 };
 
 // Softmax statistics of a row at temperature T, kept over the raw logits:
@@ -426,10 +439,403 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
 }
 
 // ---------------------------------------------------------------------------
+// Row filters for the filtered walk (top-k, then top-p over what top-k kept): one CTA
+// per row, computed when the walk reaches the row's node.  The cut is found by a radix select over the rows' order keys (11-bit
+// digits, most significant first), with per-bin counts and fixed-point masses
+// (2^((l - max) c) scaled by 2^40, integer sums, so the decisions do not depend on
+// the order of the atomics); ties at the cut go to the lower token.
+// ---------------------------------------------------------------------------
+constexpr int kFiltThreads = 256;
+constexpr int kFiltBins = 2048;
+constexpr int kFiltMaxV = 1 << 22;              // the index select uses two 11-bit digits
+
+constexpr int kCand = 2048;                    // largest bin the sorted path takes
+
+struct FiltSmem {
+    unsigned int cnt[kFiltBins];
+    unsigned long long mass[kFiltBins];
+    unsigned long long sk[kCand];              // a bin's elements: (key << 32) | ~index, sorted
+    int ncand;
+    unsigned int wcnt[kFiltThreads / 32];
+    unsigned long long wmass[kFiltThreads / 32];
+    float redf[kFiltThreads / 32];
+    int redi[kFiltThreads / 32];
+    int found_bin;
+    unsigned int found_cnt;
+    unsigned long long found_mass;
+    int imax;
+};
+
+__device__ __forceinline__ unsigned long long fixed_mass(float l, float lmax, float c) {
+    return __float2ull_rz(exp2f((l - lmax) * c) * 0x1p40f);     // exact: <= 2^40, 24-bit mantissa
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Distance bin of a logit: (max - l) c in 1/64 of a log2 unit, the far tail (mass below
+// 2^-31.98 of the maximum's) in the last bin.  Monotone: a larger logit never has a
+// larger bin, and equal logits share one.
+__device__ __forceinline__ int dist_bin(float l, float lmax, float c) {
+    const float d = (lmax - l) * c;
+    return d < (float)(kFiltBins - 1) / 64.f ? (int)(d * 64.f) : kFiltBins - 1;
+}
+
+// Calls f(t, x[t]) for every t in [0, V), spread over the CTA's kFiltThreads threads;
+// four float4 loads in flight per thread when x is 16-byte aligned and V a multiple of
+// 4.  The order in which one thread sees its elements is fixed.
+template <class F>
+__device__ __forceinline__ void row_for_each(const float* __restrict__ x, int V, F&& f) {
+    const int tid = threadIdx.x;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0 && (V & 3) == 0) {
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        const int V4 = V >> 2;
+        int i = tid;
+        for (; i + 3 * kFiltThreads < V4; i += 4 * kFiltThreads) {
+            float4 w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w[u] = __ldg(x4 + i + u * kFiltThreads);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * (i + u * kFiltThreads);
+                f(t, w[u].x);
+                f(t + 1, w[u].y);
+                f(t + 2, w[u].z);
+                f(t + 3, w[u].w);
+            }
+        }
+        for (; i < V4; i += kFiltThreads) {
+            const float4 w = __ldg(x4 + i);
+            const int t = 4 * i;
+            f(t, w.x);
+            f(t + 1, w.y);
+            f(t + 2, w.z);
+            f(t + 3, w.w);
+        }
+    } else {
+        for (int t = tid; t < V; t += kFiltThreads) f(t, x[t]);
+    }
+}
+
+// Gather the elements of distance bin b (at most kCand of them) and sort them by (key
+// desc, index asc) into sm.sk[0 .. ncand).
+__device__ void gather_sort(FiltSmem& sm, const float* x, int V, int b, float lmax, float c) {
+    const int tid = threadIdx.x;
+    if (tid == 0) sm.ncand = 0;
+    __syncthreads();
+    row_for_each(x, V, [&](int t, float l) {
+        if (dist_bin(l, lmax, c) == b) {
+            const int pos = atomicAdd(&sm.ncand, 1);
+            if (pos < kCand)
+                sm.sk[pos] = ((unsigned long long)order_key(l) << 32) | (unsigned long long)(~(uint32_t)t);
+        }
+    });
+    __syncthreads();
+    const int n = min(sm.ncand, kCand);
+    int n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (int j = n + tid; j < n2; j += kFiltThreads) sm.sk[j] = 0ull;     // sorts last
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < n2; i += kFiltThreads) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long a = sm.sk[i], bb = sm.sk[j];
+                    if (desc ? (a < bb) : (a > bb)) { sm.sk[i] = bb; sm.sk[j] = a; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Add one element (count 1, mass m) to bin `bin` of the block histogram; bin < 0 adds
+// nothing, and a zero mass skips the 64-bit atomic.
+__device__ __forceinline__ void hist_add(FiltSmem& sm, int bin, unsigned long long m) {
+    if (bin < 0) return;
+    atomicAdd(&sm.cnt[bin], 1u);
+    if (m) atomicAdd(&sm.mass[bin], m);
+}
+
+__device__ __forceinline__ bool elig(uint32_t k, int t, uint32_t k0, int i0) {
+    return k > k0 || (k == k0 && t <= i0);
+}
+
+// Scan the bins in rank order (descending when DESC) for the bin where the running metric
+// (count, or mass when MASS) first reaches `remaining` (>= 1, <= the bins' total).  Writes
+// found_bin and the count and mass of the bins before it.
+template <bool MASS, bool DESC>
+__device__ void scan_bins(FiltSmem& sm, int nb, unsigned long long remaining) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = nb / kFiltThreads;
+    const int first = DESC ? nb - 1 - tid * per : tid * per;
+    if (tid == 0) { sm.found_bin = 0; sm.found_cnt = 0u; sm.found_mass = 0ull; }
+    unsigned int lc = 0;
+    unsigned long long lm = 0;
+    for (int j = 0; j < per; ++j) {
+        const int bin = DESC ? first - j : first + j;
+        lc += sm.cnt[bin];
+        lm += sm.mass[bin];
+    }
+    unsigned int ic = lc;
+    unsigned long long im = lm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int yc = __shfl_up_sync(0xffffffffu, ic, o);
+        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
+        if (lane >= o) { ic += yc; im += ym; }
+    }
+    if (lane == 31) { sm.wcnt[warp] = ic; sm.wmass[warp] = im; }
+    __syncthreads();
+    unsigned int rc = ic - lc;
+    unsigned long long rm = im - lm;
+    for (int w = 0; w < warp; ++w) { rc += sm.wcnt[w]; rm += sm.wmass[w]; }
+    const unsigned long long before = MASS ? rm : rc, mine = MASS ? lm : lc;
+    if (before < remaining && before + mine >= remaining) {
+        for (int j = 0; j < per; ++j) {
+            const int bin = DESC ? first - j : first + j;
+            const unsigned long long v = MASS ? sm.mass[bin] : sm.cnt[bin];
+            if ((MASS ? rm : rc) + v >= remaining) {
+                sm.found_bin = bin;
+                sm.found_cnt = rc;
+                sm.found_mass = rm;
+                break;
+            }
+            rc += sm.cnt[bin];
+            rm += sm.mass[bin];
+        }
+    }
+    __syncthreads();
+}
+
+struct Cut {
+    uint32_t key;
+    int idx;
+    unsigned long long mass_upto;     // mass of the elements up to and including the cut
+};
+
+// Among the row's elements eligible under (k0, i0), in rank order (key desc, index asc),
+// the element at which the running count (MASS false) or fixed-point mass (MASS true)
+// first reaches `target` (1 <= target <= the eligible total).
+template <bool MASS>
+__device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, float c,
+                            unsigned long long target, uint32_t k0, int i0) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0u, pmask = 0u;
+    unsigned long long mb = 0ull, remaining = target, m_eq_total = 0ull;
+    unsigned int n_eq = 0u;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        for (int i = tid; i < nb; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+        __syncthreads();
+        for (int base = 0; base < V; base += kFiltThreads) {          // warp-uniform trips
+            const int t = base + tid;
+            const float l = t < V ? x[t] : -INFINITY;
+            const uint32_t k = order_key(l);
+            const bool in = t < V && (k & pmask) == prefix && elig(k, t, k0, i0);
+            hist_add(sm, in ? (int)((k >> shift) & (uint32_t)(nb - 1)) : -1,
+                     in ? fixed_mass(l, lmax, c) : 0ull);
+        }
+        __syncthreads();
+        scan_bins<MASS, true>(sm, nb, remaining);
+        const int bin = sm.found_bin;
+        remaining -= MASS ? sm.found_mass : (unsigned long long)sm.found_cnt;
+        mb += sm.found_mass;
+        if (pass == 2) { n_eq = sm.cnt[bin]; m_eq_total = sm.mass[bin]; }
+        prefix |= (uint32_t)bin << shift;
+        pmask |= (uint32_t)(nb - 1) << shift;
+        __syncthreads();
+    }
+    // the elements whose key is the cut's: they share one value, so one mass each; the
+    // cut keeps the first `need` of them by index
+    if (n_eq == 0u) n_eq = 1u;                         // (cannot happen: the cut's bin is not empty)
+    const unsigned long long m_eq = m_eq_total / n_eq;
+    unsigned long long need = MASS ? (remaining + m_eq - 1ull) / m_eq : remaining;
+    if (need > n_eq) need = n_eq;
+    int idx;
+    if (need == n_eq) {
+        if (tid == 0) sm.imax = -1;
+        __syncthreads();
+        for (int t = tid; t < V; t += kFiltThreads)
+            if (order_key(x[t]) == prefix && elig(prefix, t, k0, i0)) atomicMax(&sm.imax, t);
+        __syncthreads();
+        idx = sm.imax;
+        __syncthreads();
+    } else {
+        uint32_t iprefix = 0u, imask = 0u;
+        unsigned long long rem = need;
+        for (int pass = 0; pass < 2; ++pass) {
+            const int shift = pass == 0 ? 11 : 0;
+            for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+            __syncthreads();
+            for (int base = 0; base < V; base += kFiltThreads) {      // warp-uniform trips
+                const int t = base + tid;
+                bool in = t < V && ((uint32_t)t & imask) == iprefix;
+                if (in) {
+                    const uint32_t k = order_key(x[t]);
+                    in = k == prefix && elig(k, t, k0, i0);
+                }
+                hist_add(sm, in ? (int)(((uint32_t)t >> shift) & (kFiltBins - 1)) : -1, 0ull);
+            }
+            __syncthreads();
+            scan_bins<false, false>(sm, kFiltBins, rem);
+            rem -= sm.found_cnt;
+            iprefix |= (uint32_t)sm.found_bin << shift;
+            imask |= (uint32_t)(kFiltBins - 1) << shift;
+            __syncthreads();
+        }
+        idx = (int)iprefix;
+    }
+    return Cut{prefix, idx, mb + need * m_eq};
+}
+
+// The filter of one row of logits x[0 .. V-1] at c = log2(e) / T, computed by the
+// whole CTA (kFiltThreads threads, all of which must call it): the maximum, the cut
+// (order key, index) of the kept set and the kept set's sum of exp2((l - max) c).
+// Thread 0 writes *out.
+__device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, float c, int top_k,
+                           float top_p, FilterParam* out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float mx = -INFINITY;
+    int bad = 0;
+    row_for_each(x, V, [&](int, float l) {
+        bad |= (l != l) | (l == INFINITY);
+        mx = fmaxf(mx, l);
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) { sm.redf[warp] = mx; sm.redi[warp] = bad; }
+    __syncthreads();
+    float lmax = -INFINITY;
+    int bd = 0;
+    for (int w = 0; w < kFiltThreads / 32; ++w) { lmax = fmaxf(lmax, sm.redf[w]); bd |= sm.redi[w]; }
+    __syncthreads();
+    if (bd || lmax == -INFINITY) {
+        if (tid == 0) *out = FilterParam{lmax, 0.f, 0u, 0, 1, 0, 0, 0};
+        return;
+    }
+    uint32_t key = 0u;                 // keep everything
+    int idx = 0x7fffffff;
+    const bool do_k = top_k > 0 && top_k < V;
+    const bool do_p = top_p > 0.f && top_p < 1.f;
+    auto fm = [&](unsigned long long e) { return fixed_mass(key_float((uint32_t)(e >> 32)), lmax, c); };
+    if (do_k || do_p) {
+        // Fast path: a histogram over distance bins (fine where the probability mass is),
+        // then an exact sort of the one bin the cut falls in.  The radix select takes over
+        // when that bin is the far tail or holds more than kCand elements.
+        for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+        __syncthreads();
+        row_for_each(x, V, [&](int, float l) {
+            hist_add(sm, dist_bin(l, lmax, c), do_p ? fixed_mass(l, lmax, c) : 0ull);
+        });
+        __syncthreads();
+        bool hist = true;                 // the histogram is still intact
+        int bk = -1, nk = 0;              // top-k cut: its bin, and how many of its sorted elements stay
+        unsigned long long mk = 0ull;     // mass of the bins before bk
+        unsigned long long total = 0ull;  // mass of what top-k keeps
+        if (do_k) {
+            scan_bins<false, false>(sm, kFiltBins, (unsigned long long)top_k);
+            const int bin = sm.found_bin;
+            const unsigned int cb = sm.found_cnt;
+            mk = sm.found_mass;
+            if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
+                gather_sort(sm, x, V, bin, lmax, c);
+                nk = top_k - (int)cb;
+                const unsigned long long e = sm.sk[nk - 1];
+                key = (uint32_t)(e >> 32);
+                idx = (int)(~(uint32_t)e);
+                total = mk;
+                for (int j = 0; j < nk; ++j) total += fm(sm.sk[j]);
+                bk = bin;
+            } else {
+                const Cut k = block_select<false>(sm, x, V, lmax, c, (unsigned long long)top_k, 0u,
+                                                  0x7fffffff);
+                key = k.key;
+                idx = k.idx;
+                total = k.mass_upto;
+                hist = false;
+            }
+        }
+        if (do_p) {
+            if (!do_k)
+                for (int i = 0; i < kFiltBins; ++i) total += sm.mass[i];
+            unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
+            tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
+            bool done = false;
+            if (hist && bk >= 0 && tgt > mk) {
+                // the cut lies among the elements of bk that top-k keeps (already sorted)
+                unsigned long long acc = mk;
+                int j = 0;
+                for (; j < nk - 1; ++j) {
+                    acc += fm(sm.sk[j]);
+                    if (acc >= tgt) break;
+                }
+                key = (uint32_t)(sm.sk[j] >> 32);
+                idx = (int)(~(uint32_t)sm.sk[j]);
+                done = true;
+            } else if (hist) {
+                if (bk >= 0) {            // only the bins before top-k's cut bin remain eligible
+                    __syncthreads();
+                    for (int i = bk + tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+                    __syncthreads();
+                }
+                scan_bins<true, false>(sm, kFiltBins, tgt);
+                const int bin = sm.found_bin;
+                const unsigned long long mb = sm.found_mass;
+                if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
+                    gather_sort(sm, x, V, bin, lmax, c);
+                    const int n = min(sm.ncand, kCand);
+                    unsigned long long acc = mb;
+                    int j = 0;
+                    for (; j < n - 1; ++j) {
+                        acc += fm(sm.sk[j]);
+                        if (acc >= tgt) break;
+                    }
+                    key = (uint32_t)(sm.sk[j] >> 32);
+                    idx = (int)(~(uint32_t)sm.sk[j]);
+                    done = true;
+                }
+            }
+            if (!done) {
+                __syncthreads();
+                const Cut pc = block_select<true>(sm, x, V, lmax, c, tgt, key, idx);
+                idx = pc.key == key ? min(pc.idx, idx) : pc.idx;
+                key = pc.key;
+            }
+        }
+        __syncthreads();
+    }
+    // S over the kept set; per-thread sums combined in a fixed order
+    float s = 0.f;
+    row_for_each(x, V, [&](int t, float l) {
+        if (elig(order_key(l), t, key, idx)) s += exp2f((l - lmax) * c);
+    });
+    s = warp_sum(s);
+    if (lane == 0) sm.redf[warp] = s;
+    __syncthreads();
+    if (tid == 0) {
+        float S = 0.f;
+        for (int w = 0; w < kFiltThreads / 32; ++w) S += sm.redf[w];
+        *out = FilterParam{lmax, S, key, idx, 0, 0, 0, 0};
+    }
+}
+
+// ---------------------------------------------------------------------------
 template <int CS, int NT, bool D2T, bool FILT>
 __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
     using C = Cluster<CS, NT>;
     __shared__ VerifySmem<NT> sm;
+    FiltSmem* fsm = nullptr;                 // the filtered walk's row-filter scratch
+    if constexpr (FILT) {
+        static_assert(NT == kFiltThreads, "a row filter takes the whole CTA");
+        __shared__ FiltSmem fs;
+        fsm = &fs;
+    }
     const int tid = threadIdx.x;
     const int rank = cta_rank_in_cluster(CS);
     const int b = blockIdx.x / CS;
@@ -505,8 +911,20 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
             // filtered walk: this node's row filters; logits outside them read as -inf
             FilterParam fqv{}, fpv{};
             if constexpr (FILT) {
-                fqv = a.fq[(int64_t)b * n + v];
-                if (prow) fpv = a.fp[(int64_t)b * a.R + sm.row[v]];
+                // Filtered only now that the walk has reached v: rank 0 filters q(v) and
+                // rank 1 (rank 0 again in a one-CTA cluster) p(v); after the cluster
+                // barrier every CTA reads both filters back past L1.
+                FilterParam* fq_slot = a.fq + (int64_t)b * n + v;
+                FilterParam* fp_slot = prow ? a.fp + (int64_t)b * a.R + sm.row[v] : nullptr;
+                if (rank == 0) filter_row(*fsm, qrow, V, c, a.top_k, a.top_p, fq_slot);
+                if (prow && rank == (CS > 1 ? 1 : 0)) {
+                    if constexpr (CS == 1) __syncthreads();
+                    filter_row(*fsm, prow, V, c, a.top_k, a.top_p, fp_slot);
+                }
+                __threadfence();
+                C::sync();
+                fqv = load_filter(fq_slot);
+                if (prow) fpv = load_filter(fp_slot);
             }
             auto mq = [&](int t, float l) -> float {
                 if constexpr (FILT) return filter_keeps(fqv, t, l) ? l : -INFINITY;
@@ -844,379 +1262,6 @@ softmax_stats_kernel(const float* __restrict__ logits, int64_t rows, int V, floa
     }
 }
 
-// ---------------------------------------------------------------------------
-// Row filters for the filtered walk (top-k, then top-p over what top-k kept): one CTA
-// per row.  The cut is found by a radix select over the rows' order keys (11-bit
-// digits, most significant first), with per-bin counts and fixed-point masses
-// (2^((l - max) c) scaled by 2^40, integer sums, so the decisions do not depend on
-// the order of the atomics); ties at the cut go to the lower token.
-// ---------------------------------------------------------------------------
-constexpr int kFiltThreads = 256;
-constexpr int kFiltBins = 2048;
-constexpr int kFiltMaxV = 1 << 22;              // the index select uses two 11-bit digits
-
-constexpr int kCand = 2048;                    // largest bin the sorted path takes
-
-struct FiltSmem {
-    unsigned int cnt[kFiltBins];
-    unsigned long long mass[kFiltBins];
-    unsigned long long sk[kCand];              // a bin's elements: (key << 32) | ~index, sorted
-    int ncand;
-    unsigned int wcnt[kFiltThreads / 32];
-    unsigned long long wmass[kFiltThreads / 32];
-    float redf[kFiltThreads / 32];
-    int redi[kFiltThreads / 32];
-    int found_bin;
-    unsigned int found_cnt;
-    unsigned long long found_mass;
-    int imax;
-};
-
-__device__ __forceinline__ unsigned long long fixed_mass(float l, float lmax, float c) {
-    return __float2ull_rz(exp2f((l - lmax) * c) * 0x1p40f);     // exact: <= 2^40, 24-bit mantissa
-}
-
-__device__ __forceinline__ float key_float(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// Distance bin of a logit: (max - l) c in 1/64 of a log2 unit, the far tail (mass below
-// 2^-31.98 of the maximum's) in the last bin.  Monotone: a larger logit never has a
-// larger bin, and equal logits share one.
-__device__ __forceinline__ int dist_bin(float l, float lmax, float c) {
-    const float d = (lmax - l) * c;
-    return d < (float)(kFiltBins - 1) / 64.f ? (int)(d * 64.f) : kFiltBins - 1;
-}
-
-// Gather the elements of distance bin b (at most kCand of them) and sort them by (key
-// desc, index asc) into sm.sk[0 .. ncand).
-__device__ void gather_sort(FiltSmem& sm, const float* x, int V, int b, float lmax, float c) {
-    const int tid = threadIdx.x;
-    if (tid == 0) sm.ncand = 0;
-    __syncthreads();
-    for (int t = tid; t < V; t += kFiltThreads) {
-        const float l = x[t];
-        if (dist_bin(l, lmax, c) == b) {
-            const int pos = atomicAdd(&sm.ncand, 1);
-            if (pos < kCand)
-                sm.sk[pos] = ((unsigned long long)order_key(l) << 32) | (unsigned long long)(~(uint32_t)t);
-        }
-    }
-    __syncthreads();
-    const int n = min(sm.ncand, kCand);
-    int n2 = 1;
-    while (n2 < n) n2 <<= 1;
-    for (int j = n + tid; j < n2; j += kFiltThreads) sm.sk[j] = 0ull;     // sorts last
-    __syncthreads();
-    for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < n2; i += kFiltThreads) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;
-                    const unsigned long long a = sm.sk[i], bb = sm.sk[j];
-                    if (desc ? (a < bb) : (a > bb)) { sm.sk[i] = bb; sm.sk[j] = a; }
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// Add one element (count 1, mass m) to bin `bin` of the block histogram; bin < 0 adds
-// nothing, and a zero mass skips the 64-bit atomic.
-__device__ __forceinline__ void hist_add(FiltSmem& sm, int bin, unsigned long long m) {
-    if (bin < 0) return;
-    atomicAdd(&sm.cnt[bin], 1u);
-    if (m) atomicAdd(&sm.mass[bin], m);
-}
-
-__device__ __forceinline__ bool elig(uint32_t k, int t, uint32_t k0, int i0) {
-    return k > k0 || (k == k0 && t <= i0);
-}
-
-// Scan the bins in rank order (descending when DESC) for the bin where the running metric
-// (count, or mass when MASS) first reaches `remaining` (>= 1, <= the bins' total).  Writes
-// found_bin and the count and mass of the bins before it.
-template <bool MASS, bool DESC>
-__device__ void scan_bins(FiltSmem& sm, int nb, unsigned long long remaining) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = nb / kFiltThreads;
-    const int first = DESC ? nb - 1 - tid * per : tid * per;
-    if (tid == 0) { sm.found_bin = 0; sm.found_cnt = 0u; sm.found_mass = 0ull; }
-    unsigned int lc = 0;
-    unsigned long long lm = 0;
-    for (int j = 0; j < per; ++j) {
-        const int bin = DESC ? first - j : first + j;
-        lc += sm.cnt[bin];
-        lm += sm.mass[bin];
-    }
-    unsigned int ic = lc;
-    unsigned long long im = lm;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned int yc = __shfl_up_sync(0xffffffffu, ic, o);
-        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
-        if (lane >= o) { ic += yc; im += ym; }
-    }
-    if (lane == 31) { sm.wcnt[warp] = ic; sm.wmass[warp] = im; }
-    __syncthreads();
-    unsigned int rc = ic - lc;
-    unsigned long long rm = im - lm;
-    for (int w = 0; w < warp; ++w) { rc += sm.wcnt[w]; rm += sm.wmass[w]; }
-    const unsigned long long before = MASS ? rm : rc, mine = MASS ? lm : lc;
-    if (before < remaining && before + mine >= remaining) {
-        for (int j = 0; j < per; ++j) {
-            const int bin = DESC ? first - j : first + j;
-            const unsigned long long v = MASS ? sm.mass[bin] : sm.cnt[bin];
-            if ((MASS ? rm : rc) + v >= remaining) {
-                sm.found_bin = bin;
-                sm.found_cnt = rc;
-                sm.found_mass = rm;
-                break;
-            }
-            rc += sm.cnt[bin];
-            rm += sm.mass[bin];
-        }
-    }
-    __syncthreads();
-}
-
-struct Cut {
-    uint32_t key;
-    int idx;
-    unsigned long long mass_upto;     // mass of the elements up to and including the cut
-};
-
-// Among the row's elements eligible under (k0, i0), in rank order (key desc, index asc),
-// the element at which the running count (MASS false) or fixed-point mass (MASS true)
-// first reaches `target` (1 <= target <= the eligible total).
-template <bool MASS>
-__device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, float c,
-                            unsigned long long target, uint32_t k0, int i0) {
-    const int tid = threadIdx.x;
-    uint32_t prefix = 0u, pmask = 0u;
-    unsigned long long mb = 0ull, remaining = target, m_eq_total = 0ull;
-    unsigned int n_eq = 0u;
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int nb = pass == 2 ? 1024 : 2048;
-        for (int i = tid; i < nb; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
-        __syncthreads();
-        for (int base = 0; base < V; base += kFiltThreads) {          // warp-uniform trips
-            const int t = base + tid;
-            const float l = t < V ? x[t] : -INFINITY;
-            const uint32_t k = order_key(l);
-            const bool in = t < V && (k & pmask) == prefix && elig(k, t, k0, i0);
-            hist_add(sm, in ? (int)((k >> shift) & (uint32_t)(nb - 1)) : -1,
-                     in ? fixed_mass(l, lmax, c) : 0ull);
-        }
-        __syncthreads();
-        scan_bins<MASS, true>(sm, nb, remaining);
-        const int bin = sm.found_bin;
-        remaining -= MASS ? sm.found_mass : (unsigned long long)sm.found_cnt;
-        mb += sm.found_mass;
-        if (pass == 2) { n_eq = sm.cnt[bin]; m_eq_total = sm.mass[bin]; }
-        prefix |= (uint32_t)bin << shift;
-        pmask |= (uint32_t)(nb - 1) << shift;
-        __syncthreads();
-    }
-    // the elements whose key is the cut's: they share one value, so one mass each; the
-    // cut keeps the first `need` of them by index
-    if (n_eq == 0u) n_eq = 1u;                         // (cannot happen: the cut's bin is not empty)
-    const unsigned long long m_eq = m_eq_total / n_eq;
-    unsigned long long need = MASS ? (remaining + m_eq - 1ull) / m_eq : remaining;
-    if (need > n_eq) need = n_eq;
-    int idx;
-    if (need == n_eq) {
-        if (tid == 0) sm.imax = -1;
-        __syncthreads();
-        for (int t = tid; t < V; t += kFiltThreads)
-            if (order_key(x[t]) == prefix && elig(prefix, t, k0, i0)) atomicMax(&sm.imax, t);
-        __syncthreads();
-        idx = sm.imax;
-        __syncthreads();
-    } else {
-        uint32_t iprefix = 0u, imask = 0u;
-        unsigned long long rem = need;
-        for (int pass = 0; pass < 2; ++pass) {
-            const int shift = pass == 0 ? 11 : 0;
-            for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
-            __syncthreads();
-            for (int base = 0; base < V; base += kFiltThreads) {      // warp-uniform trips
-                const int t = base + tid;
-                bool in = t < V && ((uint32_t)t & imask) == iprefix;
-                if (in) {
-                    const uint32_t k = order_key(x[t]);
-                    in = k == prefix && elig(k, t, k0, i0);
-                }
-                hist_add(sm, in ? (int)(((uint32_t)t >> shift) & (kFiltBins - 1)) : -1, 0ull);
-            }
-            __syncthreads();
-            scan_bins<false, false>(sm, kFiltBins, rem);
-            rem -= sm.found_cnt;
-            iprefix |= (uint32_t)sm.found_bin << shift;
-            imask |= (uint32_t)(kFiltBins - 1) << shift;
-            __syncthreads();
-        }
-        idx = (int)iprefix;
-    }
-    return Cut{prefix, idx, mb + need * m_eq};
-}
-
-__global__ void __launch_bounds__(kFiltThreads)
-row_filter_kernel(const float* __restrict__ target, int nq, const float* __restrict__ draft, int V,
-                  float c, int top_k, float top_p, FilterParam* fq, FilterParam* fp,
-                  const int32_t* __restrict__ parent, const int32_t* __restrict__ draft_row, int n,
-                  int R) {
-    __shared__ FiltSmem sm;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t r = blockIdx.x;
-    const bool isq = r < nq;
-    if (!isq) {
-        // a draft row is read only as the distribution after a node with children
-        const int b = (int)((r - nq) / R), row = (int)((r - nq) % R);
-        if (tid == 0) sm.imax = 0;
-        __syncthreads();
-        if (tid < n && tid > 0) {
-            const int p = parent[(int64_t)b * n + tid];
-            if (p >= 0 && p < n && (draft_row ? draft_row[(int64_t)b * n + p] : p) == row) sm.imax = 1;
-        }
-        __syncthreads();
-        if (!sm.imax) return;          // never read by the walk: left unwritten
-        __syncthreads();
-    }
-    const float* x = isq ? target + r * (int64_t)V : draft + (r - nq) * (int64_t)V;
-    FilterParam* out = isq ? fq + r : fp + (r - nq);
-    float mx = -INFINITY;
-    int bad = 0;
-    for (int t = tid; t < V; t += kFiltThreads) {
-        const float l = x[t];
-        bad |= (l != l) | (l == INFINITY);
-        mx = fmaxf(mx, l);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) { sm.redf[warp] = mx; sm.redi[warp] = bad; }
-    __syncthreads();
-    float lmax = -INFINITY;
-    int bd = 0;
-    for (int w = 0; w < kFiltThreads / 32; ++w) { lmax = fmaxf(lmax, sm.redf[w]); bd |= sm.redi[w]; }
-    __syncthreads();
-    if (bd || lmax == -INFINITY) {
-        if (tid == 0) *out = FilterParam{lmax, 0.f, 0u, 0, 1, 0, 0, 0};
-        return;
-    }
-    uint32_t key = 0u;                 // keep everything
-    int idx = 0x7fffffff;
-    const bool do_k = top_k > 0 && top_k < V;
-    const bool do_p = top_p > 0.f && top_p < 1.f;
-    auto fm = [&](unsigned long long e) { return fixed_mass(key_float((uint32_t)(e >> 32)), lmax, c); };
-    if (do_k || do_p) {
-        // Fast path: a histogram over distance bins (fine where the probability mass is),
-        // then an exact sort of the one bin the cut falls in.  The radix select takes over
-        // when that bin is the far tail or holds more than kCand elements.
-        for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
-        __syncthreads();
-        for (int base = 0; base < V; base += kFiltThreads) {          // warp-uniform trips
-            const int t = base + tid;
-            const bool in = t < V;
-            const float l = in ? x[t] : -INFINITY;
-            hist_add(sm, in ? dist_bin(l, lmax, c) : -1, in && do_p ? fixed_mass(l, lmax, c) : 0ull);
-        }
-        __syncthreads();
-        bool hist = true;                 // the histogram is still intact
-        int bk = -1, nk = 0;              // top-k cut: its bin, and how many of its sorted elements stay
-        unsigned long long mk = 0ull;     // mass of the bins before bk
-        unsigned long long total = 0ull;  // mass of what top-k keeps
-        if (do_k) {
-            scan_bins<false, false>(sm, kFiltBins, (unsigned long long)top_k);
-            const int bin = sm.found_bin;
-            const unsigned int cb = sm.found_cnt;
-            mk = sm.found_mass;
-            if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
-                gather_sort(sm, x, V, bin, lmax, c);
-                nk = top_k - (int)cb;
-                const unsigned long long e = sm.sk[nk - 1];
-                key = (uint32_t)(e >> 32);
-                idx = (int)(~(uint32_t)e);
-                total = mk;
-                for (int j = 0; j < nk; ++j) total += fm(sm.sk[j]);
-                bk = bin;
-            } else {
-                const Cut k = block_select<false>(sm, x, V, lmax, c, (unsigned long long)top_k, 0u,
-                                                  0x7fffffff);
-                key = k.key;
-                idx = k.idx;
-                total = k.mass_upto;
-                hist = false;
-            }
-        }
-        if (do_p) {
-            if (!do_k)
-                for (int i = 0; i < kFiltBins; ++i) total += sm.mass[i];
-            unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
-            tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
-            bool done = false;
-            if (hist && bk >= 0 && tgt > mk) {
-                // the cut lies among the elements of bk that top-k keeps (already sorted)
-                unsigned long long acc = mk;
-                int j = 0;
-                for (; j < nk - 1; ++j) {
-                    acc += fm(sm.sk[j]);
-                    if (acc >= tgt) break;
-                }
-                key = (uint32_t)(sm.sk[j] >> 32);
-                idx = (int)(~(uint32_t)sm.sk[j]);
-                done = true;
-            } else if (hist) {
-                if (bk >= 0) {            // only the bins before top-k's cut bin remain eligible
-                    __syncthreads();
-                    for (int i = bk + tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
-                    __syncthreads();
-                }
-                scan_bins<true, false>(sm, kFiltBins, tgt);
-                const int bin = sm.found_bin;
-                const unsigned long long mb = sm.found_mass;
-                if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
-                    gather_sort(sm, x, V, bin, lmax, c);
-                    const int n = min(sm.ncand, kCand);
-                    unsigned long long acc = mb;
-                    int j = 0;
-                    for (; j < n - 1; ++j) {
-                        acc += fm(sm.sk[j]);
-                        if (acc >= tgt) break;
-                    }
-                    key = (uint32_t)(sm.sk[j] >> 32);
-                    idx = (int)(~(uint32_t)sm.sk[j]);
-                    done = true;
-                }
-            }
-            if (!done) {
-                __syncthreads();
-                const Cut pc = block_select<true>(sm, x, V, lmax, c, tgt, key, idx);
-                idx = pc.key == key ? min(pc.idx, idx) : pc.idx;
-                key = pc.key;
-            }
-        }
-        __syncthreads();
-    }
-    // S over the kept set; per-thread sums combined in a fixed order
-    float s = 0.f;
-    for (int t = tid; t < V; t += kFiltThreads) {
-        const float l = x[t];
-        if (elig(order_key(l), t, key, idx)) s += exp2f((l - lmax) * c);
-    }
-    s = warp_sum(s);
-    if (lane == 0) sm.redf[warp] = s;
-    __syncthreads();
-    if (tid == 0) {
-        float S = 0.f;
-        for (int w = 0; w < kFiltThreads / 32; ++w) S += sm.redf[w];
-        *out = FilterParam{lmax, S, key, idx, 0, 0, 0, 0};
-    }
-}
 
 int verify_cluster_size(int B) {
     static int forced = -1;
@@ -1277,7 +1322,7 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
     const float c = temperature > 0.f ? kLog2e / temperature : 0.f;
     VerifyArgs a{target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, max_depth,
                  temperature, c, seed, accept_len, path, emit, row_stats, dev_status, Vd, t2d,
-                 nullptr, nullptr};
+                 nullptr, nullptr, 0, 0.f};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool filt = temperature > 0.f && ((top_k > 0 && top_k < V) || (top_p > 0.f && top_p < 1.f));
     cudaError_t e;
@@ -1289,11 +1334,10 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
             return EAGLE_ERR_CAPACITY;
         FilterParam* fq = static_cast<FilterParam*>(workspace);
         FilterParam* fp = fq + (size_t)B * n;
-        row_filter_kernel<<<(unsigned)(B * (n + R)), kFiltThreads, 0, s>>>(
-            target_logits, B * n, draft_logits, V, c, top_k, top_p, fq, fp, parent, draft_row, n, R);
-        EAGLE_CHECK_LAUNCH();
         a.fq = fq;
         a.fp = fp;
+        a.top_k = top_k;
+        a.top_p = top_p;
         e = launch_walk<false, true>(a, s);
     } else {
         e = t2d ? launch_walk<true, false>(a, s) : launch_walk<false, false>(a, s);

@@ -156,7 +156,7 @@ eagle_status eagle_verify_accept(const float* target_logits, const float* draft_
  * at T = 0 (greedy) both are ignored.
  *   workspace  device, >= eagle_verify_filter_workspace_size(B, n, R) bytes,
  *              16-byte aligned; needed only when a filter is on (one 32-byte
- *              filter per target and draft row, computed for every row first).
+ *              filter per target and draft row, written when the walk visits it).
  * Errors: EAGLE_ERR_INVALID_ARG for top_k < 0 or top_p < 0 / not finite;
  * EAGLE_ERR_CAPACITY for a missing or small workspace; EAGLE_ERR_SHAPE for
  * V > 4194304.  The filter decisions use the probability mass in 2^-40 fixed

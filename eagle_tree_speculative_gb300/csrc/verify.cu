@@ -80,6 +80,7 @@ struct VerifyArgs {
     FilterParam* fp;       // per draft row [B * R], filtered walk only (written on visit)
     int top_k;             // filtered walk only
     float top_p;
+    bool target_in_device; // target rows in device memory (not pinned host memory)
 };
 
 // Softmax statistics of a row at temperature T, kept over the raw logits:
@@ -450,6 +451,7 @@ constexpr int kFiltBins = 2048;
 constexpr int kFiltMaxV = 1 << 22;              // the index select uses two 11-bit digits
 
 constexpr int kCand = 2048;                    // largest bin the sorted path takes
+constexpr int kNearBins = 256;                 // the first histogram's bins: 4 log2 units
 
 struct FiltSmem {
     unsigned int cnt[kFiltBins];
@@ -464,6 +466,9 @@ struct FiltSmem {
     unsigned int found_cnt;
     unsigned long long found_mass;
     int imax;
+    unsigned long long tot;                    // the row's total mass
+    unsigned long long near_mass;              // count and mass of the bins below the limit
+    unsigned int near_cnt;
 };
 
 __device__ __forceinline__ unsigned long long fixed_mass(float l, float lmax, float c) {
@@ -483,21 +488,22 @@ __device__ __forceinline__ int dist_bin(float l, float lmax, float c) {
 }
 
 // Calls f(t, x[t]) for every t in [0, V), spread over the CTA's kFiltThreads threads;
-// four float4 loads in flight per thread when x is 16-byte aligned and V a multiple of
-// 4.  The order in which one thread sees its elements is fixed.
+// eight float4 loads in flight per thread when x is 16-byte aligned and V a multiple
+// of 4.  The order in which one thread sees its elements is fixed.
 template <class F>
 __device__ __forceinline__ void row_for_each(const float* __restrict__ x, int V, F&& f) {
+    constexpr int DEPTH = 8;
     const int tid = threadIdx.x;
     if ((reinterpret_cast<uintptr_t>(x) & 15) == 0 && (V & 3) == 0) {
         const float4* x4 = reinterpret_cast<const float4*>(x);
         const int V4 = V >> 2;
         int i = tid;
-        for (; i + 3 * kFiltThreads < V4; i += 4 * kFiltThreads) {
-            float4 w[4];
+        for (; i + (DEPTH - 1) * kFiltThreads < V4; i += DEPTH * kFiltThreads) {
+            float4 w[DEPTH];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) w[u] = __ldg(x4 + i + u * kFiltThreads);
+            for (int u = 0; u < DEPTH; ++u) w[u] = __ldg(x4 + i + u * kFiltThreads);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < DEPTH; ++u) {
                 const int t = 4 * (i + u * kFiltThreads);
                 f(t, w[u].x);
                 f(t + 1, w[u].y);
@@ -518,14 +524,16 @@ __device__ __forceinline__ void row_for_each(const float* __restrict__ x, int V,
     }
 }
 
-// Gather the elements of distance bin b (at most kCand of them) and sort them by (key
-// desc, index asc) into sm.sk[0 .. ncand).
-__device__ void gather_sort(FiltSmem& sm, const float* x, int V, int b, float lmax, float c) {
+// Gather the elements of distance bin b (of bins 0 .. b when `upto`; at most kCand of
+// them) and sort them by (key desc, index asc) into sm.sk[0 .. ncand).
+__device__ void gather_sort(FiltSmem& sm, const float* x, int V, int b, float lmax, float c,
+                            bool upto) {
     const int tid = threadIdx.x;
     if (tid == 0) sm.ncand = 0;
     __syncthreads();
     row_for_each(x, V, [&](int t, float l) {
-        if (dist_bin(l, lmax, c) == b) {
+        const int bin = dist_bin(l, lmax, c);
+        if (upto ? bin <= b : bin == b) {
             const int pos = atomicAdd(&sm.ncand, 1);
             if (pos < kCand)
                 sm.sk[pos] = ((unsigned long long)order_key(l) << 32) | (unsigned long long)(~(uint32_t)t);
@@ -552,12 +560,24 @@ __device__ void gather_sort(FiltSmem& sm, const float* x, int V, int b, float lm
     }
 }
 
+// Adds m to a 64-bit shared-memory counter with 32-bit atomics: the low word first, then
+// the high word plus the carry out of that addition (read from the low word's old value).
+// Each addition's carry is its own, so once every thread is done the counter holds the
+// exact sum, whatever the order.
+__device__ __forceinline__ void add_u64_split(unsigned long long* ctr, unsigned long long m) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(ctr);      // little endian: w[0] low, w[1] high
+    const uint32_t lo = (uint32_t)m, hi = (uint32_t)(m >> 32);
+    const uint32_t old = atomicAdd(&w[0], lo);
+    const uint32_t up = hi + (old + lo < old ? 1u : 0u);
+    if (up) atomicAdd(&w[1], up);
+}
+
 // Add one element (count 1, mass m) to bin `bin` of the block histogram; bin < 0 adds
-// nothing, and a zero mass skips the 64-bit atomic.
+// nothing, and a zero mass skips the mass update.
 __device__ __forceinline__ void hist_add(FiltSmem& sm, int bin, unsigned long long m) {
     if (bin < 0) return;
     atomicAdd(&sm.cnt[bin], 1u);
-    if (m) atomicAdd(&sm.mass[bin], m);
+    if (m) add_u64_split(&sm.mass[bin], m);
 }
 
 __device__ __forceinline__ bool elig(uint32_t k, int t, uint32_t k0, int i0) {
@@ -698,8 +718,19 @@ __device__ Cut block_select(FiltSmem& sm, const float* x, int V, float lmax, flo
 // (order key, index) of the kept set and the kept set's sum of exp2((l - max) c).
 // Thread 0 writes *out.
 __device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, float c, int top_k,
-                           float top_p, FilterParam* out) {
+                           float top_p, FilterParam* out, bool l2_prefetch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the passes below read the row four or five times: bring it into L2 in one request
+    // per 64 KB while the first pass starts (rows in device memory only)
+    if (l2_prefetch && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const int64_t bytes = ((int64_t)V * 4) & ~int64_t(15);
+        for (int64_t o = (int64_t)tid * 65536; o < bytes; o += (int64_t)kFiltThreads * 65536) {
+            const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(
+                             reinterpret_cast<const char*>(x) + o), "r"(n)
+                         : "memory");
+        }
+    }
     float mx = -INFINITY;
     int bad = 0;
     row_for_each(x, V, [&](int, float l) {
@@ -726,25 +757,81 @@ __device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, flo
     auto fm = [&](unsigned long long e) { return fixed_mass(key_float((uint32_t)(e >> 32)), lmax, c); };
     if (do_k || do_p) {
         // Fast path: a histogram over distance bins (fine where the probability mass is),
-        // then an exact sort of the one bin the cut falls in.  The radix select takes over
-        // when that bin is the far tail or holds more than kCand elements.
-        for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
-        __syncthreads();
-        row_for_each(x, V, [&](int, float l) {
-            hist_add(sm, dist_bin(l, lmax, c), do_p ? fixed_mass(l, lmax, c) : 0ull);
-        });
-        __syncthreads();
+        // then an exact sort of the elements the cut falls among.  The radix select takes
+        // over when those are in the far tail or more than kCand of them.
+        // The histogram first covers only the bins within 4 log2 units of the maximum; it
+        // is rebuilt over every bin unless those already hold the cut (top_k elements, or
+        // without top-k the top-p mass), so the bins it feeds the scans are always exact.
+        unsigned long long total_all = 0ull;      // exact mass of the row (top-p alone)
+        for (int limit = kNearBins;; limit = kFiltBins) {
+            for (int i = tid; i < kFiltBins; i += kFiltThreads) { sm.cnt[i] = 0u; sm.mass[i] = 0ull; }
+            if (tid == 0) { sm.tot = 0ull; sm.near_cnt = 0u; sm.near_mass = 0ull; }
+            __syncthreads();
+            unsigned long long tm = 0ull;
+            const bool need_total = do_p && !do_k;
+            if (need_total) {
+                row_for_each(x, V, [&](int, float l) {
+                    const int bin = dist_bin(l, lmax, c);
+                    const unsigned long long m = fixed_mass(l, lmax, c);
+                    tm += m;
+                    if (bin < limit) hist_add(sm, bin, m);
+                });
+            } else {
+                row_for_each(x, V, [&](int, float l) {
+                    const int bin = dist_bin(l, lmax, c);
+                    if (bin < limit) hist_add(sm, bin, do_p ? fixed_mass(l, lmax, c) : 0ull);
+                });
+            }
+            if (need_total) add_u64_split(&sm.tot, tm);
+            __syncthreads();
+            total_all = sm.tot;
+            if (limit == kFiltBins) break;
+            unsigned int nc = 0u;
+            unsigned long long nm = 0ull;
+            for (int i = tid; i < limit; i += kFiltThreads) { nc += sm.cnt[i]; nm += sm.mass[i]; }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                nc += __shfl_xor_sync(0xffffffffu, nc, o);
+                nm += __shfl_xor_sync(0xffffffffu, nm, o);
+            }
+            if (lane == 0) {
+                atomicAdd(&sm.near_cnt, nc);
+                add_u64_split(&sm.near_mass, nm);
+            }
+            __syncthreads();
+            bool enough;
+            if (do_k) {
+                enough = sm.near_cnt >= (unsigned int)top_k;
+            } else {
+                unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total_all);
+                tgt = tgt < 1ull ? 1ull : (tgt > total_all ? total_all : tgt);
+                enough = sm.near_mass >= tgt;
+            }
+            __syncthreads();
+            if (enough) break;
+        }
         bool hist = true;                 // the histogram is still intact
-        int bk = -1, nk = 0;              // top-k cut: its bin, and how many of its sorted elements stay
-        unsigned long long mk = 0ull;     // mass of the bins before bk
+        int bk = -1, nk = 0;              // top-k cut: its bin, and how many sorted elements stay
+        unsigned long long mk = 0ull;     // mass of what precedes sm.sk[0]
         unsigned long long total = 0ull;  // mass of what top-k keeps
         if (do_k) {
             scan_bins<false, false>(sm, kFiltBins, (unsigned long long)top_k);
             const int bin = sm.found_bin;
             const unsigned int cb = sm.found_cnt;
             mk = sm.found_mass;
-            if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
-                gather_sort(sm, x, V, bin, lmax, c);
+            if (bin < kFiltBins - 1 && cb + sm.cnt[bin] <= (unsigned int)kCand) {
+                // every element up to the cut bin fits: sort them all; the first top_k are
+                // the top-k set, and the top-p cut (if any) is among them
+                gather_sort(sm, x, V, bin, lmax, c, true);
+                nk = top_k;
+                mk = 0ull;
+                const unsigned long long e = sm.sk[nk - 1];
+                key = (uint32_t)(e >> 32);
+                idx = (int)(~(uint32_t)e);
+                for (int j = 0; j < nk; ++j) total += fm(sm.sk[j]);
+                bk = bin;
+            } else if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
+                gather_sort(sm, x, V, bin, lmax, c, false);
                 nk = top_k - (int)cb;
                 const unsigned long long e = sm.sk[nk - 1];
                 key = (uint32_t)(e >> 32);
@@ -762,13 +849,12 @@ __device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, flo
             }
         }
         if (do_p) {
-            if (!do_k)
-                for (int i = 0; i < kFiltBins; ++i) total += sm.mass[i];
+            if (!do_k) total = total_all;
             unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
             tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
             bool done = false;
             if (hist && bk >= 0 && tgt > mk) {
-                // the cut lies among the elements of bk that top-k keeps (already sorted)
+                // the cut lies among the sorted elements that top-k keeps
                 unsigned long long acc = mk;
                 int j = 0;
                 for (; j < nk - 1; ++j) {
@@ -788,7 +874,7 @@ __device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, flo
                 const int bin = sm.found_bin;
                 const unsigned long long mb = sm.found_mass;
                 if (bin < kFiltBins - 1 && sm.cnt[bin] <= (unsigned int)kCand) {
-                    gather_sort(sm, x, V, bin, lmax, c);
+                    gather_sort(sm, x, V, bin, lmax, c, false);
                     const int n = min(sm.ncand, kCand);
                     unsigned long long acc = mb;
                     int j = 0;
@@ -827,7 +913,7 @@ __device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, flo
 
 // ---------------------------------------------------------------------------
 template <int CS, int NT, bool D2T, bool FILT>
-__global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArgs a) {
     using C = Cluster<CS, NT>;
     __shared__ VerifySmem<NT> sm;
     FiltSmem* fsm = nullptr;                 // the filtered walk's row-filter scratch
@@ -916,10 +1002,10 @@ __global__ void __launch_bounds__(NT, 4) verify_walk_kernel(VerifyArgs a) {
                 // barrier every CTA reads both filters back past L1.
                 FilterParam* fq_slot = a.fq + (int64_t)b * n + v;
                 FilterParam* fp_slot = prow ? a.fp + (int64_t)b * a.R + sm.row[v] : nullptr;
-                if (rank == 0) filter_row(*fsm, qrow, V, c, a.top_k, a.top_p, fq_slot);
+                if (rank == 0) filter_row(*fsm, qrow, V, c, a.top_k, a.top_p, fq_slot, a.target_in_device);
                 if (prow && rank == (CS > 1 ? 1 : 0)) {
                     if constexpr (CS == 1) __syncthreads();
-                    filter_row(*fsm, prow, V, c, a.top_k, a.top_p, fp_slot);
+                    filter_row(*fsm, prow, V, c, a.top_k, a.top_p, fp_slot, true);
                 }
                 __threadfence();
                 C::sync();
@@ -1322,7 +1408,7 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
     const float c = temperature > 0.f ? kLog2e / temperature : 0.f;
     VerifyArgs a{target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, max_depth,
                  temperature, c, seed, accept_len, path, emit, row_stats, dev_status, Vd, t2d,
-                 nullptr, nullptr, 0, 0.f};
+                 nullptr, nullptr, 0, 0.f, false};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool filt = temperature > 0.f && ((top_k > 0 && top_k < V) || (top_p > 0.f && top_p < 1.f));
     cudaError_t e;
@@ -1338,6 +1424,11 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
         a.fp = fp;
         a.top_k = top_k;
         a.top_p = top_p;
+        cudaPointerAttributes pa{};
+        const cudaError_t qe = cudaPointerGetAttributes(&pa, target_logits);
+        if (qe != cudaSuccess) cudaGetLastError();   // the query's own error, not a launch's
+        a.target_in_device = qe == cudaSuccess &&
+                             (pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged);
         e = launch_walk<false, true>(a, s);
     } else {
         e = t2d ? launch_walk<true, false>(a, s) : launch_walk<false, false>(a, s);

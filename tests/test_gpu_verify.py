@@ -338,3 +338,29 @@ def test_filtered_trees_match_oracle(V, top_k, top_p, quant):
     seen = ~np.isnan(r[1, :, :, 0])
     b_i, n_i = np.nonzero(seen)
     np.testing.assert_allclose(r[1, b_i, n_i, 1], Zd[b_i, rows[b_i, n_i]], rtol=1e-5)
+
+
+@pytest.mark.parametrize("B,quant", [(100, 0.0), (160, 0.5), (320, 0.0)])
+def test_filtered_walk_at_every_cluster_size(B, quant):
+    """The walk's cluster shrinks as B grows (8 CTAs per sequence up to B = 76, then 4,
+    2 and, above B = 304, one); the filtered walk filters each visited row on rank 0
+    (target) and rank 1 (draft), or both on rank 0 in a one-CTA cluster.  Small trees
+    (16 nodes, depth 4, 4 children per level) over V = 1003, top-k 12 and top-p 0.8,
+    against oracle.verify_accept_filtered."""
+    import dataclasses
+    E = _gpu()
+    cfg = dataclasses.replace(W.CONFIGS["sweep_70b"], n=16, depth=4, top_k=4)
+    tgt, drows, tree = _tree_case(cfg, B, seed=61, V=1003)
+    if quant:
+        tgt = (np.round(tgt / quant) * quant).astype(np.float32)
+        drows = (np.round(drows / quant) * quant).astype(np.float32)
+    ref = oracle.verify_accept_filtered(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, 1.0,
+                                        seed=31, top_k=12, top_p=0.8, draft_row=tree["draft_row"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc, path, emit = E.eagle_verify_accept(
+        _cuda(tgt), _cuda(drows), _cuda(tree["tokens"]), _cuda(tree["parent"]), cfg.depth, 1.0, 31,
+        draft_row=_cuda(tree["draft_row"]), dev_status=st, top_k=12, top_p=0.8)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and (ref["status"] == 0).all()
+    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy())
+    assert_tie_budget(dec, ties)

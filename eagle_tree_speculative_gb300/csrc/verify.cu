@@ -986,6 +986,7 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
     int buf = 0;
     int err = sm.err;
     int v = 0, acc_n = 0, y = -1;
+    unsigned long long ready_q = 0ull, ready_p = 0ull;   // nodes whose filters are written
     if (tid == 0) sm.path[0] = 0;
 
     while (!err) {
@@ -997,18 +998,45 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
             // filtered walk: this node's row filters; logits outside them read as -inf
             FilterParam fqv{}, fpv{};
             if constexpr (FILT) {
-                // Filtered only now that the walk has reached v: rank 0 filters q(v) and
-                // rank 1 (rank 0 again in a one-CTA cluster) p(v); after the cluster
-                // barrier every CTA reads both filters back past L1.
+                // Rows are filtered when the walk reaches their node, one row per CTA of
+                // the cluster: q(v) and p(v) first, then, on the CTAs that would idle, the
+                // rows of v's first children, which the walk visits next if it accepts
+                // one of them (that visit then needs no round).  Every CTA derives the
+                // same jobs and ready masks; after the barrier each reads back past L1.
                 FilterParam* fq_slot = a.fq + (int64_t)b * n + v;
                 FilterParam* fp_slot = prow ? a.fp + (int64_t)b * a.R + sm.row[v] : nullptr;
-                if (rank == 0) filter_row(*fsm, qrow, V, c, a.top_k, a.top_p, fq_slot, a.target_in_device);
-                if (prow && rank == (CS > 1 ? 1 : 0)) {
-                    if constexpr (CS == 1) __syncthreads();
-                    filter_row(*fsm, prow, V, c, a.top_k, a.top_p, fp_slot, true);
+                const bool need_q = !((ready_q >> v) & 1ull);
+                const bool need_p = prow && !((ready_p >> v) & 1ull);
+                if (need_q || need_p) {
+                    int jn[CS > 2 ? CS : 2];          // job: node, and whether its draft row
+                    bool jp[CS > 2 ? CS : 2];
+                    int nj = 0;
+                    if (need_q) { jn[nj] = v; jp[nj] = false; ++nj; }
+                    if (need_p) { jn[nj] = v; jp[nj] = true; ++nj; }
+                    for (int ch = v + 1; ch < n && nj < CS; ++ch) {
+                        if (sm.parent[ch] != v) continue;
+                        if (!((ready_q >> ch) & 1ull)) { jn[nj] = ch; jp[nj] = false; ++nj; }
+                        if (nj < CS && sm.nkids[ch] > 0 && !((ready_p >> ch) & 1ull)) {
+                            jn[nj] = ch; jp[nj] = true; ++nj;
+                        }
+                    }
+                    for (int j = rank; j < nj; j += CS) {
+                        if (j >= CS) __syncthreads();          // one-CTA clusters run several
+                        const int u = jn[j];
+                        if (jp[j])
+                            filter_row(*fsm, drf_b + (int64_t)sm.row[u] * Vdl, V, c, a.top_k, a.top_p,
+                                       a.fp + (int64_t)b * a.R + sm.row[u], true);
+                        else
+                            filter_row(*fsm, tgt_b + (int64_t)u * Vl, V, c, a.top_k, a.top_p,
+                                       a.fq + (int64_t)b * n + u, a.target_in_device);
+                    }
+                    for (int j = 0; j < nj; ++j) {
+                        if (jp[j]) ready_p |= 1ull << jn[j];
+                        else ready_q |= 1ull << jn[j];
+                    }
+                    __threadfence();
+                    C::sync();
                 }
-                __threadfence();
-                C::sync();
                 fqv = load_filter(fq_slot);
                 if (prow) fpv = load_filter(fp_slot);
             }

@@ -44,28 +44,27 @@
 
 #include "common.cuh"
 #include "tc_common.cuh"
+#include "attn_tc_common.cuh"
 
 namespace eagle {
 namespace attn_tc {
 
-constexpr int TBN = 128;                          // keys per tile
+using attn_common::TBN;
+using attn_common::NSBUF;
+using attn_common::KV_BOX_BYTES;
+using attn_common::K_BYTES;
+using attn_common::TMEM_COLS;
+using attn_common::S_COL0;
+using attn_common::O_COL0;
+using attn_common::Q_COL0;
+
 constexpr int KSTAGES = 3;                        // K ring
-constexpr int VSTAGES = 3;                        // V ring
+constexpr int VSTAGES = 3;                        // V ring (the MMA loop takes one depth)
+static_assert(KSTAGES == VSTAGES, "one ring depth");
 constexpr int kPrefetch = 3;                      // L2 prefetch distance beyond each ring
-constexpr int NSBUF = 2;                          // S and P buffers in TMEM
 constexpr int ROWS_PER_CTA = 128;                 // one M-tile
-constexpr int KV_BOX_BYTES = TBN * 64 * 2;        // 16 KB: 128 keys x 64 dims
-constexpr int K_BYTES = 2 * KV_BOX_BYTES;         // 32 KB (one K or V tile)
 constexpr int SMEM_BYTES = (KSTAGES + VSTAGES) * K_BYTES + 2048;
 constexpr int kThreads = 256;                     // warps 0-3 roles, 4-7 softmax
-constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: S[buf] at buf * 128 (P[buf], bf16 pairs, is written over the first 64
-// columns of S[buf]), O at 256, Q (bf16 pairs) at 384
-constexpr uint32_t S_COL0 = 0, O_COL0 = 256, Q_COL0 = 384;
-constexpr float kRescaleThreshold = 8.f;          // log2 units
-
-constexpr uint32_t kIdescQK = idesc_bf16(128, TBN, 0, 0);
-constexpr uint32_t kIdescPV = idesc_bf16(128, kHeadDim, 0, 1);
 
 struct Args {
     const uint16_t* q;
@@ -234,77 +233,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else if (warp == 1) {
         if (lane == 0 && T > 0) {
             // ---------------- MMA issuer ----------------
-            // Descriptors are built once; every operand below differs from its base
-            // only in the 14-bit start-address field (all addresses < 256 KB), so an
-            // MMA costs two adds.  Offsets are compile-time constants after unrolling.
-            const uint64_t dK0 = sw128_desc(s32(sK));
-            const uint64_t dV0 = sw128_desc_mn(s32(sV), KV_BOX_BYTES, 1024);
-            const uint32_t ocol = tmem + O_COL0;
-            auto issue_qk = [&](int j) {     // S[j % 2] = Q K_j^T (Q from TMEM); frees K stage j
-                const uint64_t dk = dK0 + (uint64_t)(((j % KSTAGES) * K_BYTES) >> 4);
-                const uint32_t scol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
-#pragma unroll
-                for (int k = 0; k < kHeadDim / 16; ++k)   // 16 dims = 8 packed TMEM columns
-                    umma_f16_ts(scol, tmem + Q_COL0 + k * 8,
-                                dk + (uint64_t)((((k >> 2) * KV_BOX_BYTES) + (k & 3) * 32) >> 4),
-                                kIdescQK, k > 0 ? 1u : 0u);
-                umma_commit(s32(&bars->s_full[j % NSBUF]));
-                umma_commit(s32(&bars->k_empty[j % KSTAGES]));
-            };
-            auto issue_pv = [&](int j) {     // O += P[j % 2] V_j; frees V stage j
-                const uint64_t dv = dV0 + (uint64_t)(((j % VSTAGES) * K_BYTES) >> 4);
-                const uint32_t pcol = tmem + S_COL0 + (uint32_t)((j % NSBUF) * TBN);
-                const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-                for (int k = 0; k < TBN / 16; ++k)   // 16 keys = 8 packed TMEM columns
-                    umma_f16_ts(ocol, pcol + k * 8, dv + (uint64_t)((k * 16 * 128) >> 4), kIdescPV,
-                                k > 0 ? 1u : acc0);
-                umma_commit(s32(&bars->pv_done[j % NSBUF]));
-                umma_commit(s32(&bars->v_empty[j % VSTAGES]));
-            };
-            auto wait_on = [&](uint64_t* bar, uint32_t parity) {
-                if (!mbar_wait(s32(bar), parity, abort_flag)) return false;
-                tc_fence_after();
-                return true;
-            };
-            bool ok = wait_on(&bars->q_full, 0u);
-            for (int j = 0; ok && j < min(T, NSBUF); ++j) {
-                ok = wait_on(&bars->k_full[j % KSTAGES], ((uint32_t)j / KSTAGES) & 1u);
-                if (ok) issue_qk(j);
-            }
-            // Issue whichever is ready first: QK^T of tile js (its S buffer, which held
-            // P of tile js-2, consumed by that tile's PV; its K tile landed) or PV of
-            // tile jp (its P written, its V tile landed), so a late K tile never holds
-            // back a PV and its V stage, and a late P never holds back the next scores.  Each completion
-            // tested is the next one of its barrier, so one parity bit names it.
-            int js = min(T, NSBUF), jp = 0;
-            long long t_last = clock64();
-            uint32_t idle = 0;
-            while (ok && jp < T) {
-                bool progressed = false;
-                if (js < T &&
-                    mbar_try_wait(s32(&bars->pv_done[js % NSBUF]), ((uint32_t)(js - NSBUF) / NSBUF) & 1u) &&
-                    mbar_try_wait(s32(&bars->k_full[js % KSTAGES]), ((uint32_t)js / KSTAGES) & 1u)) {
-                    tc_fence_after();
-                    issue_qk(js++);
-                    progressed = true;
-                }
-                if (jp < js &&
-                    mbar_try_wait(s32(&bars->p_full[jp % NSBUF]), ((uint32_t)jp / NSBUF) & 1u) &&
-                    mbar_try_wait(s32(&bars->v_full[jp % VSTAGES]), ((uint32_t)jp / VSTAGES) & 1u)) {
-                    tc_fence_after();
-                    issue_pv(jp++);
-                    progressed = true;
-                }
-                if (progressed) {
-                    t_last = clock64();
-                } else if ((++idle & 63u) == 0u) {
-                    if (*abort_flag) ok = false;
-                    else if (clock64() - t_last > kTimeoutCycles) { *abort_flag = 1; ok = false; }
-                }
-            }
-            umma_commit(s32(&bars->drain));
-            mbar_wait(s32(&bars->drain), 0u, abort_flag, /*honour_abort=*/false);
+            attn_common::mma_issue_loop<KSTAGES>(bars, tmem, sK, sV, T, abort_flag);
         }
     } else if (warp >= 4) {
         // ---------------- softmax: one thread per query row ----------------
@@ -326,21 +255,7 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             tc_fence_after();
             const uint32_t s_addr = s_addr0 + (uint32_t)((j % NSBUF) * TBN);
             float x[TBN];
-            {
-                uint32_t u0[32], u1[32], u2[32], u3[32];
-                tmem_ld32_nowait(s_addr, u0);
-                tmem_ld32_nowait(s_addr + 32, u1);
-                tmem_ld32_nowait(s_addr + 64, u2);
-                tmem_ld32_nowait(s_addr + 96, u3);
-                asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = __uint_as_float(u0[c]);
-                    x[32 + c] = __uint_as_float(u1[c]);
-                    x[64 + c] = __uint_as_float(u2[c]);
-                    x[96 + c] = __uint_as_float(u3[c]);
-                }
-            }
+            attn_common::load_scores(s_addr, x);
             const int key0 = j == T - 1 ? last0 : kb + j * TBN;
             if (key0 + TBN > L || key0 + TBN > ke || !valid || key0 < last_fresh && j == T - 1) {
                 // visibility of the tile's keys as a 128-bit map: committed keys below L,
@@ -364,58 +279,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 for (int c = 0; c < TBN; ++c)
                     if (!((vis[c >> 6] >> (c & 63)) & 1ull)) x[c] = -INFINITY;
             }
-            // row max over the tile: eight independent chains, then a tree
-            float m8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = x[e];
-#pragma unroll
-            for (int c = 8; c < TBN; c += 8)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], x[c + e]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            mx *= sc;                              // scale > 0 commutes with max
-            float alpha = 1.f;
-            if (mx > mref + kRescaleThreshold || (mref == -INFINITY && mx > -INFINITY)) {
-                alpha = mref == -INFINITY ? 0.f : exp2f(mref - mx);
-                mref = mx;
-                l *= alpha;
+            if (!attn_common::softmax_tile(bars, x, sc, mref, l, s_addr, o_addr, j, lane, abort_flag)) {
+                ok = false;
+                break;
             }
-            // P of tile j goes over S of tile j, whose MMA was issued after the PV of
-            // tile j-2 had finished with that buffer.  PV of tile j-1 is awaited only
-            // before the output accumulator is rescaled.
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                got = mbar_wait(s32(&bars->pv_done[(j - 1) % NSBUF]), ((uint32_t)(j - 1) / NSBUF) & 1u,
-                                abort_flag);
-                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < kHeadDim / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(o_addr + cc * 32, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(o_addr + cc * 32, o);
-                }
-            }
-            const float base = mref == -INFINITY ? 0.f : mref;
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};      // four partial sums, no long FADD chain
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(x[64 * h + 2 * e], sc, -base));
-                    const float p1 = ex2_approx(fmaf(x[64 * h + 2 * e + 1], sc, -base));
-                    ps[e & 3] += p0 + p1;
-                    pk[e] = pack2(p0, p1);
-                }
-                tmem_st32(s_addr + (uint32_t)(32 * h), pk);   // P, bf16 pairs, over S
-            }
-            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s32(&bars->p_full[j % NSBUF]));
         }
         bool got = ok && T > 0 ? mbar_wait(s32(&bars->pv_done[(T - 1) % NSBUF]),
                                            ((uint32_t)(T - 1) / NSBUF) & 1u, abort_flag)

@@ -64,3 +64,55 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(_lib.LibraryMissing):
         _lib.load()
+
+
+def test_ttt_attention_argument_checks_return_before_any_device_work(lib_path):
+    """eagle_ttt_attn validates on the host and returns before touching the device:
+    bad rounds and sizes give their status codes, an empty batch is a no-op (NULL
+    pointers allowed), and misaligned pointers are refused.  No GPU is needed."""
+    L = ctypes.CDLL(lib_path)
+    f = L.eagle_ttt_attn
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_void_p,
+                                                                ctypes.c_void_p]
+    OK, INVALID, SHAPE = 0, 1, 2
+    p = 4096                                      # a 16-byte aligned, never dereferenced address
+    # B, S, Hq, Hkv, head_dim, R1, r, scale
+    assert f(None, None, None, None, 0, 8, 4, 2, 128, 3, 1, 0.1, None, None) == OK
+    assert f(p, p, p, p, 1, 8, 4, 2, 128, 3, 3, 0.1, None, None) == INVALID     # r >= R1
+    assert f(p, p, p, p, 1, 8, 4, 2, 128, 3, -1, 0.1, None, None) == INVALID    # r < 0
+    assert f(p, p, p, p, 1, 0, 4, 2, 128, 3, 1, 0.1, None, None) == INVALID     # S < 1
+    assert f(p, p, p, p, 1, 8, 4, 2, 128, 3, 1, 0.0, None, None) == INVALID     # scale
+    assert f(p, p, p, p, 1, 8, 4, 2, 64, 3, 1, 0.1, None, None) == SHAPE        # head_dim
+    assert f(p, p, p, p, 1, 8, 4, 3, 128, 3, 1, 0.1, None, None) == SHAPE       # Hq % Hkv
+    assert f(p, p, p, p, 1, 8, 4, 2, 128, 17, 1, 0.1, None, None) == SHAPE      # R1 > 16
+    assert f(None, p, p, p, 1, 8, 4, 2, 128, 3, 1, 0.1, None, None) == INVALID  # NULL q
+    assert f(p + 4, p, p, p, 1, 8, 4, 2, 128, 3, 1, 0.1, None, None) == INVALID  # misaligned
+
+
+def test_filtered_verify_rejects_bad_filter_parameters(lib_path):
+    """top_k < 0 and a negative or non-finite top_p are refused on the host; with valid
+    parameters an empty batch returns OK without device work (the positive control).
+    Arguments are placed by the parameter names the header declares."""
+    import re
+    from eagle_tree_speculative_gb300 import _lib
+    L = ctypes.CDLL(lib_path)
+    f = L.eagle_verify_accept_filtered
+    f.restype = ctypes.c_int
+    f.argtypes = _lib.SIGNATURES["eagle_verify_accept_filtered"][1]
+    text = open(HEADER).read()
+    decl = re.search(r"eagle_status eagle_verify_accept_filtered\((.*?)\);", text, re.S).group(1)
+    params = [x.strip().split()[-1].lstrip("*") for x in decl.replace("\n", " ").split(",")]
+    assert len(params) == len(f.argtypes)
+    p = 4096                                      # a 16-byte aligned, never dereferenced address
+
+    def run(top_k, top_p):
+        vals = {"B": 0, "n": 2, "V": 8, "R": 2, "max_depth": 1, "temperature": 1.0, "seed": 0,
+                "top_k": top_k, "top_p": top_p, "ws_bytes": 0}
+        return f(*[vals.get(nm, p) for nm in params])
+
+    assert run(5, 0.5) == 0
+    assert run(-1, 0.5) == 1
+    assert run(5, -0.1) == 1
+    assert run(5, float("inf")) == 1
+    assert run(5, float("nan")) == 1

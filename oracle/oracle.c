@@ -477,8 +477,9 @@ int orc_tree_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
 
 /* ------------------------------------------------------------------------
  * Training-time-test attention (TTT page, section
- * "训练时的 attention mask 为什么要特殊处理").  Round 0 runs on the original tokens with the ordinary causal mask.
- * Round r >= 1 feeds back, at every position i, the token the previous round
+ * "训练时的 attention mask 为什么要特殊处理").  Round 0 runs on the original
+ * tokens with the ordinary causal mask.  Round r >= 1 feeds back, at every
+ * position i, the token the previous round
  * predicted there; a simulated token may see only its own ancestors: the
  * original tokens up to its position (0..i) and the tokens of rounds 1..r at
  * the same position (its own chain, itself included), never another

@@ -441,10 +441,12 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
 
 // ---------------------------------------------------------------------------
 // Row filters for the filtered walk (top-k, then top-p over what top-k kept): one CTA
-// per row, computed when the walk reaches the row's node.  The cut is found by a radix select over the rows' order keys (11-bit
-// digits, most significant first), with per-bin counts and fixed-point masses
-// (2^((l - max) c) scaled by 2^40, integer sums, so the decisions do not depend on
-// the order of the atomics); ties at the cut go to the lower token.
+// per row, computed when the walk reaches the row's node (or its parent).  The cut is
+// usually found from a histogram over distance bins and an exact sort of the elements
+// up to the cut; otherwise by a radix select over the rows' order keys (11-bit digits,
+// most significant first).  Both keep per-bin counts and fixed-point masses
+// (2^((l - max) c) scaled by 2^40, integer sums, so the decisions do not depend on the
+// order of the atomics); ties at the cut go to the lower token.
 // ---------------------------------------------------------------------------
 constexpr int kFiltThreads = 256;
 constexpr int kFiltBins = 2048;

@@ -270,6 +270,23 @@ def eagle2_expand(level, final, logits, top_k, depth, n_out, tree_state, hidden=
         _stream(stream)))
 
 
+def eagle2_tree_candidates(tree_state, B, top_k, depth, stream=None):
+    """Every candidate of a tree state as CUDA tensors [B, C]: dict(value, conf (f32),
+    token, parent, depth, draft_row (int32)), C = 1 + top_k + (depth - 1) * top_k^2."""
+    _dev(tree_state, "tree_state")
+    C = 1 + top_k + (depth - 1) * top_k * top_k
+    dev = tree_state.device
+    out = {"value": torch.empty(B, C, device=dev), "conf": torch.empty(B, C, device=dev)}
+    for name in ("token", "parent", "depth", "draft_row"):
+        out[name] = torch.empty(B, C, dtype=torch.int32, device=dev)
+    nbytes = tree_state.numel() * tree_state.element_size()
+    _check("eagle2_tree_candidates", lib().eagle2_tree_candidates(
+        _ptr(tree_state), nbytes, B, top_k, depth, _ptr(out["value"]), _ptr(out["conf"]),
+        _ptr(out["token"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["draft_row"]),
+        _stream(stream)))
+    return out
+
+
 def eagle_static_tree(choices):
     """Plan a static draft tree from its choices (rank paths from the root) on the host.
     Returns dict(parent, rank, depth, draft_row) of int32 numpy arrays [n]."""

@@ -37,6 +37,7 @@ SIGNATURES = {
                            _P, _P, _P]),
     "eagle2_expand_d2t": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _SZ, _P, _P,
                                _P, _P, _P, _P, _P]),
+    "eagle2_tree_candidates": (_I, [_P, _SZ, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "eagle_static_tree": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "eagle_static_tree_level": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "eagle2_expand_static_state": (_I, [_I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P,

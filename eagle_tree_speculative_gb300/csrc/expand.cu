@@ -47,13 +47,15 @@ constexpr int kSegMax = 4;        // vocabulary segments per draft row
 
 // Per-sequence tree state, 32-bit words:
 //   [0..3] reserved
-//   value[C] f32, parent[C], token[C], depth[C], row[C], frontier[kKMax],
+//   value[C] f32, parent[C], token[C], depth[C], row[C], conf[C] f32 (the draft
+//   confidence c of each candidate; V of a candidate = V of its parent * c),
+//   frontier[kKMax],
 //   per (frontier row s < k, segment g < kSegMax), at index s * kSegMax + g:
 //   seg_stat[3] (max f32, sum f32, non-finite flag), seg_val[k] f32, seg_tok[k]
 struct StateView {
     __host__ __device__ static int cand_count(int k, int D) { return 1 + k + (D - 1) * k * k; }
     __host__ __device__ static int64_t words(int k, int D) {
-        return 4 + 5LL * cand_count(k, D) + kKMax + (int64_t)k * kSegMax * (3 + 2LL * k);
+        return 4 + 6LL * cand_count(k, D) + kKMax + (int64_t)k * kSegMax * (3 + 2LL * k);
     }
 };
 
@@ -64,6 +66,7 @@ struct SeqState {
     int* token;
     int* depth;
     int* row;
+    float* conf;
     int* frontier;
     int* seg_stat;    // [k * kSegMax][3]
     float* seg_val;   // [k * kSegMax][k]
@@ -80,7 +83,8 @@ __device__ __forceinline__ SeqState seq_state(void* base, int b, int k, int D) {
     s.token = p + 4 + 2 * C;
     s.depth = p + 4 + 3 * C;
     s.row = p + 4 + 4 * C;
-    s.frontier = p + 4 + 5 * C;
+    s.conf = reinterpret_cast<float*>(p + 4 + 5 * C);
+    s.frontier = p + 4 + 6 * C;
     s.seg_stat = s.frontier + kKMax;
     s.seg_val = reinterpret_cast<float*>(s.seg_stat + 3 * k * kSegMax);
     s.seg_tok = s.seg_stat + 3 * k * kSegMax + k * k * kSegMax;
@@ -558,6 +562,7 @@ select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t
         st.token[0] = -1;
         st.depth[0] = 0;
         st.row[0] = 0;
+        st.conf[0] = 1.0f;
         st.frontier[0] = 0;
     }
     __syncthreads();
@@ -566,8 +571,10 @@ select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t
         const int s = e / k, j = e % k;
         const int id = level == 1 ? 1 + j : 1 + k + (level - 2) * k * k + s * k + j;
         const int par = st.frontier[s];
-        const float val = __fmul_rn(st.value[par], s_conf[s * kKMax + j]);
+        const float c = s_conf[s * kKMax + j];
+        const float val = __fmul_rn(st.value[par], c);
         st.value[id] = val;
+        st.conf[id] = c;
         st.parent[id] = par;
         const int tk = s_tok[s * kKMax + j];            // id in the logits' vocabulary
         st.token[id] = d2t ? tk + d2t[tk] : tk;         // draft id -> target id
@@ -668,6 +675,25 @@ rerank_kernel(int k, int D, int level, int n_out, const void* state, int32_t* ou
     }
 }
 
+// ---------------------------------------------------------------------------
+// Copy of every candidate's fields out of the tree state, [B, C] per field.
+__global__ void tree_candidates_kernel(const void* state, int k, int D, float* value, float* conf,
+                                       int32_t* token, int32_t* parent, int32_t* depth,
+                                       int32_t* row) {
+    const int b = blockIdx.y;
+    const int C = StateView::cand_count(k, D);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= C) return;
+    SeqState st = seq_state(const_cast<void*>(state), b, k, D);
+    const int64_t o = (int64_t)b * C + i;
+    if (value) value[o] = st.value[i];
+    if (conf) conf[o] = st.conf[i];
+    if (token) token[o] = st.token[i];
+    if (parent) parent[o] = st.parent[i];
+    if (depth) depth[o] = st.depth[i];
+    if (row) row[o] = st.row[i];
+}
+
 }  // namespace
 }  // namespace eagle
 
@@ -686,19 +712,16 @@ extern "C" size_t eagle2_expand_scratch_size(int B, int V, int top_k) {
 
 namespace eagle {
 namespace {
-eagle_status expand_common(int level, int final, const void* hidden, const void* lm_head_w,
-                           float* logits, int B, int H, int V, int top_k, int depth, int n_out,
-                           void* tree_state, size_t state_bytes, float* partials,
-                           size_t partials_bytes, const int32_t* d2t, int32_t* out_tokens,
-                           int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
-                           int32_t* dev_status, eagle_stream_t stream) {
-    if (B < 0 || V < 1 || top_k < 1 || depth < 1 || level < 1 || level > depth || !logits ||
-        !tree_state)
+// Host checks of one expansion level that do not involve the tree state or the
+// partials (shared by the scratch and the fixed-array entry points).
+eagle_status expand_validate(int level, int final, const void* hidden, const void* lm_head_w,
+                             const float* logits, int B, int H, int V, int top_k, int depth,
+                             int n_out, const int32_t* out_tokens, const int32_t* out_parent,
+                             const int32_t* out_draft_row) {
+    if (B < 0 || V < 1 || top_k < 1 || depth < 1 || level < 1 || level > depth || !logits)
         return EAGLE_ERR_INVALID_ARG;
     if (top_k > kKMax || depth > kDepthMax || top_k > V) return EAGLE_ERR_SHAPE;
-    if (state_bytes < eagle2_tree_state_size(B, top_k, depth)) return EAGLE_ERR_CAPACITY;
-    const int C = StateView::cand_count(top_k, depth);
-    if (C > 4096) return EAGLE_ERR_SHAPE;
+    if (StateView::cand_count(top_k, depth) > 4096) return EAGLE_ERR_SHAPE;
     if (final) {
         if (!out_tokens || !out_parent || !out_draft_row) return EAGLE_ERR_INVALID_ARG;
         if (n_out < 2 || n_out > kMaxNodes) return EAGLE_ERR_SHAPE;
@@ -706,6 +729,21 @@ eagle_status expand_common(int level, int final, const void* hidden, const void*
         if (n_out > have) return EAGLE_ERR_SHAPE;
     }
     if (hidden && (!lm_head_w || H < 1)) return EAGLE_ERR_INVALID_ARG;
+    return EAGLE_OK;
+}
+
+eagle_status expand_common(int level, int final, const void* hidden, const void* lm_head_w,
+                           float* logits, int B, int H, int V, int top_k, int depth, int n_out,
+                           void* tree_state, size_t state_bytes, float* partials,
+                           size_t partials_bytes, const int32_t* d2t, int32_t* out_tokens,
+                           int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
+                           int32_t* dev_status, eagle_stream_t stream) {
+    if (!tree_state) return EAGLE_ERR_INVALID_ARG;
+    const eagle_status vs = expand_validate(level, final, hidden, lm_head_w, logits, B, H, V,
+                                            top_k, depth, n_out, out_tokens, out_parent,
+                                            out_draft_row);
+    if (vs != EAGLE_OK) return vs;
+    if (state_bytes < eagle2_tree_state_size(B, top_k, depth)) return EAGLE_ERR_CAPACITY;
     // fused top-k: every 256-column tile of a row was (or is now) reduced by the
     // GEMM's epilogue to its statistics and top-k; only those partials are merged
     const bool fused = partials != nullptr;
@@ -783,6 +821,23 @@ extern "C" eagle_status eagle2_expand_d2t(int level, int final, const void* hidd
                          out_parent, out_draft_row, frontier_tokens, dev_status, stream);
 }
 
+extern "C" eagle_status eagle2_tree_candidates(const void* tree_state, size_t state_bytes, int B,
+                                               int top_k, int depth, float* value, float* conf,
+                                               int32_t* token, int32_t* parent,
+                                               int32_t* cand_depth, int32_t* draft_row,
+                                               eagle_stream_t stream) {
+    if (B < 0 || top_k < 1 || depth < 1 || !tree_state) return EAGLE_ERR_INVALID_ARG;
+    if (top_k > kKMax || depth > kDepthMax) return EAGLE_ERR_SHAPE;
+    if (state_bytes < eagle2_tree_state_size(B, top_k, depth)) return EAGLE_ERR_CAPACITY;
+    if (B == 0) return EAGLE_OK;
+    const int C = StateView::cand_count(top_k, depth);
+    const dim3 grid((C + 255) / 256, B);
+    tree_candidates_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        tree_state, top_k, depth, value, conf, token, parent, cand_depth, draft_row);
+    EAGLE_CHECK_LAUNCH();
+    return EAGLE_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Allocation-free variant: the tree state lives in a file-scope device array.
 // ---------------------------------------------------------------------------
@@ -800,7 +855,8 @@ void* g_static_ptr[kMaxDevices] = {};
 
 // Device address of g_static_tree_state on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached.  The cache is not told about
+// cudaDeviceReset: after a reset of a device the cached address is stale.
 eagle_status static_state_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EAGLE_ERR_CUDA;
@@ -826,9 +882,13 @@ extern "C" eagle_status eagle2_expand_static_state(int level, int final, const v
                                                    int32_t* out_draft_row,
                                                    int32_t* frontier_tokens, int32_t* dev_status,
                                                    eagle_stream_t stream) {
-    const size_t need = eagle2_tree_state_size(B, top_k, depth);
-    if (need == 0 && B != 0) return EAGLE_ERR_SHAPE;
-    if (need > kStaticStateBytes) return EAGLE_ERR_CAPACITY;
+    // The same host checks as eagle2_expand, in the same order and before any device
+    // call, so both entry points report the same status for the same bad argument.
+    const eagle_status vs = expand_validate(level, final, hidden, lm_head_w, logits, B, H, V,
+                                            top_k, depth, n_out, out_tokens, out_parent,
+                                            out_draft_row);
+    if (vs != EAGLE_OK) return vs;
+    if (eagle2_tree_state_size(B, top_k, depth) > kStaticStateBytes) return EAGLE_ERR_CAPACITY;
     void* state = nullptr;
     const eagle_status st = static_state_address(&state);
     if (st != EAGLE_OK) return st;

@@ -368,20 +368,14 @@ __device__ __forceinline__ void row_stats_slice(const float* row, int lo, int hi
     }
 }
 
-// E = -ln u' for the race uniform u' = (2 (w >> 9) + 1) 2^-24.  Near u' = 1 (where
-// the race is usually won: E is small) it uses the exact complement
-// v = 1 - u' = (2^24 - 2 (w >> 9) - 1) 2^-24 and the Taylor series of -ln(1 - v),
-// v + v^2/2 + v^3/3 + v^4/4 (truncation below v^5/5 < 2^-30 relative for
-// v < 2^-6); elsewhere -log2(u') ln 2 with the hardware log2, whose error is
-// then small relative to |log2 u'| > 0.02.
+// E = -ln u' for the race uniform u' = (2 (w >> 9) + 1) 2^-24, as -log1p(-v) of the
+// exact complement v = 1 - u' = (2^24 - 2 (w >> 9) - 1) 2^-24 (a float: fewer than
+// 24 significant bits).  CUDA's log1pf is within 1 ulp over its whole range, so E
+// carries a relative error of at most 2^-23 at every u', including u' near 1 where
+// the race is usually won (E small).
 __device__ __forceinline__ float race_exponential(uint32_t w) {
-    const uint32_t a = 2u * (w >> 9) + 1u;                 // u' = a 2^-24
-    const uint32_t comp = (1u << 24) - a;                   // v = comp 2^-24, exact
-    if (comp < (1u << 18)) {
-        const float v = (float)comp * 0x1p-24f;
-        return v * (1.f + v * (0.5f + v * (1.f / 3.f + v * 0.25f)));
-    }
-    return -__log2f((float)a * 0x1p-24f) * 0.69314718055994531f;
+    const uint32_t comp = (1u << 24) - (2u * (w >> 9) + 1u);    // in [1, 2^24 - 1]
+    return -log1pf(-(float)comp * 0x1p-24f);
 }
 
 // Exponential race over the weights w_t (any positive scale): argmax_t w_t / E_t,
@@ -403,7 +397,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (rr[e] > 0.f) {
-                    const KeyIdx cand{__fdividef(rr[e], race_exponential(wx[e])), t + e};
+                    const KeyIdx cand{rr[e] / race_exponential(wx[e]), t + e};
                     if (ki_better(cand, best)) best = cand;
                 }
             }
@@ -431,7 +425,7 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
             if (rr > 0.f) {
                 const uint4 w = philox4x32_10(make_uint4((uint32_t)t >> 2, 0u, b, kTagRace), k0, k1);
                 const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-                const KeyIdx cand{__fdividef(rr, race_exponential(wx[t & 3])), t};
+                const KeyIdx cand{rr / race_exponential(wx[t & 3]), t};
                 if (ki_better(cand, best)) best = cand;
             }
         }

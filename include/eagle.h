@@ -295,6 +295,24 @@ eagle_status eagle2_expand(int level, int final, const void* hidden, const void*
                            int32_t* out_tokens, int32_t* out_parent, int32_t* out_draft_row,
                            int32_t* frontier_tokens, int32_t* dev_status, eagle_stream_t stream);
 
+/* eagle2_tree_candidates -- read back every candidate of a tree state.
+ * Same page and section as eagle2_expand: each candidate's draft confidence c
+ * (the temperature-1 softmax probability of its token in its parent's draft
+ * row) and path value V = V(parent) * c (float32 product, root V = 1) are the
+ * numbers the per-level and global selections rank.  For each sequence b and
+ * candidate id i (numbered as in eagle2_expand, C = 1 + top_k + (depth-1)
+ * top_k^2 ids, root 0) writes, at [b * C + i]:
+ *   value f32, conf f32, token int32 (target id), parent int32 (candidate id,
+ *   root -1), cand_depth int32 (level, root 0), draft_row int32 (row of the
+ *   draft logits the candidate was expanded from as a frontier node, else -1).
+ * Each output may be NULL.  Only ids generated by the levels run so far hold
+ * data.  tree_state / state_bytes as given to eagle2_expand.  Enqueued on
+ * stream after the expansion calls; nothing is modified. */
+eagle_status eagle2_tree_candidates(const void* tree_state, size_t state_bytes, int B, int top_k,
+                                    int depth, float* value, float* conf, int32_t* token,
+                                    int32_t* parent, int32_t* cand_depth, int32_t* draft_row,
+                                    eagle_stream_t stream);
+
 /* eagle2_expand_d2t -- eagle2_expand with a draft vocabulary: V is the draft
  * vocabulary size (the LM head's rows and the logits' width), the ranking is
  * over draft ids (ties to the lower draft id), and each chosen draft id d enters
@@ -357,10 +375,12 @@ eagle_status eagle_static_tree_level(int level, const float* logits, const int32
  * and partials/partials_bytes (none: the top-k reads the logits rows).
  *   - Returns EAGLE_ERR_CAPACITY, launching nothing, when
  *     eagle2_tree_state_size(B, top_k, depth) exceeds 4 MiB (for top_k = 10,
- *     depth = 8 that is 17,980 bytes per sequence: up to 233 sequences).
+ *     depth = 8 that is 20,824 bytes per sequence: up to 201 sequences).
+ *     Other invalid arguments return the status eagle2_expand gives them.
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream
- *     capture.
+ *     capture.  After cudaDeviceReset on a device the cached address is stale:
+ *     do not call this entry point on that device again in the same process.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents: the levels of one tree must run in order, and calls that overlap
  *     on the GPU (other streams, other host threads, another tree in between)

@@ -50,9 +50,9 @@ def test_host_only_queries(lib_path):
     assert E.lib().eagle_abi_version() == 100
     assert E.lib().eagle_status_str(2) == b"EAGLE_ERR_SHAPE"
     # workspace and tree-state sizes are pure host arithmetic
-    # header, 5 words per candidate (711 at k=10, D=8), frontier, and per (row, segment)
+    # header, 6 words per candidate (711 at k=10, D=8), frontier, and per (row, segment)
     # of up to 4 vocabulary segments: 3 statistics words + k values + k tokens
-    assert E.tree_state_size(64, 10, 8) == 64 * 4 * (4 + 5 * 711 + 16 + 10 * 4 * (3 + 2 * 10))
+    assert E.tree_state_size(64, 10, 8) == 64 * 4 * (4 + 6 * 711 + 16 + 10 * 4 * (3 + 2 * 10))
     assert E.tree_state_size(1, 17, 8) == 0                # top_k above the limit
     assert E.tree_attn_workspace_size(64, 60, 32, 8, 128, 4156) >= 0
     assert E.tree_attn_workspace_size(1, 60, 32, 8, 64, 4156) == 0    # head_dim != 128
@@ -116,3 +116,33 @@ def test_filtered_verify_rejects_bad_filter_parameters(lib_path):
     assert run(5, -0.1) == 1
     assert run(5, float("inf")) == 1
     assert run(5, float("nan")) == 1
+
+
+def test_static_state_entry_reports_the_same_argument_errors(lib_path):
+    """eagle2_expand_static_state checks its arguments on the host, like eagle2_expand and
+    before any device call, so the two entry points give the same status for the same bad
+    argument (no GPU is needed for that)."""
+    L = ctypes.CDLL(lib_path)
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    ex = L.eagle2_expand
+    ex.restype = I
+    ex.argtypes = [I, I, P, P, P, I, I, I, I, I, I, P, SZ, P, SZ, P, P, P, P, P, P]
+    st = L.eagle2_expand_static_state
+    st.restype = I
+    st.argtypes = [I, I, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]
+    p = 4096                                        # never dereferenced
+    cases = [  # level, final, B, V, top_k, depth, n_out
+        (1, 0, -1, 100, 10, 8, 60),                 # B < 0
+        (1, 0, 4, 100, 0, 8, 60),                   # top_k = 0
+        (1, 0, 4, 100, 17, 8, 60),                  # top_k above the limit
+        (1, 0, 4, 100, 10, 0, 60),                  # depth = 0
+        (1, 0, 4, 5, 10, 8, 60),                    # top_k > V
+        (9, 0, 4, 100, 10, 8, 60),                  # level beyond depth
+        (1, 1, 4, 100, 10, 8, 65),                  # n_out above 64
+        (2, 1, 4, 100, 10, 8, 200),                 # n_out above the candidates
+    ]
+    for lvl, fin, B, V, k, D, n in cases:
+        a = ex(lvl, fin, None, None, p, B, 0, V, k, D, n, p, 1 << 40, None, 0, p, p, p, None,
+               None, None)
+        b = st(lvl, fin, None, None, p, B, 0, V, k, D, n, p, p, p, None, None, None)
+        assert a == b and a != 0, (lvl, fin, B, V, k, D, n, a, b)

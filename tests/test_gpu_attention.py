@@ -78,11 +78,17 @@ def test_llama3_8b_shape_b64_full_size_sampled():
            sample=[0, 31, 63])
 
 
-@pytest.mark.parametrize("B,L", [(8, 512), (1, 8192)])
-def test_llama70b_shape_sweep_points(B, L):
+@pytest.mark.parametrize("B,L,sample", [
+    (1, 8192, None), (1, 16384, None), (1, 32768, None),          # every row; split KV
+    (8, 512, [0, 7]), (8, 16384, [0, 7]), (8, 32768, [5]),
+    (32, 2048, [0, 31]), (32, 16384, [17]),
+    (64, 1024, [0, 63]), (64, 4096, [0, 40, 63]), (64, 8192, [63])])
+def test_llama70b_shape_sweep_points(B, L, sample):
+    """The Llama-70B sweep's attention (64 q / 8 kv heads, 48-node trees) over its batch
+    sizes and KV lengths up to 32768; sampled sequences are checked row by row."""
     cfg = W.CONFIGS["sweep_70b"]
-    _check(B=B, n=cfg.n, Hq=cfg.Hq, Hkv=cfg.Hkv, kv_len=L, Lmax=L + cfg.n, seed=7 + B,
-           sample=[0, B - 1] if B > 1 else None)
+    _check(B=B, n=cfg.n, Hq=cfg.Hq, Hkv=cfg.Hkv, kv_len=L, Lmax=L + cfg.n, seed=7 + B + L,
+           sample=sample)
 
 
 def test_capacity_and_tree_errors_set_status_and_zero_output():

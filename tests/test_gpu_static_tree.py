@@ -89,7 +89,7 @@ def test_static_tree_verify_and_attention_match_oracle(T):
     torch.cuda.synchronize()
     assert int(status.item()) == 0 and (ref["status"] == 0).all()
     dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(),
-                              exact=(T == 0.0))
+                              exact=(T == 0.0), rows=(tgt, drows, drow, T))
     assert_tie_budget(dec, ties)
     assert ref["accept_len"].mean() > 0.3
     # tree attention with the static tree as the mask source (Vicuna-like heads, short cache)

@@ -51,7 +51,7 @@ def test_chain_1000_steps_match_oracle(T):
     ref = oracle.verify_accept(tgt, drf, tok, par, D, T, seed=0)
     acc, path, emit, st, rs = _run_gpu(tgt, drf, tok, par, D, T, 0, row_stats=True)
     assert st == 0 and (ref["status"] == 0).all()
-    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0), rows=(tgt, drf, None, T))
     assert_tie_budget(dec, ties)
     if T > 0:
         # softmax statistics of every visited row, 1e-5 relative
@@ -84,7 +84,8 @@ def test_eagle2_tree_b1_shape_matches_oracle(T):
     acc, path, emit, st = _run_gpu(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, T, 5,
                                    draft_row=tree["draft_row"])
     assert st == 0
-    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0),
+                              rows=(tgt, drows, tree["draft_row"], T))
     assert_tie_budget(dec, ties)
     assert ref["accept_len"].mean() > 0.5     # the synthetic draft is informative
 
@@ -101,8 +102,38 @@ def test_llama70b_sweep_trees_match_oracle(V, T, sigma):
     acc, path, emit, st = _run_gpu(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, T, 13,
                                    draft_row=tree["draft_row"])
     assert st == 0 and (ref["status"] == 0).all()
-    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0),
+                              rows=(tgt, drows, tree["draft_row"], T))
     assert_tie_budget(dec, ties)
+
+
+@pytest.fixture(scope="module",
+                params=[(V, sg) for V in (32000, 128256) for sg in (0.1, 0.5, 1.0)],
+                ids=lambda p: f"V{p[0]}-sigma{p[1]}")
+def sweep_b64(request):
+    """Llama-70B sweep trees (48 nodes, depth 6, top-10) for 64 sequences at one (V, sigma);
+    the first 32 sequences are the B = 32 case (inputs are keyed per sequence)."""
+    V, sigma = request.param
+    tgt, drows, tree = _tree_case(W.CONFIGS["sweep_70b"], 64, seed=71, V=V, sigma=sigma)
+    return V, sigma, tgt, drows, tree
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+@pytest.mark.parametrize("B", [32, 64])
+def test_llama70b_sweep_full_batches_match_oracle(sweep_b64, B, T):
+    """The sweep's verify at B = 32 and 64, V in {32000, 128256}, T in {0, 1}, draft noise
+    sigma in {0.1, 0.5, 1.0}: bit-exact at T = 0, near-ties only at T = 1."""
+    V, sigma, tgt, drows, tree = sweep_b64
+    cfg = W.CONFIGS["sweep_70b"]
+    t, d = tgt[:B], drows[:B]
+    tk, pa, dr = tree["tokens"][:B], tree["parent"][:B], tree["draft_row"][:B]
+    ref = oracle.verify_accept(t, d, tk, pa, cfg.depth, T, seed=19, draft_row=dr)
+    acc, path, emit, st = _run_gpu(t, d, tk, pa, cfg.depth, T, 19, draft_row=dr)
+    assert st == 0 and (ref["status"] == 0).all()
+    dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0), rows=(t, d, dr, T))
+    assert_tie_budget(dec, ties)
+    print(f"B={B} V={V} T={T} sigma={sigma}: mean accept_len {ref['accept_len'].mean():.3f}, "
+          f"decisions {dec}, near-ties {ties}")
 
 
 def test_eagle3_tree_b64_full_size_matches_oracle():
@@ -114,7 +145,7 @@ def test_eagle3_tree_b64_full_size_matches_oracle():
     acc, path, emit, st = _run_gpu(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, 1.0, 9,
                                    draft_row=tree["draft_row"])
     assert st == 0
-    dec, ties = compare_walks(ref, acc, path, emit)
+    dec, ties = compare_walks(ref, acc, path, emit, rows=(tgt, drows, tree["draft_row"], 1.0))
     assert_tie_budget(dec, ties)
 
 
@@ -130,7 +161,7 @@ def test_unaligned_vocab_and_tiny_vocab(V):
         ref = oracle.verify_accept(tgt, drf, tok, par, 4, T, seed=3)
         acc, path, emit, st = _run_gpu(tgt, drf, tok, par, 4, T, 3)
         assert st == 0
-        dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0))
+        dec, ties = compare_walks(ref, acc, path, emit, exact=(T == 0.0), rows=(tgt, drf, None, T))
         assert_tie_budget(dec, ties)
 
 
@@ -142,7 +173,7 @@ def test_root_only_tree_emits_one_bonus_token():
     ref = oracle.verify_accept(tgt, tgt, tok, par, 0, 1.0, seed=8)
     acc, path, emit, st = _run_gpu(tgt, tgt, tok, par, 0, 1.0, 8)
     assert st == 0 and (acc == 0).all() and (path[:, 0] == 0).all()
-    compare_walks(ref, acc, path, emit)
+    compare_walks(ref, acc, path, emit, rows=(tgt, tgt, None, 1.0))
 
 
 def test_device_errors_flag_and_skip_without_trapping():
@@ -261,7 +292,8 @@ def test_d2t_trees_match_oracle(V, Vd, T):
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and (ref["status"] == 0).all()
     dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(),
-                              exact=(T == 0.0))
+                              exact=(T == 0.0),
+                              rows=(tgt, oracle.d2t_scatter(drows, d2t, V), tree["draft_row"], T))
     assert_tie_budget(dec, ties)
     # a random quarter of the target ids leaves most of q's mass outside the draft
     # vocabulary, so acceptance is low; some drafts are still accepted
@@ -324,15 +356,16 @@ def test_filtered_trees_match_oracle(V, top_k, top_p, quant):
         draft_row=_cuda(tree["draft_row"]), row_stats=rs, dev_status=st, top_k=top_k, top_p=top_p)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and (ref["status"] == 0).all()
-    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy())
+    ft = oracle.filter_logits(tgt, 1.0, top_k, top_p)
+    fd = oracle.filter_logits(drows, 1.0, top_k, top_p)
+    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(),
+                              rows=(ft, fd, tree["draft_row"], 1.0))
     assert_tie_budget(dec, ties)
     r = rs.cpu().numpy()
-    ft = oracle.filter_logits(tgt, 1.0, top_k, top_p)
     m, Z, _, _ = oracle.softmax_rows(ft, 1.0)
     seen = ~np.isnan(r[0, :, :, 0])
     assert seen.sum() >= 8
     np.testing.assert_allclose(r[0][..., 1][seen], Z[seen], rtol=1e-5)
-    fd = oracle.filter_logits(drows, 1.0, top_k, top_p)
     _, Zd, _, _ = oracle.softmax_rows(fd, 1.0)
     rows = tree["draft_row"]
     seen = ~np.isnan(r[1, :, :, 0])
@@ -362,5 +395,8 @@ def test_filtered_walk_at_every_cluster_size(B, quant):
         draft_row=_cuda(tree["draft_row"]), dev_status=st, top_k=12, top_p=0.8)
     torch.cuda.synchronize()
     assert int(st.item()) == 0 and (ref["status"] == 0).all()
-    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy())
+    rows = (oracle.filter_logits(tgt, 1.0, 12, 0.8), oracle.filter_logits(drows, 1.0, 12, 0.8),
+            tree["draft_row"], 1.0)
+    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(),
+                              rows=rows)
     assert_tie_budget(dec, ties)

@@ -94,32 +94,54 @@ def test_leviathan_chisquare_v8_50000_steps():
     assert _chisq_pvalue(np.bincount(first, minlength=V), _softmax(_logits(p))) < 1e-6
 
 
-def test_leviathan_chisquare_chain_config_rows_binned():
-    """Rows shaped like the chain configuration (target ~ N(0, 2^2), draft = target +
-    N(0, 0.5^2)), V = 2000, 50,000 steps, tokens binned into 50 equal-q-mass bins."""
-    V, B, chunk = 2000, 50_000, 10_000
-    tgt_row, drf_row = W.chain_logits(1, 1, V, sigma=0.5, target_std=2.0, seed=3)
-    tgt_row, drf_row = tgt_row[0, 0], drf_row[0, 0]
-    q = _softmax(tgt_row)
+def _chain_row_first_tokens(tgt_row, drf_row, steps, seed, chunk=1000):
+    """First emitted token of `steps` independent one-draft chain steps on fixed rows
+    (target q, draft p; the draft token d ~ p).  The target row after the draft only
+    feeds the bonus token, never the first one, so it is a one-token row here."""
+    V = tgt_row.size
     p = _softmax(drf_row)
-    g = W.rng(3, 7)
+    g = W.rng(seed, 7)
+    after = np.full(V, NEG)
+    after[0] = 0.0
+    tgt = np.ascontiguousarray(np.broadcast_to(np.stack([tgt_row, after]), (chunk, 2, V)))
+    drf = np.broadcast_to(drf_row, (chunk, 2, V))
+    par = np.broadcast_to(W.chain_tree(2), (chunk, 2))
     firsts = []
-    for c in range(B // chunk):
+    for c in range(steps // chunk):
         tok = np.full((chunk, 2), -1, np.int32)
         tok[:, 1] = g.choice(V, size=chunk, p=p)
-        tgt = np.broadcast_to(tgt_row, (chunk, 2, V))
-        drf = np.broadcast_to(drf_row, (chunk, 2, V))
-        par = np.broadcast_to(W.chain_tree(2), (chunk, 2))
-        res = oracle.verify_accept(tgt, drf, tok, par, max_depth=1, T=1.0, seed=900 + c)
+        res = oracle.verify_accept(tgt, drf, tok, par, max_depth=1, T=1.0, seed=seed * 1000 + c)
         firsts.append(res["emit"][:, 0])
-    first = np.concatenate(firsts)
+    return np.concatenate(firsts)
+
+
+def _equal_mass_bins(q, nbins):
     order = np.argsort(q)
     cum = np.cumsum(q[order])
-    bin_of_rank = np.minimum((cum * 50).astype(int), 49)
-    bins = np.empty(V, int)
-    bins[order] = bin_of_rank
-    qbin = np.bincount(bins, weights=q, minlength=50)
-    assert _chisq_pvalue(np.bincount(bins[first], minlength=50), qbin) > 1e-3
+    bins = np.empty(q.size, int)
+    bins[order] = np.minimum((cum * nbins).astype(int), nbins - 1)
+    return bins, np.bincount(bins, weights=q, minlength=nbins)
+
+
+def test_leviathan_chisquare_chain_config_rows_binned():
+    """A chain-configuration row pair (V = 32000, target ~ N(0, 2^2), draft = target +
+    N(0, 0.5^2)): over 50,000 steps the first emitted token, binned into 50 bins of
+    equal q mass (df = 49), is distributed as q, for each of 3 seeds (p-value > 1e-3, at
+    most one of the three below 0.05); binned against p instead, the test rejects."""
+    V, steps = 32000, 50_000
+    tgt_row, drf_row = W.chain_logits(1, 1, V, sigma=0.5, target_std=2.0, seed=3)
+    tgt_row, drf_row = tgt_row[0, 0], drf_row[0, 0]
+    q, p = _softmax(tgt_row), _softmax(drf_row)
+    bins, qbin = _equal_mass_bins(q, 50)
+    pbin = np.bincount(bins, weights=p, minlength=50)
+    pvals = []
+    for seed in (1, 2, 3):
+        first = _chain_row_first_tokens(tgt_row, drf_row, steps, seed)
+        counts = np.bincount(bins[first], minlength=50)
+        pvals.append(_chisq_pvalue(counts, qbin))
+        assert _chisq_pvalue(counts, pbin) < 1e-6          # the test has power
+    assert min(pvals) > 1e-3, pvals
+    assert sum(pv < 0.05 for pv in pvals) <= 1, pvals
 
 
 def test_race_sampler_matches_normalised_weights():

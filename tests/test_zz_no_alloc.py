@@ -1,8 +1,11 @@
 """eagle2_expand_static_state: the tree state lives in the library's own device array.
 
+It serves callers that may not allocate device memory once they run: a serving loop
+that reserves its memory at start-up, or code behind another framework's allocator.
 Called through the C ABI (ctypes, raw device pointers) and compared bit for bit with
 eagle2_expand on caller-provided scratch, for two trees expanded one after the other,
-so the second tree runs on whatever the first left in the array.  This file sorts
+so the second tree runs on whatever the first left in the array; a full tree through
+it leaves the device's free memory and torch's allocation unchanged.  This file sorts
 last so that the array has also seen every earlier test's process state.
 """
 import ctypes
@@ -112,3 +115,36 @@ def test_static_state_rejects_trees_beyond_its_capacity():
     assert rc == EAGLE_ERR_CAPACITY
     B_ok = (4 << 20) // per_seq
     assert int(L.eagle2_tree_state_size(B_ok, k, D)) <= (4 << 20)
+
+
+def test_static_state_allocates_nothing():
+    """After one warm-up tree (which loads the kernels), a full tree through the
+    fixed-array entry point changes neither the device's free memory (cudaMemGetInfo)
+    nor torch's allocated bytes."""
+    cfg = W.CONFIGS["expand_b64"]
+    k, D, n = cfg.top_k, cfg.depth, cfg.n
+    lg = _logits(25, 64, 32000)
+    B = lg.shape[0]
+    E, L = _L()
+    dev = lg.device
+    tok = torch.empty((B, n), dtype=torch.int32, device=dev)
+    par, row = torch.empty_like(tok), torch.empty_like(tok)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def tree():
+        for lvl in range(1, D + 1):
+            rc = L.eagle2_expand_static_state(lvl, int(lvl == D), None, None, lg.data_ptr(), B, 0,
+                                              lg.shape[2], k, D, n, tok.data_ptr(), par.data_ptr(),
+                                              row.data_ptr(), None, st.data_ptr(), stream)
+            assert rc == 0
+        torch.cuda.synchronize()
+
+    tree()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    tree()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert free1 == free0, (free0, free1)
+    assert int(st.item()) == 0

@@ -51,41 +51,53 @@ def measured_peaks():
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons, each stamped on arrival;
+    stop(t0, t1) keeps the samples that arrived inside the timed region [t0, t1]."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.idx = gpu_index
+        self.interval = interval_ms
         self.proc = None
         self.lines = []
 
-    def start(self):
+    def start(self, wait_first_s: float = 3.0):
+        """Start sampling; return once the first sample has arrived (or after wait_first_s)."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
             self.proc = None
+            return
+        t_end = time.perf_counter() + wait_first_s
+        while not self.lines and time.perf_counter() < t_end:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(2 * self.interval / 1000.0)          # the sample that covers t1
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        slack = self.interval / 1000.0
+        inside = [ln for ts, ln in self.lines
+                  if t0 is None or (t0 <= ts <= t1 + slack)]
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in inside:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -99,7 +111,9 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "interval_ms": self.interval,
+                "window": "samples that arrived inside the timed region",
+                "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- our arm
@@ -237,6 +251,20 @@ def step_throughput(world, ms_per_step):
     return world * 1000.0 / ms_per_step
 
 
+def time_region_steps(fn, steps, torch):
+    """Total device time of `steps` calls of fn and each call's own time (ms): one event
+    before every step and one after the last, all on the launching stream."""
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        fn(i)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[-1]), per
+
+
 def time_region(fn, steps, torch):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -273,17 +301,18 @@ def run_ours(args, rank, world, dist):
     except Exception as exc:  # capture unsupported: time the eager calls instead
         graph = None
         print(f"graph capture failed ({exc}); timing eager launches", file=sys.stderr)
-    if dist:
-        dist.barrier()
     clocks = ClockSampler(local)
     clocks.start()
-    if graph is not None:
-        ms = time_region(lambda i: graph.replay(), args.steps, torch)
-    else:
-        ms = time_region(lambda i: st.run(i), args.steps, torch)
-    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    step_fn = (lambda i: graph.replay()) if graph is not None else (lambda i: st.run(i))
+    t0 = time.perf_counter()
+    ms, per_step = time_region_steps(step_fn, args.steps, torch)
+    t1 = time.perf_counter()
+    clk = clocks.stop(t0, t1)
     ms = reduce_over_ranks(ms, dist, dev, "max")
     ms_per_step = ms / args.steps
+    step_median = reduce_over_ranks(float(np.median(per_step)), dist, dev, "max")
     acc_graph = float(st.accept_len.sum().item() + st.B)   # the replayed step's accepted tokens
 
     # -------- eager timed region: per-launch GEMM times (CUDA events on the stream) --------
@@ -311,6 +340,8 @@ def run_ours(args, rank, world, dist):
     # -------- per-call breakdown (separate short timing) --------
     br = breakdown(st, torch)
     ttt = ttt_attn_figures(torch, dev, peaks)
+    other = {"chain_b1_b1000": chain_config(torch, dev),
+             "eagle2_b1_vicuna13b": eagle2_b1_config(torch, dev, peaks)}
 
     # -------- end to end through the public API with host buffers --------
     e2e = run_e2e(st, torch, max(5, min(args.steps, 20)), graph)
@@ -326,22 +357,18 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4),
-        "timing": "CUDA graph of one step replayed" if graph is not None else "eager launches",
+        "ms_per_step_median": round(step_median, 4),
+        "ms_per_step_p10_p90": [round(float(np.percentile(per_step, 10)), 4),
+                                round(float(np.percentile(per_step, 90)), 4)],
+        "timing": ("CUDA graph of one step replayed; value from the whole timed region, median "
+                   "from one event pair per step") if graph is not None else "eager launches",
         "eager_ms_per_step_wall": round(1e3 * t_eager / eager_steps, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16 GEMM/attention (fp32 accumulate), f32 logits",
         "data": "synthetic (seeded normals; random-init LM head; no datasets or trained weights)",
-        "config": {"workload": "EAGLE-3 tree verify step, B=64, Llama-3-8B shape: EAGLE-2 "
-                               "expansion 8 levels x top-10 (LM head 4096->128256), rerank to 60 "
-                               "nodes, tree attention 1 layer (32q/8kv heads, d=128, KV 4096), "
-                               "verify V=128256 T=1 sigma=0.3, KV compaction 32 layers",
-                   "B": CFG.B, "nodes": CFG.n, "depth": CFG.depth, "top_k": CFG.top_k,
-                   "vocab": CFG.V, "hidden": CFG.H, "kv_len": CFG.L, "attn_layers": 1,
-                   "compact_layers": CFG.n_layers, "temperature": 1.0,
-                   "l2": "inputs larger than L2 (LM head 1.05 GB, logits 2.3 GB, KV 1.1 GB/layer)",
-                   "parallelism": f"replicas x{world} (sequence-sharded, no collective)"},
+        "config": workload_config(world),
         "accepted_tokens_per_s": round(tok_all_ranks * 1000.0 / ms_per_step, 1),
         "mean_accept_len_plus_1": round(tok_all_ranks / (world * st.B), 4),
         "graph_step_accepted_tokens": acc_graph,
@@ -358,6 +385,8 @@ def run_ours(args, rank, world, dist):
                      "gemm_flops_per_step_all_levels": gemm_flops / eager_steps,
                      "timed": f"{eager_steps} eager steps, events around each launch"},
         "breakdown_ms": br,
+        "roofline_hbm": hbm_rooflines(br, peaks),
+        "other_configs": other,
         "ttt_attn": ttt,
         "e2e": e2e,
         "e2e_target_in_place": e2e_in_place,
@@ -415,6 +444,270 @@ def ttt_attn_figures(torch, dev, peaks, reps=20):
     return res
 
 
+def timed_ms(fn, torch, reps=20, warm=3):
+    """Median per-call device time (ms) of fn over reps calls, one event pair per call."""
+    for _ in range(warm):
+        fn()
+    _, per = time_region_steps(lambda i: fn(), reps, torch)
+    return float(np.median(per))
+
+
+def chain_config(torch, dev, reps=200):
+    """Chain verify (config 0): root + 5 drafts, V = 32000, target ~ N(0, 2^2), draft =
+    target + N(0, 0.5^2), drafts sampled from p (T = 1) or its argmax (T = 0); no
+    attention.  Latency of one B = 1 call, and throughput of 1000 independent steps as
+    one B = 1000 call."""
+    import eagle_tree_speculative_gb300 as E
+    c = W.CONFIGS["chain"]
+    n, V, D = c.n, c.V, c.depth
+    g = torch.Generator(device=dev).manual_seed(SEED + 31)
+    res = {"workload": "chain verify, 5 drafts, V=32000, sigma=0.5; B=1 latency and one B=1000 "
+                       "launch (1000 independent steps); no attention"}
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for B in (1, 1000):
+        tgt = torch.randn(B, n, V, device=dev, generator=g) * c.target_std
+        drf = tgt + torch.randn(B, n, V, device=dev, generator=g) * c.sigma
+        par = torch.arange(-1, n - 1, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+        for T in (1.0, 0.0):
+            tok = torch.full((B, n), -1, dtype=torch.int32, device=dev)
+            if T > 0:
+                pr = torch.softmax(drf[:, :n - 1] / T, -1).reshape(-1, V)
+                tok[:, 1:] = torch.multinomial(pr, 1, generator=g).view(B, n - 1).int()
+            else:
+                tok[:, 1:] = drf[:, :n - 1].argmax(-1).int()
+            acc = torch.empty(B, dtype=torch.int32, device=dev)
+            path = torch.empty(B, D + 1, dtype=torch.int32, device=dev)
+            emit = torch.empty_like(path)
+            fn = lambda: E.eagle_verify_accept(tgt, drf, tok, par, D, T, 5, accept_len=acc,  # noqa
+                                               path=path, emit=emit, dev_status=st)
+            ms = timed_ms(fn, torch, reps=reps if B == 1 else 50)
+            key = f"T{int(T)}"
+            if B == 1:
+                res[f"B1_{key}_us_per_step"] = round(ms * 1e3, 2)
+            else:
+                res[f"B1000_{key}_steps_per_s"] = round(1000.0 / (ms * 1e-3), 1)
+                res[f"B1000_{key}_ms_per_launch"] = round(ms, 4)
+                res[f"B1000_{key}_mean_accept_len_plus_1"] = round(float(acc.float().mean()) + 1, 4)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"chain device status {int(st.item())}")
+    return res
+
+
+def eagle2_b1_config(torch, dev, peaks, reps=100):
+    """EAGLE-2 tree at B = 1, Vicuna-13B shape (config 1): expansion of a 60-node depth-6
+    top-10 tree from given draft logits (V = 32000), tree attention of one layer (40 / 40
+    heads, d = 128, KV 2048: the split-KV path), verify at T = 0 and T = 1, and KV
+    compaction over 40 layers.  Latency of each call and of the whole step as one graph."""
+    import eagle_tree_speculative_gb300 as E
+    c = W.CONFIGS["eagle2_b1"]
+    B, n, D, k, V = 1, c.n, c.depth, c.top_k, c.V
+    layers = 40
+    g = torch.Generator(device=dev).manual_seed(SEED + 41)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    trow = torch.randn(B, c.R, V, device=dev, generator=g) * c.target_std
+    drows = trow + torch.randn(B, c.R, V, device=dev, generator=g) * c.sigma
+    state = torch.empty(E.tree_state_size(B, k, D), dtype=torch.uint8, device=dev)
+    tok = torch.empty(B, n, dtype=torch.int32, device=dev)
+    par, row = torch.empty_like(tok), torch.empty_like(tok)
+
+    def expand():
+        for lvl in range(1, D + 1):
+            E.eagle2_expand(lvl, lvl == D, drows, k, D, n, state, out_tokens=tok, out_parent=par,
+                            out_draft_row=row, dev_status=st)
+    expand()
+    torch.cuda.synchronize()
+    r = row.long()[0]
+    tgt = torch.where((r >= 0)[:, None], trow[0, r.clamp(min=0)],
+                      torch.randn(n, V, device=dev, generator=g) * c.target_std)[None].contiguous()
+    q = torch.randn(B, n, c.Hq, c.head_dim, device=dev, generator=g).to(torch.bfloat16)
+    kc = torch.randn(layers, B, c.Hkv, c.Lmax, c.head_dim, device=dev, generator=g,
+                     dtype=torch.bfloat16)
+    vc = torch.randn_like(kc)
+    kv0 = torch.full((B,), c.L, dtype=torch.int32, device=dev)
+    kv = kv0.clone()
+    out = torch.empty_like(q)
+    ws_n = E.tree_attn_workspace_size(B, n, c.Hq, c.Hkv, c.head_dim, c.Lmax)
+    ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty(B, D + 1, dtype=torch.int32, device=dev)
+    emit = torch.empty_like(path)
+    attn = lambda: E.eagle_tree_attn(q, kc[0], vc[0], kv0, par, out=out, workspace=ws,  # noqa
+                                     dev_status=st)
+    res = {"workload": "EAGLE-2 tree, B=1, Vicuna-13B shape: 60 nodes, depth 6, top-10, "
+                       "V=32000 (expansion from given logits), attention 40/40 heads d=128 "
+                       "KV 2048 (split KV), compaction 40 layers",
+           "split_kv_workspace_bytes": int(ws_n)}
+    res["expand_6_levels_us"] = round(timed_ms(expand, torch, reps) * 1e3, 2)
+    a = timed_ms(attn, torch, reps)
+    kv_bytes = 2 * B * c.Hkv * (c.L + n) * c.head_dim * 2
+    res["tree_attn_us"] = round(a * 1e3, 2)
+    res["tree_attn_GBps"] = round(kv_bytes / (a * 1e-3) / 1e9, 1)
+    res["tree_attn_frac_hbm"] = round(kv_bytes / (a * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+
+    def comp():
+        E.eagle_kv_compact(kc, vc, kv, path, acc, D, dev_status=st)
+        kv.copy_(kv0)
+    for T in (0.0, 1.0):
+        ver = lambda: E.eagle_verify_accept(tgt, drows, tok, par, D, T, 3, draft_row=row,  # noqa
+                                            accept_len=acc, path=path, emit=emit, dev_status=st)
+        v = timed_ms(ver, torch, reps)
+        res[f"verify_T{int(T)}_us"] = round(v * 1e3, 2)
+        res[f"accept_len_T{int(T)}"] = int(acc.item())
+
+        def step():
+            expand()
+            attn()
+            ver()
+            comp()
+        gr = torch.cuda.CUDAGraph()
+        step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gr, capture_error_mode="relaxed"):
+            step()
+        res[f"step_T{int(T)}_us_graph"] = round(timed_ms(gr.replay, torch, reps) * 1e3, 2)
+    res["kv_compact_40_layers_us"] = round(timed_ms(comp, torch, reps) * 1e3, 2)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"eagle2_b1 device status {int(st.item())}")
+    return res
+
+
+def sweep_70b(torch, dev, peaks, reps=20):
+    """The Llama-70B sweep (config 4): 64 q / 8 kv heads, d = 128, 48-node depth-6 top-10
+    trees.  Each call is timed alone (median of `reps`):
+      attention   one layer over B x L (B in 1/8/32/64, L in 512 .. 32768); its binding
+                  roof is the larger of bytes / HBM peak and FLOPs / bf16 peak (burst: the
+                  kernel is timed alone);
+      verify      B x V x T x sigma (V in 32000/128256, T in 0/1, sigma in 0.1/0.5/1.0),
+                  trees expanded on the GPU from synthetic draft rows (target = draft -
+                  noise on expanded nodes, fresh rows at leaves); reports the accepted
+                  length histogram, tau = mean(accept_len + 1), alpha1 = P(accept_len >= 1)
+                  and GB/s over the visited rows (each visited node's target and draft row
+                  once; T = 0 reads target rows only);
+      softmax     the eager statistics of every target row, per B x V;
+      compaction  80 layers (Llama-70B) per B.
+    The step grid adds attention(B, L) + verify(B, V, T, sigma) + compaction(B)."""
+    import eagle_tree_speculative_gb300 as E
+    c = W.CONFIGS["sweep_70b"]
+    ex = c.extra
+    n, D, k, Hq, Hkv, d = c.n, c.depth, c.top_k, c.Hq, c.Hkv, c.head_dim
+    R = c.R
+    layers = 80
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    g = torch.Generator(device=dev).manual_seed(SEED + 51)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {"attn": [], "verify": [], "softmax": [], "compact": [],
+           "peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "source": peaks["source"]}}
+    Bmax = max(ex["B"])
+
+    def tree_for(V, sigma):
+        trow = torch.randn(Bmax, R, V, device=dev, generator=g) * c.target_std
+        drows = trow + torch.randn(Bmax, R, V, device=dev, generator=g) * sigma
+        state = torch.empty(E.tree_state_size(Bmax, k, D), dtype=torch.uint8, device=dev)
+        tok = torch.empty(Bmax, n, dtype=torch.int32, device=dev)
+        par, row = torch.empty_like(tok), torch.empty_like(tok)
+        for lvl in range(1, D + 1):
+            E.eagle2_expand(lvl, lvl == D, drows, k, D, n, state, out_tokens=tok,
+                            out_parent=par, out_draft_row=row, dev_status=st)
+        rows = row.long()
+        tgt = torch.empty(Bmax, n, V, device=dev)
+        for b in range(Bmax):
+            r = rows[b]
+            tgt[b] = torch.where((r >= 0)[:, None], trow[b, r.clamp(min=0)],
+                                 torch.randn(n, V, device=dev, generator=g) * c.target_std)
+        del trow, state
+        return tgt, drows, tok, par, row
+
+    # ---- attention over B x L (trees of the V = 32000, sigma = 0.5 case) ----
+    _, _, _, par_a, _ = tree_for(32000, 0.5)
+    for B in ex["B"]:
+        parent = par_a[:B].contiguous()
+        for L in ex["L"]:
+            Lmax = L + n
+            q = torch.randn(B, n, Hq, d, device=dev, generator=g).to(torch.bfloat16)
+            kc = torch.randn(B, Hkv, Lmax, d, device=dev, generator=g, dtype=torch.bfloat16)
+            vc = torch.randn_like(kc)
+            kv = torch.full((B,), L, dtype=torch.int32, device=dev)
+            out = torch.empty_like(q)
+            wsn = E.tree_attn_workspace_size(B, n, Hq, Hkv, d, Lmax)
+            ws = torch.empty(max(wsn, 1), dtype=torch.uint8, device=dev)
+            ms = timed_ms(lambda: E.eagle_tree_attn(q, kc, vc, kv, parent, out=out, workspace=ws,
+                                                    dev_status=st), torch, reps)
+            nbytes = 2 * B * Hkv * Lmax * d * 2 + 2 * B * n * Hq * d * 2
+            flops = 4.0 * B * n * Hq * d * Lmax
+            t_h, t_t = nbytes / (hbm * 1e9), flops / (tc * 1e12)
+            res["attn"].append({"B": B, "L": L, "ms": round(ms, 4),
+                                "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                "TFLOPs": round(flops / (ms * 1e-3) / 1e12, 1),
+                                "bound": "hbm" if t_h >= t_t else "tensor",
+                                "frac": round(max(t_h, t_t) / (ms * 1e-3), 4),
+                                "split_kv": bool(wsn)})
+            del q, kc, vc, out, ws
+    torch.cuda.empty_cache()
+    # ---- verify and softmax statistics over B x V x T x sigma ----
+    for V in ex["V"]:
+        for sigma in ex["sigma"]:
+            tgt, drows, tok, par, row = tree_for(V, sigma)
+            for B in ex["B"]:
+                t_, d_, k_, p_, r_ = (x[:B].contiguous() for x in (tgt, drows, tok, par, row))
+                acc = torch.empty(B, dtype=torch.int32, device=dev)
+                path = torch.empty(B, D + 1, dtype=torch.int32, device=dev)
+                emit = torch.empty_like(path)
+                for T in (0.0, 1.0):
+                    ms = timed_ms(lambda: E.eagle_verify_accept(
+                        t_, d_, k_, p_, D, T, 11, draft_row=r_, accept_len=acc, path=path,
+                        emit=emit, dev_status=st), torch, reps)
+                    a = acc.cpu().numpy()
+                    nbytes = float((a + 1).sum()) * V * 4 * (2 if T > 0 else 1)
+                    res["verify"].append({
+                        "B": B, "V": V, "T": T, "sigma": sigma, "us": round(ms * 1e3, 2),
+                        "GBps_visited": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                        "frac_visited": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                        "tau": round(float(a.mean()) + 1, 4),
+                        "alpha1": round(float((a >= 1).mean()), 4),
+                        "accept_len_hist": np.bincount(a, minlength=D + 1).tolist()})
+                if sigma == ex["sigma"][0]:
+                    ms = timed_ms(lambda: E.eagle_softmax_stats(t_, 1.0, dev_status=st), torch,
+                                  reps)
+                    nbytes = B * n * V * 4
+                    res["softmax"].append({"B": B, "V": V, "ms": round(ms, 4),
+                                           "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                           "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)})
+            del tgt, drows, tok, par, row
+            torch.cuda.empty_cache()
+    # ---- compaction, 80 layers ----
+    for B in ex["B"]:
+        Lmax = 512 + n
+        kc = torch.randn(layers, B, Hkv, Lmax, d, device=dev, generator=g, dtype=torch.bfloat16)
+        vc = torch.randn_like(kc)
+        kv0 = torch.full((B,), 512, dtype=torch.int32, device=dev)
+        kv = kv0.clone()
+        path = torch.full((B, D + 1), -1, dtype=torch.int32, device=dev)
+        path[:, :5] = torch.tensor([0, 3, 14, 25, 36], dtype=torch.int32)
+        acc = torch.full((B,), 4, dtype=torch.int32, device=dev)
+
+        def comp():
+            E.eagle_kv_compact(kc, vc, kv, path, acc, D, dev_status=st)
+            kv.copy_(kv0)
+        ms = timed_ms(comp, torch, reps)
+        res["compact"].append({"B": B, "layers": layers, "accepted": 4, "us": round(ms * 1e3, 2)})
+        del kc, vc
+        torch.cuda.empty_cache()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"sweep device status {int(st.item())}")
+    # ---- the step grid ----
+    attn = {(r["B"], r["L"]): r["ms"] for r in res["attn"]}
+    comp = {r["B"]: r["us"] * 1e-3 for r in res["compact"]}
+    grid = []
+    for r in res["verify"]:
+        for L in ex["L"]:
+            ms = attn[(r["B"], L)] + r["us"] * 1e-3 + comp[r["B"]]
+            grid.append({"B": r["B"], "L": L, "V": r["V"], "T": r["T"], "sigma": r["sigma"],
+                         "ms": round(ms, 4), "steps_per_s": round(1e3 / ms, 1),
+                         "accepted_tokens_per_s": round(r["B"] * r["tau"] * 1e3 / ms, 1)})
+    res["step_grid"] = grid
+    return res
+
+
 def breakdown(st, torch, reps=20):
     """Per-call device time (ms) with its HBM figure, each call timed alone."""
     E = st.E
@@ -422,23 +715,24 @@ def breakdown(st, torch, reps=20):
     res = {}
 
     def t(fn):
-        for _ in range(3):
-            fn()
-        return time_region(lambda i: fn(), reps, torch) / reps
+        return timed_ms(fn, torch, reps)
 
     res["expand_8_levels"] = round(t(lambda: st.expand()), 4)
     a = t(lambda: E.eagle_tree_attn(st.q, st.kc[0], st.vc[0], st.kv_len0, st.parent,
                                     out=st.attn_out, workspace=st.attn_ws))
     kv_bytes = 2 * c.B * c.Hkv * (c.L + c.n) * c.head_dim * 2
     flops = 4.0 * c.B * c.n * c.Hq * c.head_dim * (c.L + c.n)
+    qo_bytes = 2 * c.B * c.n * c.Hq * c.head_dim * 2
     res["tree_attn_1_layer"] = round(a, 4)
-    res["tree_attn_GBps"] = round(kv_bytes / (a * 1e-3) / 1e9, 1)
+    res["tree_attn_GBps"] = round((kv_bytes + qo_bytes) / (a * 1e-3) / 1e9, 1)
     res["tree_attn_TFLOPs"] = round(flops / (a * 1e-3) / 1e12, 1)
+    res["tree_attn_bytes"] = kv_bytes + qo_bytes
     v = t(lambda: E.eagle_verify_accept(st.target, st.logits, st.tokens, st.parent, st.D, 1.0, 7,
                                         draft_row=st.draft_row, accept_len=st.accept_len,
                                         path=st.path, emit=st.emit))
     res["verify_accept"] = round(v, 4)
     rows_visited = float(st.accept_len.sum().item() + st.B)
+    res["verify_visited_row_bytes"] = 2 * rows_visited * c.V * 4
     res["verify_visited_row_GBps"] = round(2 * rows_visited * c.V * 4 / (v * 1e-3) / 1e9, 1)
 
     def comp():
@@ -447,8 +741,29 @@ def breakdown(st, torch, reps=20):
     res["kv_compact_32_layers"] = round(t(comp), 4)
     s = t(lambda: E.eagle_softmax_stats(st.target, 1.0))
     res["softmax_stats_all_rows_standalone"] = round(s, 4)
+    res["softmax_stats_bytes"] = st.target.numel() * 4
     res["softmax_stats_GBps"] = round(st.target.numel() * 4 / (s * 1e-3) / 1e9, 1)
     return res
+
+
+def hbm_rooflines(br, peaks):
+    """HBM roofline fractions of the step's memory-bound calls, each timed alone (median):
+    algorithmic bytes per launch / time, against the measured copy bandwidth."""
+    hbm = peaks["hbm_gbs"]
+    out = {}
+    for name, key_ms, key_b, what in (
+            ("tree_attn", "tree_attn_1_layer", "tree_attn_bytes",
+             "K and V of the committed cache plus the tree rows, Q and O, one layer"),
+            ("verify_accept", "verify_accept", "verify_visited_row_bytes",
+             "target and draft rows of the visited nodes, once each (re-reads not counted)"),
+            ("softmax_stats", "softmax_stats_all_rows_standalone", "softmax_stats_bytes",
+             "every target row once (the eager statistics pass)")):
+        gbs = br[key_b] / (br[key_ms] * 1e-3) / 1e9
+        out[name] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 4), "bytes_per_launch": br[key_b],
+                     "ms_per_launch": br[key_ms], "bytes": what}
+    out["peak_source"] = f"{peaks['source']} hbm_gbs (copy bandwidth)"
+    return out
 
 
 def run_e2e(st, torch, steps, graph=None, copy_streams=4, target_chunks=8, target_in_place=False):
@@ -639,39 +954,91 @@ def cpu_threads():
         return os.cpu_count()
 
 
+def set_oracle_threads(n):
+    """Thread count of the oracle's OpenMP loops (its libgomp ICV on this thread)."""
+    import ctypes
+
+    import oracle
+    oracle.lib()
+    ctypes.CDLL("libgomp.so.1").omp_set_num_threads(int(n))
+
+
 SAMPLE_DESC = ("one sequence per sample: expansion from 71 draft-logit rows, verify walk, "
                "32-layer compaction, tree attention for 1 of 8 kv heads, 1 of 4544 LM-head "
                "rows; scaled to the full B=64 step (x64 sequences, x8 heads, x4544 rows)")
 
 
-def cpu_baseline(budget_s=15.0):
-    s = OracleSample()
-    ests = []
+def oracle_rate(s, budget_s, threads):
+    """Median sampled step estimate of the oracle at `threads` OpenMP threads."""
+    set_oracle_threads(threads)
+    ests, secs = [], []
     t_start = time.perf_counter()
     while not ests or time.perf_counter() - t_start < budget_s:
+        t0 = time.perf_counter()
         est, _ = s.run()
+        secs.append(time.perf_counter() - t0)
         ests.append(est)
-    est = float(np.median(ests))
-    return {"value": round(1.0 / est, 6), "unit": "steps/s", "cores": cpu_threads(),
-            "kind": "oracle", "sample": SAMPLE_DESC + f"; {len(ests)} samples"}
+    return float(np.median(ests)), float(np.median(secs)), len(ests)
+
+
+def cpu_baseline(budget_s=15.0):
+    """The oracle as it stands on the host cores, at all threads (the contract figure) and
+    at one thread."""
+    s = OracleSample()
+    allc = cpu_threads()
+    est, sec, n = oracle_rate(s, budget_s, allc)
+    est1, sec1, n1 = oracle_rate(s, budget_s / 2, 1)
+    set_oracle_threads(allc)
+    return {"value": round(1.0 / est, 6), "unit": "steps/s", "cores": allc,
+            "kind": "oracle", "sample": SAMPLE_DESC + f"; {n} samples of {sec:.2f} s",
+            "one_thread": {"value": round(1.0 / est1, 6), "unit": "steps/s", "cores": 1,
+                           "sample": f"the same sample; {n1} samples of {sec1:.2f} s"}}
+
+
+def workload_config(world):
+    return {"workload": "EAGLE-3 tree verify step, B=64, Llama-3-8B shape: EAGLE-2 "
+                        "expansion 8 levels x top-10 (LM head 4096->128256), rerank to 60 "
+                        "nodes, tree attention 1 layer (32q/8kv heads, d=128, KV 4096), "
+                        "verify V=128256 T=1 sigma=0.3, KV compaction 32 layers",
+            "B": CFG.B, "nodes": CFG.n, "depth": CFG.depth, "top_k": CFG.top_k,
+            "vocab": CFG.V, "hidden": CFG.H, "kv_len": CFG.L, "attn_layers": 1,
+            "compact_layers": CFG.n_layers, "temperature": 1.0,
+            "l2": "inputs larger than L2 (LM head 1.05 GB, logits 2.3 GB, KV 1.1 GB/layer)",
+            "parallelism": f"replicas x{world} (sequence-sharded, no collective)"}
 
 
 def run_reference(args, rank, world):
+    """The oracle arm: each step is one bounded sample of the workload (one sequence's
+    expansion, walk and compaction, one kv head's attention, one LM-head row), timed on
+    the host cores; `value` extrapolates it to the full B=64 step."""
     if rank != 0:
         return None
     s = OracleSample()
+    allc = cpu_threads()
+    set_oracle_threads(allc)
     for _ in range(args.warmup):
         s.run()
-    ests = [s.run()[0] for _ in range(args.steps)]
+    ests, secs = [], []
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        ests.append(s.run()[0])
+        secs.append(time.perf_counter() - t0)
+    wall = time.perf_counter() - t_start
     est = float(np.median(ests))
     value = 1.0 / est
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "steps/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": round(1e3 * wall / args.steps, 1),
+            "ms_per_step_note": "wall time of one bounded sample (what was timed); value is "
+                                "extrapolated from it to the full step",
+            "ms_per_full_step_extrapolated": round(est * 1e3, 1),
+            "sample_seconds_median": round(float(np.median(secs)), 3),
+            "extrapolated": True,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (CPU oracle)", "data": "synthetic",
-            "config": {"workload": "EAGLE-3 tree verify step, B=64, Llama-3-8B shape "
-                                   "(same workload as the GPU arm; bounded CPU sample, scaled)"},
-            "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": cpu_threads(),
+            "config": workload_config(world),
+            "cpu_baseline": {"value": round(value, 6), "unit": "steps/s", "cores": allc,
                              "kind": "oracle", "sample": SAMPLE_DESC},
             "e2e": {"value": round(value, 6), "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -820,12 +1187,22 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", choices=["eagle3_b64", "sweep_70b"], default="eagle3_b64",
+                    help="eagle3_b64: the B=64 step (the benchmark line, with the chain and "
+                         "B=1 Vicuna configs under other_configs); sweep_70b: the Llama-70B "
+                         "grid, one JSON line")
     ap.add_argument("--kernel-case", choices=KERNEL_CASES, default=None,
                     help="profile helper: launch one call on its own workload and exit")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     if args.kernel_case:
         kernel_case(args.kernel_case, args.reps)
+        return
+    if args.config == "sweep_70b":
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"sweep_70b": sweep_70b(torch, dev, measured_peaks())}), flush=True)
         return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -1373,14 +1373,8 @@ softmax_stats_kernel(const float* __restrict__ logits, int64_t rows, int V, floa
 }
 
 
+// CTAs per sequence: 8 while the clusters fit about four per SM, halved as B grows.
 int verify_cluster_size(int B) {
-    static int forced = -1;
-    if (forced < 0) {
-        const char* e = std::getenv("EAGLE_VERIFY_CLUSTER");
-        int f = e ? std::atoi(e) : 0;
-        forced = (f == 1 || f == 2 || f == 4 || f == 8) ? f : 0;
-    }
-    if (forced > 0) return forced;
     const int sms = device_sm_count();
     int cs = 8;
     while (cs > 1 && (int64_t)B * cs > 4LL * sms) cs >>= 1;

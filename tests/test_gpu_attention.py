@@ -125,37 +125,3 @@ def test_unwritten_cache_rows_past_the_tree_do_not_leak(Hq, Hkv, n, L, Lmax):
         ref = oracle.tree_attn(q[b:b + 1], k[b:b + 1], v[b:b + 1], kv_len[b:b + 1],
                                parent[b:b + 1], scale)
         assert attn_row_rel_err(got[b:b + 1], ref).max() <= TOL
-
-
-def test_mma_sync_cross_check_kernel_matches_oracle():
-    """The first (mma.sync) tree-attention kernel stays selectable as a cross-check
-    with EAGLE_ATTN_MMA_SYNC=1, read once per process, so it runs in a child process:
-    two sequences (one long enough to split its keys), ragged tails, against the oracle."""
-    import os
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    script = r'''
-import sys, numpy as np, torch
-sys.path.insert(0, ".")
-import oracle, workloads as W
-import eagle_tree_speculative_gb300 as E
-from tests.helpers import attn_row_rel_err
-B, n, Hq, Hkv = 2, 21, 8, 2
-L = [1500, 37]
-q, k, v, kv_len = W.attn_inputs(B, n, Hq, Hkv, 128, L, 1600, seed=71)
-parent = np.stack([W.random_tree(n, 5, 71, b) for b in range(B)])
-st = torch.zeros(1, dtype=torch.int32, device="cuda")
-out = E.eagle_tree_attn(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(kv_len).cuda(),
-                        torch.from_numpy(parent).cuda(), scale=128 ** -0.5, dev_status=st)
-torch.cuda.synchronize()
-assert int(st.item()) == 0
-ref = oracle.tree_attn(q, k, v, kv_len, parent, 128 ** -0.5)
-err = attn_row_rel_err(out.float().cpu().numpy(), ref).max()
-print("max rel err", err)
-sys.exit(0 if err <= 1e-2 else 1)
-'''
-    env = dict(os.environ, EAGLE_ATTN_MMA_SYNC="1")
-    r = subprocess.run([sys.executable, "-c", script], cwd=root, env=env, capture_output=True,
-                       text=True, timeout=300)
-    assert r.returncode == 0, r.stdout + r.stderr

@@ -208,6 +208,51 @@ def eagle_verify_accept(target_logits, draft_logits, tokens, parent, max_depth, 
     return accept_len, path, emit
 
 
+def eagle_verify_accept_sharded(target_shards, draft_shards, shard_begin, tokens, parent, max_depth,
+                                temperature, seed, draft_row=None, accept_len=None, path=None,
+                                emit=None, row_stats=None, dev_status=None, stream=None):
+    """Vocab-parallel verify: shard r of every target row ([B, n, Vr]) and draft row
+    ([B, R, Vr]) holds the ids shard_begin[r] .. shard_begin[r+1]-1 (shard_begin: S + 1
+    ints, 0 first, V last).  Returns (accept_len, path, emit) as eagle_verify_accept."""
+    S = len(target_shards)
+    begin = [int(x) for x in shard_begin]
+    if len(begin) != S + 1:
+        raise ValueError("shard_begin needs one entry per shard plus the vocabulary size")
+    for r, t in enumerate(target_shards):
+        _dev(t, f"target_shards[{r}]", torch.float32)
+        if t.shape[-1] != begin[r + 1] - begin[r]:
+            raise ValueError(f"target_shards[{r}] does not hold ids {begin[r]}..{begin[r + 1] - 1}")
+    B, n = target_shards[0].shape[:2]
+    V = begin[-1]
+    R = n
+    dptrs = None
+    if draft_shards is not None:
+        if len(draft_shards) != S:
+            raise ValueError("one draft shard per target shard")
+        for r, t in enumerate(draft_shards):
+            _dev(t, f"draft_shards[{r}]", torch.float32)
+        R = draft_shards[0].shape[1]
+        dptrs = (ctypes.c_void_p * S)(*[t.data_ptr() for t in draft_shards])
+    tptrs = (ctypes.c_void_p * S)(*[t.data_ptr() for t in target_shards])
+    cbeg = (ctypes.c_int32 * (S + 1))(*begin)
+    _dev(tokens, "tokens", torch.int32)
+    _dev(parent, "parent", torch.int32)
+    if draft_row is not None:
+        _dev(draft_row, "draft_row", torch.int32)
+    dev = tokens.device
+    D = int(max_depth)
+    accept_len = torch.empty(B, dtype=torch.int32, device=dev) if accept_len is None else accept_len
+    path = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if path is None else path
+    emit = torch.empty(B, D + 1, dtype=torch.int32, device=dev) if emit is None else emit
+    if row_stats is not None:
+        _dev(row_stats, "row_stats", torch.float32)
+    _check("eagle_verify_accept_sharded", lib().eagle_verify_accept_sharded(
+        tptrs, dptrs, cbeg, S, _ptr(draft_row), _ptr(tokens), _ptr(parent), B, n, V, R, D,
+        float(temperature), int(seed) & (2**64 - 1), _ptr(accept_len), _ptr(path), _ptr(emit),
+        _ptr(row_stats), _ptr(_status(dev_status, dev)), _stream(stream)))
+    return accept_len, path, emit
+
+
 def eagle_kv_compact(k_cache, v_cache, kv_len, path, accept_len, max_depth, dev_status=None,
                      stream=None):
     """k/v cache [n_layers,B,Hkv,Lmax,d] bf16 (in place); kv_len updated in place."""

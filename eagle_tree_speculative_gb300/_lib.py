@@ -27,6 +27,8 @@ SIGNATURES = {
     "eagle_verify_filter_workspace_size": (_SZ, [_I, _I, _I]),
     "eagle_verify_accept_filtered": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _U64, _I,
                                           _F, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "eagle_verify_accept_sharded": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _F, _U64,
+                                         _P, _P, _P, _P, _P, _P]),
     "eagle_d2t_inverse": (_I, [_P, _I, _I, _P, _P, _P]),
     "eagle_verify_accept_d2t": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _F, _U64, _P,
                                      _P, _P, _P, _P, _P]),

@@ -59,6 +59,15 @@ __device__ __forceinline__ bool filter_keeps(const FilterParam& f, int t, float 
     return k > f.key || (k == f.key && t <= f.idx);
 }
 
+// Vocabulary shards of a vocab-parallel walk: rank r holds ids [begin[r], begin[r+1])
+// of every target and draft row in its own buffers, f32 [B, n, Vr] and [B, R, Vr].
+constexpr int kMaxShards = 8;
+struct ShardTable {
+    const float* tgt[kMaxShards];
+    const float* drf[kMaxShards];
+    int begin[kMaxShards + 1];
+};
+
 struct VerifyArgs {
     const float* target;
     const float* draft;
@@ -81,6 +90,9 @@ struct VerifyArgs {
     int top_k;             // filtered walk only
     float top_p;
     bool target_in_device; // target rows in device memory (not pinned host memory)
+    int S = 0;             // vocab-parallel walk: number of shards (0: whole rows)
+    bool shard_vec4 = false;
+    ShardTable sh{};
 };
 
 // Softmax statistics of a row at temperature T, kept over the raw logits:
@@ -263,6 +275,23 @@ struct Cluster {
         const float S = sm.bc.f[0];
         buf ^= 1;
         return S;
+    }
+    // Two values held by CTA `owner` to every thread of every CTA (one cluster barrier).
+    __device__ static void bcast2(Smem& sm, int& buf, int rank, int owner, float& f0, float& f1) {
+        if (rank == owner && threadIdx.x == 0) {
+            sm.x[buf].f[0] = f0;
+            sm.x[buf].f[1] = f1;
+        }
+        sync();
+        if (threadIdx.x == 0) {
+            const Slot* o = slot(sm, buf, owner);
+            sm.bc.f[0] = o->f[0];
+            sm.bc.f[1] = o->f[1];
+        }
+        __syncthreads();
+        f0 = sm.bc.f[0];
+        f1 = sm.bc.f[1];
+        buf ^= 1;
     }
     __device__ static KeyIdx argmax(Smem& sm, int& buf, KeyIdx v, int& bad) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -923,8 +952,8 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
     const int b = blockIdx.x / CS;
     const int n = a.n, V = a.V;
     const float c = a.c;
-    const int64_t Vl = V;
-    const int64_t Vdl = D2T ? a.Vd : V;      // draft-row length
+    int64_t Vl = V;
+    int64_t Vdl = D2T ? a.Vd : V;            // draft-row length
 
     // ---- load and validate the tree (identically in every CTA) ----
     if (tid < n) {
@@ -967,12 +996,30 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
 
     // ---- vocabulary slice of this CTA ----
     const int chunk = (((V + CS - 1) / CS) + 3) & ~3;
-    const int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
+    int lo = min(V, rank * chunk), hi = min(V, lo + chunk);
     const float* tgt_b = a.target + (int64_t)b * n * Vl;
     const float* drf_b = a.draft ? a.draft + (int64_t)b * a.R * Vdl : nullptr;
-    const bool vec4 = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0) &&
-                      (a.draft == nullptr || (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0) &&
-                      (!D2T || (((a.Vd & 3) == 0) && (reinterpret_cast<uintptr_t>(a.t2d) & 15) == 0));
+    bool vec4 = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0) &&
+                (a.draft == nullptr || (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0) &&
+                (!D2T || (((a.Vd & 3) == 0) && (reinterpret_cast<uintptr_t>(a.t2d) & 15) == 0));
+    // Vocab-parallel walk: this CTA stands for rank `rank` and reads only its shard.  Its
+    // slice is the shard's id range, its rows are the shard's rows (length hi - lo), and
+    // the row bases are moved back by lo so that row[t] is the shard's element t - lo.
+    const bool sharded = !D2T && !FILT && a.S > 0;
+    int64_t shift = 0;
+    if (sharded) {
+        // CTAs past the last shard (the cluster is rounded up to a power of two) get an
+        // empty slice; their row pointers stay non-null, as "has a draft row" is read from
+        // them, and are never dereferenced (the owner of a token is always a real rank).
+        const int r = rank < a.S ? rank : 0;
+        lo = rank < a.S ? a.sh.begin[rank] : V;
+        hi = rank < a.S ? a.sh.begin[rank + 1] : V;
+        Vl = Vdl = hi - lo;
+        shift = lo;
+        tgt_b = a.sh.tgt[r] + (int64_t)b * n * Vl;
+        drf_b = a.sh.drf[r] ? a.sh.drf[r] + (int64_t)b * a.R * Vdl : nullptr;
+        vec4 = a.shard_vec4;
+    }
     // the CTA's slice of the draft row for its statistics (the target slice otherwise)
     const int chunkd = D2T ? ((((a.Vd + CS - 1) / CS) + 3) & ~3) : chunk;
     const int plo = D2T ? min(a.Vd, rank * chunkd) : lo;
@@ -986,10 +1033,10 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
     if (tid == 0) sm.path[0] = 0;
 
     while (!err) {
-        const float* qrow = tgt_b + (int64_t)v * Vl;
+        const float* qrow = tgt_b + (int64_t)v * Vl - shift;
         const bool kids = sm.nkids[v] > 0;
         if (a.T > 0.f) {
-            const float* prow = kids ? drf_b + (int64_t)sm.row[v] * Vdl : nullptr;
+            const float* prow = (kids && drf_b) ? drf_b + (int64_t)sm.row[v] * Vdl - shift : nullptr;
             const PRow<D2T> pr{prow, a.t2d};
             // filtered walk: this node's row filters; logits outside them read as -inf
             FilterParam fqv{}, fpv{};
@@ -1126,7 +1173,20 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
             for (int ch = v + 1; ch < n && kids; ++ch) {
                 if (sm.parent[ch] != v) continue;
                 const int x = sm.tok[ch];
-                const float lq = mq(x, qrow[x]), lp = mp(x, pr.one(x));
+                float lq, lp;
+                if (sharded) {
+                    // q(x) and p(x): only the rank owning x holds them
+                    int owner = 0;
+                    while (owner + 1 < a.S && x >= a.sh.begin[owner + 1]) ++owner;
+                    if (rank == owner) {
+                        lq = qrow[x];
+                        lp = pr.one(x);
+                    }
+                    C::bcast2(sm, buf, rank, owner, lq, lp);
+                } else {
+                    lq = mq(x, qrow[x]);
+                    lp = mp(x, pr.one(x));
+                }
                 const float px = prob_of(lp, P.lmax, ip, c);
                 const float r = resid_weight(lq, lp, Q, iq, P, ip, c, rs);
                 const float u = accept_uniform(a.seed, (uint32_t)b, (uint32_t)ch);
@@ -1471,6 +1531,63 @@ extern "C" eagle_status eagle_verify_accept(const float* target_logits, const fl
                          dev_status, stream);
 }
 
+extern "C" eagle_status eagle_verify_accept_sharded(
+    const float* const* target_shards, const float* const* draft_shards, const int32_t* shard_begin,
+    int S, const int32_t* draft_row, const int32_t* tokens, const int32_t* parent, int B, int n, int V,
+    int R, int max_depth, float temperature, uint64_t seed, int32_t* accept_len, int32_t* path,
+    int32_t* emit, float* row_stats, int32_t* dev_status, eagle_stream_t stream) {
+    if (!target_shards || !shard_begin || S < 1) return EAGLE_ERR_INVALID_ARG;
+    if (S > kMaxShards) return EAGLE_ERR_SHAPE;
+    if (B < 0 || n < 1 || V < 1 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
+    if (n > kMaxNodes || max_depth > kMaxNodes) return EAGLE_ERR_SHAPE;
+    if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
+    if (!tokens || !parent || !accept_len || !path || !emit) return EAGLE_ERR_INVALID_ARG;
+    if (shard_begin[0] != 0 || shard_begin[S] != V) return EAGLE_ERR_SHAPE;
+    const bool t_pos = temperature > 0.f;
+    if (t_pos) {
+        if (!draft_shards || R < 1) return EAGLE_ERR_INVALID_ARG;
+        if (!draft_row && R != n) return EAGLE_ERR_SHAPE;
+    }
+    VerifyArgs a{};
+    bool vec4 = (V & 3) == 0;
+    for (int r = 0; r < S; ++r) {
+        if (shard_begin[r + 1] <= shard_begin[r]) return EAGLE_ERR_SHAPE;     // empty shard
+        if (!target_shards[r] || (t_pos && !draft_shards[r])) return EAGLE_ERR_INVALID_ARG;
+        a.sh.tgt[r] = target_shards[r];
+        a.sh.drf[r] = t_pos ? draft_shards[r] : nullptr;
+        a.sh.begin[r] = shard_begin[r];
+        vec4 = vec4 && (shard_begin[r] & 3) == 0 &&
+               (reinterpret_cast<uintptr_t>(target_shards[r]) & 15) == 0 &&
+               (!t_pos || (reinterpret_cast<uintptr_t>(draft_shards[r]) & 15) == 0);
+    }
+    a.sh.begin[S] = V;
+    if (B == 0) return EAGLE_OK;
+    a.target = target_shards[0];
+    a.draft = t_pos ? draft_shards[0] : nullptr;
+    a.draft_row = draft_row;
+    a.tokens = tokens;
+    a.parent = parent;
+    a.B = B; a.n = n; a.V = V; a.R = R; a.D = max_depth;
+    a.T = temperature;
+    a.c = t_pos ? kLog2e / temperature : 0.f;
+    a.seed = seed;
+    a.accept_len = accept_len; a.path = path; a.emit = emit;
+    a.row_stats = row_stats;
+    a.dev_status = dev_status;
+    a.Vd = V;
+    a.S = S;
+    a.shard_vec4 = vec4;
+    constexpr int NT = kVerifyThreads;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // one CTA per rank; the cluster is the next power of two, extra CTAs hold no shard
+    cudaError_t e;
+    if (S == 1) e = launch_clustered(verify_walk_kernel<1, NT, false, false>, B, 1, NT, 0, s, a);
+    else if (S == 2) e = launch_clustered(verify_walk_kernel<2, NT, false, false>, B, 2, NT, 0, s, a);
+    else if (S <= 4) e = launch_clustered(verify_walk_kernel<4, NT, false, false>, B, 4, NT, 0, s, a);
+    else e = launch_clustered(verify_walk_kernel<8, NT, false, false>, B, 8, NT, 0, s, a);
+    return e == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+}
+
 extern "C" eagle_status eagle_verify_accept_d2t(const float* target_logits, const float* draft_logits,
                                                 const int32_t* draft_row, const int32_t* tokens,
                                                 const int32_t* parent, int B, int n, int V, int R,
@@ -1518,6 +1635,24 @@ extern "C" eagle_status eagle_d2t_inverse(const int32_t* d2t, int Vd, int V, int
     return EAGLE_OK;
 }
 
+namespace eagle {
+namespace {
+// Resident CTAs per SM of one softmax_stats_kernel variant (looked up once per variant).
+template <bool STATS, bool ARGMAX>
+int stats_ctas_per_sm() {
+    static int cached = 0;
+    if (cached == 0) {
+        int v = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &v, softmax_stats_kernel<STATS, ARGMAX>, kStatThreads, 0) != cudaSuccess)
+            return 0;
+        cached = v;
+    }
+    return cached;
+}
+}  // namespace
+}  // namespace eagle
+
 extern "C" eagle_status eagle_softmax_stats(const float* logits, int64_t rows, int V,
                                             float temperature, float* row_max, float* row_sum,
                                             int32_t* row_argmax, int32_t* dev_status,
@@ -1528,19 +1663,21 @@ extern "C" eagle_status eagle_softmax_stats(const float* logits, int64_t rows, i
     if (stats && (!row_max || !row_sum)) return EAGLE_ERR_INVALID_ARG;
     if (!stats && !row_argmax) return EAGLE_ERR_INVALID_ARG;
     if (rows == 0) return EAGLE_OK;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
-    const int grid = (int)(rows < cap ? rows : cap);
     const float c = stats ? kLog2e / temperature : 0.f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // One resident wave: every CTA of the grid is on an SM from the start (the variants
+    // differ in registers, hence in CTAs per SM), and each walks its rows grid-stride.
+    auto launch = [&](auto kernel, int per_sm) -> eagle_status {
+        if (per_sm < 1) return EAGLE_ERR_CUDA;
+        const int64_t cap = (int64_t)device_sm_count() * per_sm;
+        const int grid = (int)(rows < cap ? rows : cap);
+        kernel<<<grid, kStatThreads, 0, s>>>(logits, rows, V, temperature, c, row_max, row_sum,
+                                             row_argmax, dev_status);
+        EAGLE_CHECK_LAUNCH();
+        return EAGLE_OK;
+    };
     if (stats && row_argmax)
-        softmax_stats_kernel<true, true><<<grid, kStatThreads, 0, s>>>(
-            logits, rows, V, temperature, c, row_max, row_sum, row_argmax, dev_status);
-    else if (stats)
-        softmax_stats_kernel<true, false><<<grid, kStatThreads, 0, s>>>(
-            logits, rows, V, temperature, c, row_max, row_sum, row_argmax, dev_status);
-    else
-        softmax_stats_kernel<false, true><<<grid, kStatThreads, 0, s>>>(
-            logits, rows, V, temperature, c, row_max, row_sum, row_argmax, dev_status);
-    EAGLE_CHECK_LAUNCH();
-    return EAGLE_OK;
+        return launch(softmax_stats_kernel<true, true>, stats_ctas_per_sm<true, true>());
+    if (stats) return launch(softmax_stats_kernel<true, false>, stats_ctas_per_sm<true, false>());
+    return launch(softmax_stats_kernel<false, true>, stats_ctas_per_sm<false, true>());
 }

@@ -143,6 +143,39 @@ eagle_status eagle_verify_accept(const float* target_logits, const float* draft_
                                  float* row_stats, int32_t* dev_status, eagle_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * eagle_verify_accept_sharded -- eagle_verify_accept with every logits row split
+ * by vocabulary across S ranks, as a vocabulary-parallel LM head leaves it
+ * (Lesson "不变量：Leviathan 拒绝采样": the rule the split walk must keep; Guide
+ * "EAGLE-3：取消特征约束...": the draft head's own lm_head, which a tensor-parallel
+ * deployment splits by vocabulary).  Rank r holds ids shard_begin[r] ..
+ * shard_begin[r+1]-1 of every row in its own buffers and reads nothing else; the
+ * ranks exchange only at four points: the row statistics (max, then the rescaled
+ * sum, in rank order), the drafted token's q(x) and p(x) (from the rank owning x),
+ * each rejection's residual normaliser (a sum in rank order) and the final
+ * token's race winner (largest key, lower token on ties).  On one GPU each rank is
+ * one CTA of the sequence's thread-block cluster and the exchanges go through its
+ * distributed shared memory.  Results are those of eagle_verify_accept on the
+ * whole rows (same uniforms, same rule), up to float summation order.
+ *   target_shards  HOST array of S device pointers; shard r is f32 [B, n, Vr],
+ *                  Vr = shard_begin[r+1] - shard_begin[r]
+ *   draft_shards   HOST array of S device pointers, shard r f32 [B, R, Vr]; may
+ *                  be NULL at T = 0
+ *   shard_begin    HOST int32 [S + 1]: 0 = shard_begin[0] < ... < shard_begin[S] = V
+ *   S              1 .. 8
+ * Other arguments, outputs and device errors as eagle_verify_accept.  Host
+ * errors: EAGLE_ERR_SHAPE for S > 8, an empty shard or bounds not 0 .. V.
+ * ------------------------------------------------------------------------- */
+eagle_status eagle_verify_accept_sharded(const float* const* target_shards,
+                                         const float* const* draft_shards,
+                                         const int32_t* shard_begin, int S,
+                                         const int32_t* draft_row, const int32_t* tokens,
+                                         const int32_t* parent, int B, int n, int V, int R,
+                                         int max_depth, float temperature, uint64_t seed,
+                                         int32_t* accept_len, int32_t* path, int32_t* emit,
+                                         float* row_stats, int32_t* dev_status,
+                                         eagle_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * eagle_verify_accept_filtered -- eagle_verify_accept with top-k / top-p
  * filtering.  Guide "一次 eagenerate 调用的完整流转": eagenerate takes
  * temperature, top_p and top_k (0 = off); the pages give no further rule.

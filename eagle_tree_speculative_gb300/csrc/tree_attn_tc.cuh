@@ -93,6 +93,7 @@ struct Bars {
     int err;
     int pad;
     unsigned long long anc[kMaxNodes];
+    int par[kMaxNodes];
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -127,19 +128,10 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
+    // the parent array, one node per thread; the ancestor masks are built from it below
+    if (tid < n) bars->par[tid] = a.parent[(int64_t)b * n + tid];
     if (tid == 0) {
-        int err = 0;
-        const int32_t* par = a.parent + (int64_t)b * n;
-        if (par[0] != -1) err = EAGLE_DEV_BAD_TREE;
-        bars->anc[0] = 1ull;
-        for (int i = 1; i < n && !err; ++i) {
-            const int p = par[i];
-            if (p < 0 || p >= i) { err = EAGLE_DEV_BAD_TREE; break; }
-            bars->anc[i] = bars->anc[p] | (1ull << i);
-        }
-        if (L < 0 || (int64_t)L + n > a.Lmax) err |= EAGLE_DEV_CAPACITY;
-        if (err && rg == 0 && blockIdx.y == 0) flag_error(a.dev_status, err);
-        bars->err = err;
+        bars->err = (L < 0 || (int64_t)L + n > a.Lmax) ? EAGLE_DEV_CAPACITY : 0;
         for (int s = 0; s < KSTAGES; ++s) {
             mbar_init(s32(&bars->k_full[s]), 1);
             mbar_init(s32(&bars->k_empty[s]), 1);
@@ -165,6 +157,28 @@ tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
+    // A0: anc[i] = {i} and its ancestors, one thread per node walking up the parents in
+    // shared memory (each step goes to a smaller index, so at most i steps); a parent
+    // outside [0, i) (or a root parent other than -1) flags the tree as invalid
+    if (tid < n) {
+        unsigned long long m = 1ull << tid;
+        int e = 0;
+        if (tid == 0) {
+            if (bars->par[0] != -1) e = EAGLE_DEV_BAD_TREE;
+        } else {
+            int x = tid;
+            while (x > 0) {
+                const int p = bars->par[x];
+                if (p < 0 || p >= x) { e = EAGLE_DEV_BAD_TREE; break; }
+                m |= 1ull << p;
+                x = p;
+            }
+        }
+        bars->anc[tid] = m;
+        if (e) atomicOr(&bars->err, e);
+    }
+    __syncthreads();
+    if (tid == 0 && bars->err && rg == 0 && blockIdx.y == 0) flag_error(a.dev_status, bars->err);
     const bool err = bars->err != 0;
 
     // key range of this split: committed keys are chunked, the last split adds the tree

@@ -91,6 +91,19 @@ def test_llama70b_shape_sweep_points(B, L, sample):
            sample=sample)
 
 
+@pytest.mark.parametrize("B,n,Hq,Hkv,L", [
+    (1, 60, 32, 8, [8192]),            # two M-tiles, keys split across CTAs
+    (2, 40, 16, 4, [1000, 77]),        # 160 rows: a part-empty second M-tile;
+                                       # 77 + 40 keys fit in less than one key tile
+    (2, 60, 64, 8, [500, 2000]),       # 480 rows: four M-tiles per (sequence, kv head)
+    (3, 33, 32, 4, [129, 1, 4096]),    # 264 rows: three M-tiles, one holding 8 rows
+])
+def test_row_tiles_of_every_count(B, n, Hq, Hkv, L):
+    """(node, head) rows of one (sequence, kv head) in one to four 128-row M-tiles, with
+    ragged last tiles and caches shorter than one key tile.  Every row checked."""
+    _check(B=B, n=n, Hq=Hq, Hkv=Hkv, kv_len=L, Lmax=max(L) + n, seed=31 + n)
+
+
 def test_capacity_and_tree_errors_set_status_and_zero_output():
     import eagle_tree_speculative_gb300 as E
     q, k, v, kv_len = W.attn_inputs(2, 4, 2, 1, 128, [10, 3], 13, seed=8)

@@ -60,7 +60,7 @@ extern "C" eagle_status eagle_ttt_attn(const void* q, const void* k, const void*
     const int G = Hq / Hkv;
     const int64_t slabs = (int64_t)B * Hkv;
     const int64_t tiles = ((int64_t)S * G + ttt_tc::ROWS_PER_CTA - 1) / ttt_tc::ROWS_PER_CTA;
-    if (slabs > 0x7fffffffLL || tiles > 65535 || (int64_t)S * G > 0x7fffffffLL ||
+    if (slabs * tiles > 0x7fffffffLL || (int64_t)S * G > 0x7fffffffLL ||
         (int64_t)R1 * S > 0x7fffffffLL)
         return EAGLE_ERR_SHAPE;
     // A row tile of 128 rows spans at most 127 / G + 1 positions, one more when G
@@ -83,7 +83,10 @@ extern "C" eagle_status eagle_ttt_attn(const void* q, const void* k, const void*
     if (cudaFuncSetAttribute(ttt_tc::ttt_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              ttt_tc::SMEM_BYTES) != cudaSuccess)
         return EAGLE_ERR_CUDA;
-    dim3 grid((unsigned)slabs, (unsigned)tiles, 1);
+    a.tiles = (int)tiles;
+    // slab-major: the row tiles of one (sequence, kv head) run together, so only a few
+    // slabs' round-0 K/V are live in L2 at a time while the diagonal rows stream past
+    dim3 grid((unsigned)(slabs * tiles), 1, 1);
     ttt_tc::ttt_attn_tc_kernel<<<grid, ttt_tc::kThreads, ttt_tc::SMEM_BYTES,
                                  reinterpret_cast<cudaStream_t>(stream)>>>(mk, mv, mkd, mvd, a);
     return cudaGetLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;

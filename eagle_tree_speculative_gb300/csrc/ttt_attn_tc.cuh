@@ -68,6 +68,7 @@ struct Args {
     int PB;                   // positions per diagonal box (>= positions of any row tile)
     int RB;                   // rounds per diagonal box (PB * RB <= 128)
     int ND;                   // diagonal tiles: ceil(r / RB)
+    int tiles;                // row tiles per (sequence, kv head)
     float scale_log2;
     int32_t* dev_status;
 };
@@ -111,9 +112,10 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
     volatile int* abort_flag = &bars->abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kvz = blockIdx.x;                           // (sequence, kv head) slab
+    const int kvz = (int)(blockIdx.x / (unsigned)a.tiles);   // (sequence, kv head) slab
     const int b = kvz / a.Hkv, kvh = kvz % a.Hkv;
-    const int rg = (int)gridDim.y - 1 - (int)blockIdx.y;  // row tiles with the most keys first
+    // within a slab, the row tiles with the most keys first
+    const int rg = a.tiles - 1 - (int)(blockIdx.x % (unsigned)a.tiles);
     const int G = a.G, S = a.S, rows = S * G;
     const int row0 = rg * ROWS_PER_CTA;
     const int row_end = min(row0 + ROWS_PER_CTA, rows);

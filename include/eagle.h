@@ -269,7 +269,7 @@ eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, con
  *        1 .. R1-1 simulated; only rounds 0 .. r are read)
  *   out  bf16 [B, S, Hq, head_dim]
  * Sizes: S >= 1, 1 <= R1 <= 16, 0 <= r < R1, head_dim == 128, Hq % Hkv == 0,
- * ceil(S * Hq / Hkv / 128) <= 65535.  Every row of round 0 must be finite (rows
+ * B * Hkv * ceil(S * Hq / Hkv / 128) < 2^31.  Every row of round 0 must be finite (rows
  * past a query's position are read and masked).  All pointers 16-byte aligned;
  * with B == 0 nothing is read or written and they may be NULL.
  * Device errors: a wait that exceeds its limit sets EAGLE_DEV_TIMEOUT.

@@ -666,8 +666,8 @@ def sweep_70b(torch, dev, peaks, reps=20):
                         "alpha1": round(float((a >= 1).mean()), 4),
                         "accept_len_hist": np.bincount(a, minlength=D + 1).tolist()})
                 if sigma == ex["sigma"][0]:
-                    ms = timed_ms(lambda: E.eagle_softmax_stats(t_, 1.0, dev_status=st), torch,
-                                  reps)
+                    ms = timed_ms(lambda: E.eagle_softmax_stats(t_, 1.0, dev_status=st,
+                                                                argmax=False), torch, reps)
                     nbytes = B * n * V * 4
                     res["softmax"].append({"B": B, "V": V, "ms": round(ms, 4),
                                            "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
@@ -739,7 +739,8 @@ def breakdown(st, torch, reps=20):
         E.eagle_kv_compact(st.kc, st.vc, st.kv_len, st.path, st.accept_len, st.D)
         st.kv_len.copy_(st.kv_len0)
     res["kv_compact_32_layers"] = round(t(comp), 4)
-    s = t(lambda: E.eagle_softmax_stats(st.target, 1.0))
+    # T = 1: the row statistics (max, sum) the walk needs; the argmax is the T = 0 output
+    s = t(lambda: E.eagle_softmax_stats(st.target, 1.0, argmax=False))
     res["softmax_stats_all_rows_standalone"] = round(s, 4)
     res["softmax_stats_bytes"] = st.target.numel() * 4
     res["softmax_stats_GBps"] = round(st.target.numel() * 4 / (s * 1e-3) / 1e9, 1)
@@ -1141,7 +1142,8 @@ def kernel_case(name, reps):
                                                draft_row=row, dev_status=st, top_k=50, top_p=0.9,
                                                workspace=ws)
         else:
-            fn = lambda: E.eagle_softmax_stats(target, 1.0, dev_status=st)  # noqa: E731
+            fn = lambda: E.eagle_softmax_stats(target, 1.0, dev_status=st,  # noqa: E731
+                                               argmax=False)
     elif name == "compact":
         B = 4
         shape = (c.n_layers, B, c.Hkv, c.Lmax, c.head_dim)

@@ -393,7 +393,10 @@ def eagle2_expand_static_state(level, final, logits, top_k, depth, n_out, hidden
 
 
 def eagle_softmax_stats(logits, temperature, row_max=None, row_sum=None, row_argmax=None,
-                        dev_status=None, stream=None):
+                        dev_status=None, stream=None, argmax=True):
+    """(row_max, row_sum, row_argmax) of softmax(logits / T) per row.  At T > 0 the
+    argmax is computed only when `argmax` is true (or row_argmax is given); it is
+    returned as None otherwise."""
     _dev(logits, "logits", torch.float32)
     V = logits.shape[-1]
     rows = logits.numel() // V
@@ -402,7 +405,7 @@ def eagle_softmax_stats(logits, temperature, row_max=None, row_sum=None, row_arg
     if temperature > 0:
         row_max = torch.empty(shp, dtype=torch.float32, device=dev) if row_max is None else row_max
         row_sum = torch.empty(shp, dtype=torch.float32, device=dev) if row_sum is None else row_sum
-    if row_argmax is None:
+    if row_argmax is None and (argmax or temperature <= 0):
         row_argmax = torch.empty(shp, dtype=torch.int32, device=dev)
     _check("eagle_softmax_stats", lib().eagle_softmax_stats(
         _ptr(logits), rows, V, float(temperature), _ptr(row_max), _ptr(row_sum), _ptr(row_argmax),

@@ -224,19 +224,25 @@ def test_softmax_stats_match_oracle(V, T):
         np.testing.assert_allclose(gz.cpu().numpy(), Z, rtol=1e-5)
 
 
-def test_softmax_stats_full_size_sampled_rows():
-    """B*n = 3840 rows of V = 128256 on the GPU; 64 sampled rows checked by the oracle."""
+@pytest.mark.parametrize("argmax", [True, False])
+def test_softmax_stats_full_size_sampled_rows(argmax):
+    """B*n = 3840 rows of V = 128256 on the GPU, with and without the argmax (the
+    statistics-only variant is the one a T > 0 walk needs); 64 sampled rows checked by
+    the oracle."""
     E = _gpu()
     B, n, V = 64, 60, 128256
     x = W.per_seq_normal(B, (n, V), 2.0, 11, W.TAG_TARGET)
-    gm, gz, ga = E.eagle_softmax_stats(_cuda(x), 1.0)
+    gm, gz, ga = E.eagle_softmax_stats(_cuda(x), 1.0, argmax=argmax)
     torch.cuda.synchronize()
     rows = W.rng(11, 1).choice(B * n, size=64, replace=False)
     flat = x.reshape(B * n, V)[rows]
     m, Z, am, _ = oracle.softmax_rows(flat, 1.0)
     np.testing.assert_allclose(gm.reshape(-1).cpu().numpy()[rows], m, rtol=1e-6)
     np.testing.assert_allclose(gz.reshape(-1).cpu().numpy()[rows], Z, rtol=1e-5)
-    assert np.array_equal(ga.reshape(-1).cpu().numpy()[rows], am)
+    if argmax:
+        assert np.array_equal(ga.reshape(-1).cpu().numpy()[rows], am)
+    else:
+        assert ga is None
 
 
 # ---------------------------------------------------------------- draft vocabulary (d2t)

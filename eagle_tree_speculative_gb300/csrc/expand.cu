@@ -718,17 +718,20 @@ eagle_status expand_validate(int level, int final, const void* hidden, const voi
                              const float* logits, int B, int H, int V, int top_k, int depth,
                              int n_out, const int32_t* out_tokens, const int32_t* out_parent,
                              const int32_t* out_draft_row) {
-    if (B < 0 || V < 1 || top_k < 1 || depth < 1 || level < 1 || level > depth || !logits)
+    if (B < 0 || V < 1 || top_k < 1 || depth < 1 || level < 1 || level > depth)
         return EAGLE_ERR_INVALID_ARG;
     if (top_k > kKMax || depth > kDepthMax || top_k > V) return EAGLE_ERR_SHAPE;
     if (StateView::cand_count(top_k, depth) > 4096) return EAGLE_ERR_SHAPE;
     if (final) {
-        if (!out_tokens || !out_parent || !out_draft_row) return EAGLE_ERR_INVALID_ARG;
         if (n_out < 2 || n_out > kMaxNodes) return EAGLE_ERR_SHAPE;
         const int have = 1 + top_k + (level - 1) * top_k * top_k;
         if (n_out > have) return EAGLE_ERR_SHAPE;
     }
-    if (hidden && (!lm_head_w || H < 1)) return EAGLE_ERR_INVALID_ARG;
+    if (hidden && H < 1) return EAGLE_ERR_INVALID_ARG;
+    if (B == 0) return EAGLE_OK;                        // pointers unused: nothing read or written
+    if (!logits) return EAGLE_ERR_INVALID_ARG;
+    if (final && (!out_tokens || !out_parent || !out_draft_row)) return EAGLE_ERR_INVALID_ARG;
+    if (hidden && !lm_head_w) return EAGLE_ERR_INVALID_ARG;
     return EAGLE_OK;
 }
 
@@ -738,11 +741,12 @@ eagle_status expand_common(int level, int final, const void* hidden, const void*
                            size_t partials_bytes, const int32_t* d2t, int32_t* out_tokens,
                            int32_t* out_parent, int32_t* out_draft_row, int32_t* frontier_tokens,
                            int32_t* dev_status, eagle_stream_t stream) {
-    if (!tree_state) return EAGLE_ERR_INVALID_ARG;
     const eagle_status vs = expand_validate(level, final, hidden, lm_head_w, logits, B, H, V,
                                             top_k, depth, n_out, out_tokens, out_parent,
                                             out_draft_row);
     if (vs != EAGLE_OK) return vs;
+    if (B == 0) return EAGLE_OK;
+    if (!tree_state) return EAGLE_ERR_INVALID_ARG;
     if (state_bytes < eagle2_tree_state_size(B, top_k, depth)) return EAGLE_ERR_CAPACITY;
     // fused top-k: every 256-column tile of a row was (or is now) reduced by the
     // GEMM's epilogue to its statistics and top-k; only those partials are merged
@@ -751,7 +755,6 @@ eagle_status expand_common(int level, int final, const void* hidden, const void*
                   (reinterpret_cast<uintptr_t>(partials) & 7)))
         return EAGLE_ERR_CAPACITY;
     if (fused && (V + kGemmBN - 1) / kGemmBN > kMergeMaxTiles) return EAGLE_ERR_SHAPE;
-    if (B == 0) return EAGLE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int R = 1 + (depth - 1) * top_k;
     const int k_in = level == 1 ? 1 : top_k;
@@ -815,7 +818,7 @@ extern "C" eagle_status eagle2_expand_d2t(int level, int final, const void* hidd
                                           int32_t* out_tokens, int32_t* out_parent,
                                           int32_t* out_draft_row, int32_t* frontier_tokens,
                                           int32_t* dev_status, eagle_stream_t stream) {
-    if (!d2t) return EAGLE_ERR_INVALID_ARG;
+    if (B != 0 && !d2t) return EAGLE_ERR_INVALID_ARG;
     return expand_common(level, final, hidden, lm_head_w, logits, B, H, V, top_k, depth, n_out,
                          tree_state, state_bytes, partials, partials_bytes, d2t, out_tokens,
                          out_parent, out_draft_row, frontier_tokens, dev_status, stream);
@@ -826,10 +829,11 @@ extern "C" eagle_status eagle2_tree_candidates(const void* tree_state, size_t st
                                                int32_t* token, int32_t* parent,
                                                int32_t* cand_depth, int32_t* draft_row,
                                                eagle_stream_t stream) {
-    if (B < 0 || top_k < 1 || depth < 1 || !tree_state) return EAGLE_ERR_INVALID_ARG;
+    if (B < 0 || top_k < 1 || depth < 1) return EAGLE_ERR_INVALID_ARG;
     if (top_k > kKMax || depth > kDepthMax) return EAGLE_ERR_SHAPE;
+    if (B == 0) return EAGLE_OK;                        // nothing read or written
+    if (!tree_state) return EAGLE_ERR_INVALID_ARG;
     if (state_bytes < eagle2_tree_state_size(B, top_k, depth)) return EAGLE_ERR_CAPACITY;
-    if (B == 0) return EAGLE_OK;
     const int C = StateView::cand_count(top_k, depth);
     const dim3 grid((C + 255) / 256, B);
     tree_candidates_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
@@ -889,6 +893,7 @@ extern "C" eagle_status eagle2_expand_static_state(int level, int final, const v
                                             out_draft_row);
     if (vs != EAGLE_OK) return vs;
     if (eagle2_tree_state_size(B, top_k, depth) > kStaticStateBytes) return EAGLE_ERR_CAPACITY;
+    if (B == 0) return EAGLE_OK;                        // no device call for an empty batch
     void* state = nullptr;
     const eagle_status st = static_state_address(&state);
     if (st != EAGLE_OK) return st;
@@ -1036,11 +1041,10 @@ extern "C" eagle_status eagle_static_tree_level(int level, const float* logits, 
                                                 const int32_t* draft_row, int n, int B, int R, int V,
                                                 int32_t* tokens, int32_t* dev_status,
                                                 eagle_stream_t stream) {
-    if (!logits || !parent || !rank || !depth || !draft_row || !tokens || level < 1 || B < 0 ||
-        R < 1 || V < 1 || n < 1)
-        return EAGLE_ERR_INVALID_ARG;
+    if (level < 1 || B < 0 || R < 1 || V < 1 || n < 1) return EAGLE_ERR_INVALID_ARG;
     if (n > kMaxNodes) return EAGLE_ERR_SHAPE;
-    if (B == 0) return EAGLE_OK;
+    if (B == 0) return EAGLE_OK;                        // nothing read or written
+    if (!logits || !parent || !rank || !depth || !draft_row || !tokens) return EAGLE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     static_tree_level_kernel<<<dim3((unsigned)n, (unsigned)B), kTopkThreads, 0, s>>>(
         level, logits, parent, rank, depth, draft_row, n, R, V, tokens, dev_status);

@@ -103,12 +103,12 @@ extern "C" eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* 
                                          int n_layers, int B, int Hkv, int head_dim, int Lmax,
                                          int max_depth, int32_t* dev_status,
                                          eagle_stream_t stream) {
-    if (!k_cache || !v_cache || !kv_len || !path || !accept_len) return EAGLE_ERR_INVALID_ARG;
     if (n_layers < 0 || B < 0 || Hkv < 1 || Lmax < 1 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
     if (head_dim != kHeadDim || max_depth > kMaxNodes) return EAGLE_ERR_SHAPE;
+    if (B == 0 || n_layers == 0) return EAGLE_OK;       // nothing read or written
+    if (!k_cache || !v_cache || !kv_len || !path || !accept_len) return EAGLE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(k_cache) & 15) || (reinterpret_cast<uintptr_t>(v_cache) & 15))
         return EAGLE_ERR_INVALID_ARG;
-    if (B == 0 || n_layers == 0) return EAGLE_OK;
     CompactArgs a{static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache), kv_len, path,
                   accept_len, n_layers, B, Hkv, Lmax, max_depth, dev_status};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

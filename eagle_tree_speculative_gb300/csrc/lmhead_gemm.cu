@@ -244,11 +244,13 @@ eagle_status lmhead_gemm_launch(const void* hidden, const void* w, float* out, i
                                 int64_t ldo, int rows_per_group, int64_t group_stride,
                                 int64_t row_offset, int32_t* dev_status, cudaStream_t stream,
                                 float* part) {
-    if (part && (reinterpret_cast<uintptr_t>(part) & 7)) return EAGLE_ERR_INVALID_ARG;
-    if (!hidden || !w || !out || M < 1 || N < 1 || K < BK || rows_per_group < 1 || ldo < N ||
-        group_stride < 0 || row_offset < 0)
+    if (M < 0 || N < 1 || K < BK || rows_per_group < 1 || ldo < N || group_stride < 0 ||
+        row_offset < 0)
         return EAGLE_ERR_INVALID_ARG;
     if (K % BK != 0) return EAGLE_ERR_SHAPE;
+    if (M == 0) return EAGLE_OK;                        // nothing read or written
+    if (!hidden || !w || !out) return EAGLE_ERR_INVALID_ARG;
+    if (part && (reinterpret_cast<uintptr_t>(part) & 7)) return EAGLE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(hidden) & 15) || (reinterpret_cast<uintptr_t>(w) & 15) ||
         (reinterpret_cast<uintptr_t>(out) & 3))
         return EAGLE_ERR_INVALID_ARG;

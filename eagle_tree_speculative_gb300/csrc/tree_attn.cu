@@ -110,12 +110,12 @@ extern "C" eagle_status eagle_tree_attn(const void* q, const void* k_cache, cons
                                         int B, int n, int Hq, int Hkv, int head_dim, int Lmax,
                                         float scale, void* workspace, size_t ws_bytes,
                                         int32_t* dev_status, eagle_stream_t stream) {
-    if (!q || !k_cache || !v_cache || !kv_len || !parent || !out) return EAGLE_ERR_INVALID_ARG;
     if (B < 0 || n < 1 || Hq < 1 || Hkv < 1 || Lmax < 1 || !(scale > 0.f)) return EAGLE_ERR_INVALID_ARG;
     if (n > kMaxNodes || head_dim != kHeadDim || Hq % Hkv != 0 || Lmax < n) return EAGLE_ERR_SHAPE;
+    if (B == 0) return EAGLE_OK;                        // nothing read or written
+    if (!q || !k_cache || !v_cache || !kv_len || !parent || !out) return EAGLE_ERR_INVALID_ARG;
     for (const void* p : {q, k_cache, v_cache, (const void*)out})
         if (reinterpret_cast<uintptr_t>(p) & 15) return EAGLE_ERR_INVALID_ARG;
-    if (B == 0) return EAGLE_OK;
     const int splits = tc_splits(B, n, Hq, Hkv, Lmax);
     const size_t need = splits > 1 ? (size_t)splits * B * n * Hq * (kHeadDim + 2) * sizeof(float) : 0;
     if (need > 0 && (!workspace || ws_bytes < need)) return EAGLE_ERR_CAPACITY;

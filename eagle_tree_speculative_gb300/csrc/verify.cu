@@ -1476,13 +1476,14 @@ eagle_status verify_common(const float* target_logits, const float* draft_logits
     if (B < 0 || n < 1 || V < 1 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
     if (n > kMaxNodes || max_depth > kMaxNodes) return EAGLE_ERR_SHAPE;
     if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
+    if (temperature > 0.f && R < 1) return EAGLE_ERR_INVALID_ARG;
+    if (B == 0) return EAGLE_OK;                        // nothing read or written
     if (!target_logits || !tokens || !parent || !accept_len || !path || !emit)
         return EAGLE_ERR_INVALID_ARG;
     if (temperature > 0.f) {
-        if (!draft_logits || R < 1) return EAGLE_ERR_INVALID_ARG;
+        if (!draft_logits) return EAGLE_ERR_INVALID_ARG;
         if (!draft_row && R != n) return EAGLE_ERR_SHAPE;
     }
-    if (B == 0) return EAGLE_OK;
     const float c = temperature > 0.f ? kLog2e / temperature : 0.f;
     VerifyArgs a{target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, max_depth,
                  temperature, c, seed, accept_len, path, emit, row_stats, dev_status, Vd, t2d,
@@ -1541,17 +1542,20 @@ extern "C" eagle_status eagle_verify_accept_sharded(
     if (B < 0 || n < 1 || V < 1 || max_depth < 0) return EAGLE_ERR_INVALID_ARG;
     if (n > kMaxNodes || max_depth > kMaxNodes) return EAGLE_ERR_SHAPE;
     if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
-    if (!tokens || !parent || !accept_len || !path || !emit) return EAGLE_ERR_INVALID_ARG;
     if (shard_begin[0] != 0 || shard_begin[S] != V) return EAGLE_ERR_SHAPE;
+    for (int r = 0; r < S; ++r)
+        if (shard_begin[r + 1] <= shard_begin[r]) return EAGLE_ERR_SHAPE;     // empty shard
     const bool t_pos = temperature > 0.f;
+    if (t_pos && R < 1) return EAGLE_ERR_INVALID_ARG;
+    if (B == 0) return EAGLE_OK;                        // nothing read or written
+    if (!tokens || !parent || !accept_len || !path || !emit) return EAGLE_ERR_INVALID_ARG;
     if (t_pos) {
-        if (!draft_shards || R < 1) return EAGLE_ERR_INVALID_ARG;
+        if (!draft_shards) return EAGLE_ERR_INVALID_ARG;
         if (!draft_row && R != n) return EAGLE_ERR_SHAPE;
     }
     VerifyArgs a{};
     bool vec4 = (V & 3) == 0;
     for (int r = 0; r < S; ++r) {
-        if (shard_begin[r + 1] <= shard_begin[r]) return EAGLE_ERR_SHAPE;     // empty shard
         if (!target_shards[r] || (t_pos && !draft_shards[r])) return EAGLE_ERR_INVALID_ARG;
         a.sh.tgt[r] = target_shards[r];
         a.sh.drf[r] = t_pos ? draft_shards[r] : nullptr;
@@ -1561,7 +1565,6 @@ extern "C" eagle_status eagle_verify_accept_sharded(
                (!t_pos || (reinterpret_cast<uintptr_t>(draft_shards[r]) & 15) == 0);
     }
     a.sh.begin[S] = V;
-    if (B == 0) return EAGLE_OK;
     a.target = target_shards[0];
     a.draft = t_pos ? draft_shards[0] : nullptr;
     a.draft_row = draft_row;
@@ -1596,7 +1599,7 @@ extern "C" eagle_status eagle_verify_accept_d2t(const float* target_logits, cons
                                                 int32_t* accept_len, int32_t* path, int32_t* emit,
                                                 float* row_stats, int32_t* dev_status,
                                                 eagle_stream_t stream) {
-    if (Vd < 1 || !t2d) return EAGLE_ERR_INVALID_ARG;
+    if (Vd < 1 || (B != 0 && !t2d)) return EAGLE_ERR_INVALID_ARG;
     return verify_common(target_logits, draft_logits, draft_row, tokens, parent, B, n, V, R, Vd, t2d,
                          max_depth, temperature, seed, accept_len, path, emit, row_stats, dev_status,
                          stream);
@@ -1657,12 +1660,13 @@ extern "C" eagle_status eagle_softmax_stats(const float* logits, int64_t rows, i
                                             float temperature, float* row_max, float* row_sum,
                                             int32_t* row_argmax, int32_t* dev_status,
                                             eagle_stream_t stream) {
-    if (!logits || rows < 0 || V < 1) return EAGLE_ERR_INVALID_ARG;
+    if (rows < 0 || V < 1) return EAGLE_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || !(temperature < INFINITY)) return EAGLE_ERR_INVALID_ARG;
+    if (rows == 0) return EAGLE_OK;                     // nothing read or written
     const bool stats = temperature > 0.f;
+    if (!logits) return EAGLE_ERR_INVALID_ARG;
     if (stats && (!row_max || !row_sum)) return EAGLE_ERR_INVALID_ARG;
     if (!stats && !row_argmax) return EAGLE_ERR_INVALID_ARG;
-    if (rows == 0) return EAGLE_OK;
     const float c = stats ? kLog2e / temperature : 0.f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // One resident wave: every CTA of the grid is on an SM from the start (the variants

@@ -32,6 +32,11 @@
  *     Calls only enqueue work; results are ready when the stream is.
  *   - Host-checkable errors (bad sizes, NULL pointers, unsupported shapes) return
  *     a non-zero eagle_status and launch nothing.
+ *   - An empty batch (B == 0; rows == 0 or M == 0 for the row-wise calls;
+ *     n_layers == 0 for compaction) is a no-op: once the sizes and scalars pass
+ *     their checks the call returns EAGLE_OK without touching the device, and its
+ *     device pointers may be NULL (host tables such as shard bounds are still
+ *     checked).
  *   - Errors only visible in device data never trap: the kernel skips the
  *     affected sequence (accept_len = -1 where there is one), and ORs an
  *     EAGLE_DEV_* bit into *dev_status (an int32 in device memory the caller
@@ -270,8 +275,7 @@ eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, con
  *   out  bf16 [B, S, Hq, head_dim]
  * Sizes: S >= 1, 1 <= R1 <= 16, 0 <= r < R1, head_dim == 128, Hq % Hkv == 0,
  * B * Hkv * ceil(S * Hq / Hkv / 128) < 2^31.  Every row of round 0 must be finite (rows
- * past a query's position are read and masked).  All pointers 16-byte aligned;
- * with B == 0 nothing is read or written and they may be NULL.
+ * past a query's position are read and masked).  All pointers 16-byte aligned.
  * Device errors: a wait that exceeds its limit sets EAGLE_DEV_TIMEOUT.
  * ------------------------------------------------------------------------- */
 eagle_status eagle_ttt_attn(const void* q, const void* k, const void* v, void* out, int B, int S,

@@ -146,3 +146,53 @@ def test_static_state_entry_reports_the_same_argument_errors(lib_path):
                None, None)
         b = st(lvl, fin, None, None, p, B, 0, V, k, D, n, p, p, p, None, None, None)
         assert a == b and a != 0, (lvl, fin, B, V, k, D, n, a, b)
+
+
+def test_every_call_treats_an_empty_batch_as_a_no_op(lib_path):
+    """B == 0 (rows == 0, M == 0, n_layers == 0) with valid sizes returns OK before any
+    device work, with every device pointer NULL; the same sizes with B = 1 and NULL
+    pointers are refused, so the no-op is the empty batch's, not a missing check."""
+    from eagle_tree_speculative_gb300 import _lib
+    L = ctypes.CDLL(lib_path)
+    for name, (res, args) in _lib.SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype, fn.argtypes = res, args
+    OK, INVALID = 0, 1
+    N = None
+    begin = (ctypes.c_int * 3)(0, 300, 1000)
+    shards = (ctypes.c_void_p * 2)(None, None)
+    calls = {
+        # q k v kv_len parent out | B n Hq Hkv d Lmax scale | ws ws_bytes status stream
+        "eagle_tree_attn": lambda B: L.eagle_tree_attn(N, N, N, N, N, N, B, 60, 32, 8, 128, 4156,
+                                                       0.088, N, 0, N, N),
+        "eagle_ttt_attn": lambda B: L.eagle_ttt_attn(N, N, N, N, B, 64, 4, 2, 128, 3, 1, 0.1, N, N),
+        # tgt drf row tok par | B n V R D T seed | acc path emit stats status stream
+        "eagle_verify_accept": lambda B: L.eagle_verify_accept(N, N, N, N, N, B, 60, 1000, 60, 8,
+                                                               1.0, 0, N, N, N, N, N, N),
+        "eagle_verify_accept_d2t": lambda B: L.eagle_verify_accept_d2t(
+            N, N, N, N, N, B, 60, 1000, 60, 500, N, 8, 1.0, 0, N, N, N, N, N, N),
+        "eagle_verify_accept_filtered": lambda B: L.eagle_verify_accept_filtered(
+            N, N, N, N, N, B, 60, 1000, 60, 8, 1.0, 0, 20, 0.9, N, N, N, N, N, 0, N, N),
+        "eagle_verify_accept_sharded": lambda B: L.eagle_verify_accept_sharded(
+            shards, shards, begin, 2, N, N, N, B, 60, 1000, 60, 8, 1.0, 0, N, N, N, N, N, N),
+        # k v kv_len path acc | n_layers B Hkv d Lmax D | status stream
+        "eagle_kv_compact": lambda B: L.eagle_kv_compact(N, N, N, N, N, 32, B, 8, 128, 4160, 8,
+                                                         N, N),
+        # level final hidden w logits B H V k D n_out state bytes partials bytes out... status stream
+        "eagle2_expand": lambda B: L.eagle2_expand(3, 1, N, N, N, B, 0, 1000, 10, 3, 60, N, 0, N, 0,
+                                                   N, N, N, N, N, N),
+        "eagle2_expand_d2t": lambda B: L.eagle2_expand_d2t(3, 1, N, N, N, B, 0, 1000, 10, 3, 60, N,
+                                                           0, N, 0, N, N, N, N, N, N, N),
+        "eagle2_expand_static_state": lambda B: L.eagle2_expand_static_state(
+            3, 1, N, N, N, B, 0, 1000, 10, 3, 60, N, N, N, N, N, N),
+        "eagle2_tree_candidates": lambda B: L.eagle2_tree_candidates(N, 0, B, 10, 3, N, N, N, N, N,
+                                                                     N, N),
+        "eagle_static_tree_level": lambda B: L.eagle_static_tree_level(2, N, N, N, N, N, 26, B, 26,
+                                                                       1000, N, N, N),
+        "eagle_softmax_stats": lambda B: L.eagle_softmax_stats(N, B, 1000, 1.0, N, N, N, N, N),
+        "eagle_lmhead_gemm": lambda B: L.eagle_lmhead_gemm(N, N, N, B, 4096, 1000, 1000, 1, 0, 0,
+                                                           N, N, N),
+    }
+    for name, call in calls.items():
+        assert call(0) == OK, name
+        assert call(1) == INVALID, name

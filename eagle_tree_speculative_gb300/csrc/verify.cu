@@ -463,8 +463,8 @@ __device__ __forceinline__ KeyIdx race_slice(const float* qrow, PRow<D2T> prow, 
 }
 
 // ---------------------------------------------------------------------------
-// Row filters for the filtered walk (top-k, then top-p over what top-k kept): one CTA
-// per row, computed when the walk reaches the row's node (or its parent).  The cut is
+// Row filters for the filtered walk (top-k, then top-p over what top-k kept) on one CTA:
+// the rows that the cluster-wide filter below leaves over.  The cut is
 // usually found from a histogram over distance bins and an exact sort of the elements
 // up to the cut; otherwise by a radix select over the rows' order keys (11-bit digits,
 // most significant first).  Both keep per-bin counts and fixed-point masses
@@ -937,15 +937,496 @@ __device__ void filter_row(FiltSmem& sm, const float* __restrict__ x, int V, flo
 }
 
 // ---------------------------------------------------------------------------
+// The filters of the walk's current rows, q(v) and (when v has children) p(v),
+// computed by the whole cluster: each CTA reads only its slice [lo, hi) of each row and
+// the slices' partial results meet in distributed shared memory.
+//   1. the maximum and the non-finite check: one value per CTA and row;
+//   2. the counts and fixed-point masses of the distance bins within 4 log2 units of
+//      the maximum, merged bin by bin (and, for top-p alone, the row's total mass);
+//   3. the bin holding the top-k cut (without top-k, the top-p cut), found by every CTA
+//      from the merged histogram;
+//   4. the elements of that bin and the bins before it, gathered by each CTA from its
+//      slice, copied by every CTA from all of them and sorted (key desc, index asc); the
+//      cuts and the kept mass S follow from the sorted list.
+// The bins, the integer masses and the order are filter_row's, so the kept sets are the
+// same.  A row whose near bins do not reach the cut, or with more than kDCand elements
+// up to the cut bin (kDLocal in one slice), is filtered by filter_row on one CTA.
+// ---------------------------------------------------------------------------
+constexpr int kDBins = kNearBins;
+constexpr int kDLocal = 1024;                  // one CTA's candidates of one row
+constexpr int kDCand = 1024;                   // all candidates of one row
+static_assert(kDBins == kFiltThreads, "one bin per thread in the merge");
+
+struct DFiltSmem {
+    unsigned int hc[2][kDBins];                // this CTA's bin counts (read by the cluster)
+    unsigned long long hm[2][kDBins];          // and fixed-point masses
+    unsigned long long tot[2];                 // this CTA's total mass (top-p alone)
+    int lcnt[2];                               // this CTA's candidates
+    unsigned long long lk[2][kDLocal];
+    unsigned int gc[2][kDBins];                // merged bins
+    unsigned long long gm[2][kDBins];
+    unsigned long long tot_all[2];
+    unsigned long long sk[2][kDCand];          // all candidates, sorted
+    int ncand[2];
+    int cutbin[2];
+    int fb[2];                                 // 1: the row goes to filter_row
+    FilterParam res[2];                        // the fast path's results, for every thread
+};
+
+__device__ __forceinline__ void hist_add_d(DFiltSmem& ds, int r, int bin, unsigned long long m) {
+    atomicAdd(&ds.hc[r][bin], 1u);
+    if (m) add_u64_split(&ds.hm[r][bin], m);
+}
+
+// One element of row r in the near-bin histogram (and, for top-p alone, the row's mass).
+// d = (max - l) c is dist_bin's distance; d * 64 is exact, so bin < kDBins exactly when
+// d < kDBins / 64, and only those elements convert d to their bin.
+__device__ __forceinline__ void near_hist(DFiltSmem& ds, int r, float l, float lm, float c,
+                                          bool need_total, unsigned long long& tm) {
+    const float d = (lm - l) * c;
+    unsigned long long m = 0ull;
+    if (need_total) {
+        m = fixed_mass(l, lm, c);
+        tm += m;
+    }
+    if (d < (float)kDBins / 64.f) hist_add_d(ds, r, (int)(d * 64.f), m);   // m = 0 with top-k
+}
+
+// Element t of row r into the CTA's candidate list when its bin is at most the cut bin:
+// dist_bin(l) <= cbin exactly when d < (cbin + 1) / 64 = dlim.
+__device__ __forceinline__ void gather_elem(DFiltSmem& ds, int r, int t, float l, float lm, float c,
+                                            float dlim) {
+    if ((lm - l) * c < dlim) {
+        const int pos = atomicAdd(&ds.lcnt[r], 1);
+        if (pos < kDLocal)
+            ds.lk[r][pos] = ((unsigned long long)order_key(l) << 32) | (unsigned long long)(~(uint32_t)t);
+    }
+}
+
+union FiltScratch {
+    FiltSmem one;
+    DFiltSmem dist;
+};
+
+// f0(t, x0[t]) and, when two, f1(t, x1[t]) for t in [lo, hi), NT threads; with vec4 (lo
+// and hi multiples of 4, rows 16-byte aligned) four float4 of each row in flight per
+// thread.
+template <int NT, class F0, class F1>
+__device__ __forceinline__ void slice_for_each2(const float* __restrict__ x0, const float* __restrict__ x1,
+                                                bool two, int lo, int hi, bool vec4, F0&& f0, F1&& f1) {
+    const int tid = threadIdx.x;
+    if (vec4) {
+        int t = lo + 4 * tid;
+        for (; t + 12 * NT < hi; t += 16 * NT) {
+            float4 w0[4], w1[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w0[u] = __ldg(reinterpret_cast<const float4*>(x0 + t + 4 * u * NT));
+            if (two) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) w1[u] = __ldg(reinterpret_cast<const float4*>(x1 + t + 4 * u * NT));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int tu = t + 4 * u * NT;
+                f0(tu, w0[u].x); f0(tu + 1, w0[u].y); f0(tu + 2, w0[u].z); f0(tu + 3, w0[u].w);
+            }
+            if (two) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int tu = t + 4 * u * NT;
+                    f1(tu, w1[u].x); f1(tu + 1, w1[u].y); f1(tu + 2, w1[u].z); f1(tu + 3, w1[u].w);
+                }
+            }
+        }
+        for (; t < hi; t += 4 * NT) {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(x0 + t));
+            f0(t, w.x); f0(t + 1, w.y); f0(t + 2, w.z); f0(t + 3, w.w);
+            if (two) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(x1 + t));
+                f1(t, v.x); f1(t + 1, v.y); f1(t + 2, v.z); f1(t + 3, v.w);
+            }
+        }
+    } else {
+        for (int t = lo + tid; t < hi; t += NT) {
+            f0(t, x0[t]);
+            if (two) f1(t, x1[t]);
+        }
+    }
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sorts s[0 .. n) descending into d[0 .. n) by rank (the keys are distinct): thread
+// `first + i` places element i; `count` threads take part, n <= count.
+__device__ __forceinline__ void rank_sort(const unsigned long long* s, unsigned long long* d, int n,
+                                          int first, int count) {
+    const int i = (int)threadIdx.x - first;
+    if (i < 0 || i >= count || i >= n) return;
+    const unsigned long long e = s[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += s[j] > e;
+    d[r] = e;
+}
+
+// Bitonic sort of s[0 .. n) descending (pads to a power of two with zeros, which sort
+// last); every thread of the CTA takes part.
+template <int NT>
+__device__ void sort_desc(unsigned long long* s, int n) {
+    const int tid = threadIdx.x;
+    int n2 = 1;
+    while (n2 < n) n2 <<= 1;
+    for (int j = n + tid; j < n2; j += NT) s[j] = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < n2; i += NT) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long x = s[i], y = s[j];
+                    if (desc ? (x < y) : (x > y)) { s[i] = y; s[j] = x; }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int CS, int NT>
+__device__ void cluster_filters(VerifySmem<NT>& sm, FiltScratch& fsc, int& buf, int rank,
+                                const float* const rows[2], int nr, int lo, int hi, bool vec4, int V,
+                                float c, int top_k, float top_p, FilterParam* const slots[2],
+                                const bool prefetch[2], FilterParam out[2]) {
+    static_assert(NT == kFiltThreads, "the row filter takes the whole CTA");
+    using C = Cluster<CS, NT>;
+    DFiltSmem& ds = fsc.dist;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool do_k = top_k > 0 && top_k < V;
+    const bool do_p = top_p > 0.f && top_p < 1.f;
+    const bool need_total = do_p && !do_k;
+    const bool two = nr > 1;
+    const float* const x0 = rows[0];
+    const float* const x1 = two ? rows[1] : rows[0];
+    auto remote = [&](int rk) -> const DFiltSmem* {
+        if constexpr (CS > 1) return cg::this_cluster().map_shared_rank(&ds, rk);
+        else return &ds;
+    };
+
+    // ---- 1. maxima and the non-finite check (the slices first go to L2 in bulk) ----
+    if (vec4 && tid < 2 && (tid == 0 || two) && prefetch[tid] && hi > lo) {
+        const char* base = reinterpret_cast<const char*>(tid == 0 ? x0 : x1) + (int64_t)lo * 4;
+        for (int64_t o = 0; o < (int64_t)(hi - lo) * 4; o += 65536) {
+            const int64_t left = (int64_t)(hi - lo) * 4 - o;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(base + o),
+                         "r"((uint32_t)(left < 65536 ? left : 65536))
+                         : "memory");
+        }
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+    int bd = 0;
+    slice_for_each2<NT>(
+        x0, x1, two, lo, hi, vec4,
+        [&](int, float l) { bd |= (l != l) | (l == INFINITY); mx0 = fmaxf(mx0, l); },
+        [&](int, float l) { bd |= ((l != l) | (l == INFINITY)) << 1; mx1 = fmaxf(mx1, l); });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        bd |= __shfl_xor_sync(0xffffffffu, bd, o);
+    }
+    if (lane == 0) { sm.red[warp][0] = mx0; sm.red[warp][1] = mx1; sm.redbad[warp] = bd; }
+    __syncthreads();
+    if (tid == 0) {
+        float a0 = -INFINITY, a1 = -INFINITY;
+        int b0 = 0;
+        for (int w = 0; w < NT / 32; ++w) {
+            a0 = fmaxf(a0, sm.red[w][0]);
+            a1 = fmaxf(a1, sm.red[w][1]);
+            b0 |= sm.redbad[w];
+        }
+        sm.x[buf].f[0] = a0;
+        sm.x[buf].f[1] = a1;
+        sm.x[buf].bad = b0;
+    }
+    C::sync();
+    if (warp == 0) {
+        Slot mine{};
+        if (lane < CS) mine = *C::slot(sm, buf, lane);
+        float a0 = -INFINITY, a1 = -INFINITY;
+        int b0 = 0;
+        for (int r = 0; r < CS; ++r) {
+            a0 = fmaxf(a0, __shfl_sync(0xffffffffu, mine.f[0], r));
+            a1 = fmaxf(a1, __shfl_sync(0xffffffffu, mine.f[1], r));
+            b0 |= __shfl_sync(0xffffffffu, mine.bad, r);
+        }
+        if (lane == 0) { sm.bc.f[0] = a0; sm.bc.f[1] = a1; sm.bc.bad = b0; }
+    }
+    __syncthreads();
+    const float lmax0 = sm.bc.f[0], lmax1 = sm.bc.f[1];
+    const int bad = sm.bc.bad;
+    buf ^= 1;
+    bool live[2];
+    live[0] = !(bad & 1) && lmax0 != -INFINITY;
+    live[1] = two && !(bad & 2) && lmax1 != -INFINITY;
+    if (!live[0]) out[0] = FilterParam{lmax0, 0.f, 0u, 0, 1, 0, 0, 0};
+    if (two && !live[1]) out[1] = FilterParam{lmax1, 0.f, 0u, 0, 1, 0, 0, 0};
+    if (!live[0] && !live[1]) return;
+
+    // ---- 2. near-bin histograms of the slice ----
+    for (int i = tid; i < 2 * kDBins; i += NT) {
+        (&ds.hc[0][0])[i] = 0u;
+        (&ds.hm[0][0])[i] = 0ull;
+    }
+    if (tid < 2) { ds.tot[tid] = 0ull; ds.lcnt[tid] = 0; }
+    __syncthreads();
+    unsigned long long tm0 = 0ull, tm1 = 0ull;
+    const bool l0 = live[0], l1 = live[1];
+    {
+        // the first row iterated is q unless only p is live
+        const int ra = l0 ? 0 : 1;
+        const float lma = l0 ? lmax0 : lmax1;
+        slice_for_each2<NT>(
+            l0 ? x0 : x1, x1, l0 && l1, lo, hi, vec4,
+            [&](int, float l) { near_hist(ds, ra, l, lma, c, need_total, tm0); },
+            [&](int, float l) { near_hist(ds, 1, l, lmax1, c, need_total, tm1); });
+        if (!l0) { tm1 = tm0; tm0 = 0ull; }
+    }
+    if (need_total) {
+        tm0 = warp_sum_u64(tm0);
+        tm1 = warp_sum_u64(tm1);
+        if (lane == 0) {
+            if (tm0) add_u64_split(&ds.tot[0], tm0);
+            if (tm1) add_u64_split(&ds.tot[1], tm1);
+        }
+    }
+    __syncthreads();
+    C::sync();
+    for (int r = 0; r < 2; ++r) {
+        if (!live[r]) continue;
+        unsigned int cnt = 0u;
+        unsigned long long m = 0ull;
+        unsigned int hcs[CS];
+#pragma unroll
+        for (int rk = 0; rk < CS; ++rk) hcs[rk] = remote(rk)->hc[r][tid];
+#pragma unroll
+        for (int rk = 0; rk < CS; ++rk) cnt += hcs[rk];
+        if (need_total) {
+            unsigned long long hms[CS];
+#pragma unroll
+            for (int rk = 0; rk < CS; ++rk) hms[rk] = remote(rk)->hm[r][tid];
+#pragma unroll
+            for (int rk = 0; rk < CS; ++rk) m += hms[rk];
+        }
+        ds.gc[r][tid] = cnt;
+        ds.gm[r][tid] = m;
+        if (tid == 0 && need_total) {
+            unsigned long long t = 0ull;
+            for (int rk = 0; rk < CS; ++rk) t += remote(rk)->tot[r];
+            ds.tot_all[r] = t;
+        }
+    }
+    __syncthreads();
+
+    // ---- 3. the cut bin: warp r scans row r's bins, eight per lane ----
+    if (warp < 2) {
+        const int r = warp;
+        int fb = 1, cb = 0;
+        if (live[r]) {
+            unsigned int lc = 0u;
+            unsigned long long lm = 0ull;
+#pragma unroll
+            for (int j = 0; j < kDBins / 32; ++j) {
+                lc += ds.gc[r][lane * (kDBins / 32) + j];
+                lm += ds.gm[r][lane * (kDBins / 32) + j];
+            }
+            unsigned int ic = lc;
+            unsigned long long im = lm;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned int yc = __shfl_up_sync(0xffffffffu, ic, o);
+                const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, o);
+                if (lane >= o) { ic += yc; im += ym; }
+            }
+            const unsigned int near_cnt = __shfl_sync(0xffffffffu, ic, 31);
+            const unsigned long long near_mass = __shfl_sync(0xffffffffu, im, 31);
+            unsigned long long target;
+            bool enough;
+            if (do_k) {
+                target = (unsigned long long)top_k;
+                enough = near_cnt >= (unsigned int)top_k;
+            } else {
+                const unsigned long long tot = ds.tot_all[r];
+                target = (unsigned long long)ceil((double)top_p * (double)tot);
+                target = target < 1ull ? 1ull : (target > tot ? tot : target);
+                enough = near_mass >= target;
+            }
+            if (enough) {
+                // the lane whose bins the running metric crosses the target in
+                const unsigned long long before = do_k ? (unsigned long long)(ic - lc) : im - lm;
+                const unsigned long long mine = do_k ? (unsigned long long)lc : lm;
+                const bool here = before < target && before + mine >= target;
+                const unsigned int who = __ballot_sync(0xffffffffu, here);
+                const int src = who ? __ffs(who) - 1 : 0;
+                int bin = 0;
+                unsigned int cnt_before = 0u;
+                if (lane == src) {
+                    unsigned long long run = before;
+                    unsigned int cbf = ic - lc;
+                    for (int j = 0; j < kDBins / 32; ++j) {
+                        const int bj = lane * (kDBins / 32) + j;
+                        const unsigned long long v = do_k ? (unsigned long long)ds.gc[r][bj] : ds.gm[r][bj];
+                        if (run + v >= target) { bin = bj; break; }
+                        run += v;
+                        cbf += ds.gc[r][bj];
+                    }
+                    cnt_before = cbf;
+                }
+                bin = __shfl_sync(0xffffffffu, bin, src);
+                cnt_before = __shfl_sync(0xffffffffu, cnt_before, src);
+                cb = bin;
+                fb = (!who || cnt_before + ds.gc[r][bin] > (unsigned int)kDCand) ? 1 : 0;
+            }
+        }
+        if (lane == 0) { ds.cutbin[r] = cb; ds.fb[r] = live[r] ? fb : 0; }
+    }
+    __syncthreads();
+    bool go[2];
+    for (int r = 0; r < 2; ++r) go[r] = live[r] && !ds.fb[r];
+
+    // ---- 4. candidates: every element up to the cut bin, gathered from the slice ----
+    // (a few per slice with top-k: one shared atomic each)
+    {
+        const bool r0 = go[0], r1 = go[1];
+        const int ra = r0 ? 0 : 1;
+        const float lma = r0 ? lmax0 : lmax1;
+        const float dla = (float)(ds.cutbin[ra] + 1) / 64.f, dl1 = (float)(ds.cutbin[1] + 1) / 64.f;
+        if (r0 || r1)
+            slice_for_each2<NT>(
+                r0 ? x0 : x1, x1, r0 && r1, lo, hi, vec4,
+                [&](int t, float l) { gather_elem(ds, ra, t, l, lma, c, dla); },
+                [&](int t, float l) { gather_elem(ds, 1, t, l, lmax1, c, dl1); });
+        __syncthreads();
+        C::sync();
+    }
+    // every CTA copies the elements up to the cut bin from all lists, in rank order
+    if (tid < 2) ds.ncand[tid] = 0;
+    __syncthreads();
+    for (int r = 0; r < 2; ++r) {
+        if (!go[r]) continue;
+        int ks[CS];
+        int total = 0;
+        bool over = false;
+#pragma unroll
+        for (int rk = 0; rk < CS; ++rk) ks[rk] = remote(rk)->lcnt[r];
+#pragma unroll
+        for (int rk = 0; rk < CS; ++rk) {
+            over = over || ks[rk] > kDLocal;
+            total += ks[rk];
+        }
+        if (over || total > kDCand) {              // the same decision in every thread and CTA
+            go[r] = false;
+            if (tid == 0) ds.fb[r] = 1;
+            continue;
+        }
+        int off = 0;
+#pragma unroll
+        for (int rk = 0; rk < CS; ++rk) {
+            const DFiltSmem* o = remote(rk);
+            for (int j = tid; j < ks[rk]; j += NT) ds.sk[r][off + j] = o->lk[r][j];
+            off += ks[rk];
+        }
+        if (tid == 0) ds.ncand[r] = total;
+    }
+    __syncthreads();
+    // short lists: rank sort, half the CTA per row, into the upper half of sk
+    int soff[2] = {0, 0};
+    const bool small0 = go[0] && ds.ncand[0] <= NT / 2, small1 = go[1] && ds.ncand[1] <= NT / 2;
+    if (small0) rank_sort(ds.sk[0], ds.sk[0] + kDCand / 2, ds.ncand[0], 0, NT / 2);
+    if (small1) rank_sort(ds.sk[1], ds.sk[1] + kDCand / 2, ds.ncand[1], NT / 2, NT / 2);
+    if (small0) soff[0] = kDCand / 2;
+    if (small1) soff[1] = kDCand / 2;
+    __syncthreads();
+    for (int r = 0; r < 2; ++r)
+        if (go[r] && !(r == 0 ? small0 : small1)) sort_desc<NT>(ds.sk[r], min(ds.ncand[r], kDCand));
+
+    // ---- cuts and kept mass: warp r for row r ----
+    if (warp < 2 && go[warp]) {
+        const int r = warp;
+        const int nc = min(ds.ncand[r], kDCand);
+        const float lm = r == 0 ? lmax0 : lmax1;
+        const unsigned long long* s = ds.sk[r] + soff[r];
+        auto fm = [&](int j) { return fixed_mass(key_float((uint32_t)(s[j] >> 32)), lm, c); };
+        int cut = nc - 1;                          // without top-k everything gathered may stay
+        unsigned long long total = ds.tot_all[r];
+        if (do_k) {
+            cut = top_k - 1;
+            unsigned long long t = 0ull;
+            for (int j = lane; j < top_k; j += 32) t += fm(j);
+            total = warp_sum_u64(t);
+        }
+        if (do_p) {
+            unsigned long long tgt = (unsigned long long)ceil((double)top_p * (double)total);
+            tgt = tgt < 1ull ? 1ull : (tgt > total ? total : tgt);
+            // the first j (at most cut) whose running mass reaches tgt
+            unsigned long long run = 0ull;
+            int found = cut;
+            for (int base = 0; base < cut; base += 32) {
+                const int j = base + lane;
+                const unsigned long long m = j < cut ? fm(j) : 0ull;
+                unsigned long long inc = m;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const unsigned int hit = __ballot_sync(0xffffffffu, j < cut && run + inc >= tgt);
+                if (hit) { found = base + __ffs(hit) - 1; break; }
+                run += __shfl_sync(0xffffffffu, inc, 31);
+            }
+            cut = found;
+        }
+        float S = 0.f;
+        for (int j = lane; j <= cut; j += 32) S += exp2f((key_float((uint32_t)(s[j] >> 32)) - lm) * c);
+        S = warp_sum(S);
+        const unsigned long long e = s[cut];
+        if (lane == 0) ds.res[r] = FilterParam{lm, S, (uint32_t)(e >> 32), (int)(~(uint32_t)e), 0, 0, 0, 0};
+    }
+    __syncthreads();
+    for (int r = 0; r < 2; ++r)
+        if (go[r]) out[r] = ds.res[r];
+
+    // ---- rows the fast path does not take: filter_row on one CTA each ----
+    const bool fb0 = live[0] && ds.fb[0], fb1 = live[1] && ds.fb[1];
+    if (fb0 || fb1) {
+        C::sync();                                 // nobody reads this CTA's scratch any more
+        for (int r = 0; r < 2; ++r) {
+            if (!(r == 0 ? fb0 : fb1)) continue;
+            if (rank == r % CS) {
+                __syncthreads();
+                filter_row(fsc.one, rows[r], V, c, top_k, top_p, slots[r], prefetch[r]);
+            }
+        }
+        __threadfence();
+        C::sync();
+        if (fb0) out[0] = load_filter(slots[0]);
+        if (fb1) out[1] = load_filter(slots[1]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 template <int CS, int NT, bool D2T, bool FILT>
 __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArgs a) {
     using C = Cluster<CS, NT>;
     __shared__ VerifySmem<NT> sm;
-    FiltSmem* fsm = nullptr;                 // the filtered walk's row-filter scratch
+    FiltScratch* fsc = nullptr;              // the filtered walk's row-filter scratch
     if constexpr (FILT) {
         static_assert(NT == kFiltThreads, "a row filter takes the whole CTA");
-        __shared__ FiltSmem fs;
-        fsm = &fs;
+        __shared__ FiltScratch fs;
+        fsc = &fs;
     }
     const int tid = threadIdx.x;
     const int rank = cta_rank_in_cluster(CS);
@@ -1029,7 +1510,6 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
     int buf = 0;
     int err = sm.err;
     int v = 0, acc_n = 0, y = -1;
-    unsigned long long ready_q = 0ull, ready_p = 0ull;   // nodes whose filters are written
     if (tid == 0) sm.path[0] = 0;
 
     while (!err) {
@@ -1041,47 +1521,17 @@ __global__ void __launch_bounds__(NT, FILT ? 2 : 4) verify_walk_kernel(VerifyArg
             // filtered walk: this node's row filters; logits outside them read as -inf
             FilterParam fqv{}, fpv{};
             if constexpr (FILT) {
-                // Rows are filtered when the walk reaches their node, one row per CTA of
-                // the cluster: q(v) and p(v) first, then, on the CTAs that would idle, the
-                // rows of v's first children, which the walk visits next if it accepts
-                // one of them (that visit then needs no round).  Every CTA derives the
-                // same jobs and ready masks; after the barrier each reads back past L1.
-                FilterParam* fq_slot = a.fq + (int64_t)b * n + v;
-                FilterParam* fp_slot = prow ? a.fp + (int64_t)b * a.R + sm.row[v] : nullptr;
-                const bool need_q = !((ready_q >> v) & 1ull);
-                const bool need_p = prow && !((ready_p >> v) & 1ull);
-                if (need_q || need_p) {
-                    int jn[CS > 2 ? CS : 2];          // job: node, and whether its draft row
-                    bool jp[CS > 2 ? CS : 2];
-                    int nj = 0;
-                    if (need_q) { jn[nj] = v; jp[nj] = false; ++nj; }
-                    if (need_p) { jn[nj] = v; jp[nj] = true; ++nj; }
-                    for (int ch = v + 1; ch < n && nj < CS; ++ch) {
-                        if (sm.parent[ch] != v) continue;
-                        if (!((ready_q >> ch) & 1ull)) { jn[nj] = ch; jp[nj] = false; ++nj; }
-                        if (nj < CS && sm.nkids[ch] > 0 && !((ready_p >> ch) & 1ull)) {
-                            jn[nj] = ch; jp[nj] = true; ++nj;
-                        }
-                    }
-                    for (int j = rank; j < nj; j += CS) {
-                        if (j >= CS) __syncthreads();          // one-CTA clusters run several
-                        const int u = jn[j];
-                        if (jp[j])
-                            filter_row(*fsm, drf_b + (int64_t)sm.row[u] * Vdl, V, c, a.top_k, a.top_p,
-                                       a.fp + (int64_t)b * a.R + sm.row[u], true);
-                        else
-                            filter_row(*fsm, tgt_b + (int64_t)u * Vl, V, c, a.top_k, a.top_p,
-                                       a.fq + (int64_t)b * n + u, a.target_in_device);
-                    }
-                    for (int j = 0; j < nj; ++j) {
-                        if (jp[j]) ready_p |= 1ull << jn[j];
-                        else ready_q |= 1ull << jn[j];
-                    }
-                    __threadfence();
-                    C::sync();
-                }
-                fqv = load_filter(fq_slot);
-                if (prow) fpv = load_filter(fp_slot);
+                // The rows are filtered when the walk reaches their node, by the whole
+                // cluster (each CTA its vocabulary slice); every CTA gets both filters.
+                const float* const rws[2] = {qrow, prow};
+                FilterParam* const slots[2] = {a.fq + (int64_t)b * n + v,
+                                               prow ? a.fp + (int64_t)b * a.R + sm.row[v] : nullptr};
+                const bool pf[2] = {a.target_in_device, true};
+                FilterParam outs[2];
+                cluster_filters<CS, NT>(sm, *fsc, buf, rank, rws, prow ? 2 : 1, lo, hi, vec4, V, c,
+                                        a.top_k, a.top_p, slots, pf, outs);
+                fqv = outs[0];
+                if (prow) fpv = outs[1];
             }
             auto mq = [&](int t, float l) -> float {
                 if constexpr (FILT) return filter_keeps(fqv, t, l) ? l : -INFINITY;

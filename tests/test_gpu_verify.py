@@ -382,8 +382,9 @@ def test_filtered_trees_match_oracle(V, top_k, top_p, quant):
 @pytest.mark.parametrize("B,quant", [(100, 0.0), (160, 0.5), (320, 0.0)])
 def test_filtered_walk_at_every_cluster_size(B, quant):
     """The walk's cluster shrinks as B grows (8 CTAs per sequence up to B = 76, then 4,
-    2 and, above B = 304, one); the filtered walk filters each visited row on rank 0
-    (target) and rank 1 (draft), or both on rank 0 in a one-CTA cluster.  Small trees
+    2 and, above B = 304, one); the filtered walk splits each visited row's filter over
+    the cluster's vocabulary slices (rows it leaves over go to rank 0 for the target and
+    rank 1 for the draft, or both to rank 0 in a one-CTA cluster).  Small trees
     (16 nodes, depth 4, 4 children per level) over V = 1003, top-k 12 and top-p 0.8,
     against oracle.verify_accept_filtered."""
     import dataclasses

@@ -379,6 +379,46 @@ def test_filtered_trees_match_oracle(V, top_k, top_p, quant):
     np.testing.assert_allclose(r[1, b_i, n_i, 1], Zd[b_i, rows[b_i, n_i]], rtol=1e-5)
 
 
+def test_filtered_walk_with_fast_and_fallback_rows_in_one_call():
+    """Each visited node's two rows take different paths of the cluster filter: the
+    target rows are smooth (the cut found from the merged near-bin histogram and the
+    gathered candidates), the draft rows quantised to multiples of 2 (thousands of equal
+    logits at the cut: the one-CTA radix select).  Sequence 0's target rows are all
+    equal, so every token ties and the cut is by index alone.  Against
+    oracle.verify_accept_filtered; the visited rows' filtered sums to 1e-5."""
+    E = _gpu()
+    cfg = W.CONFIGS["sweep_70b"]
+    B, top_k, top_p = 8, 50, 0.9
+    tgt, drows, tree = _tree_case(cfg, B, seed=57, V=32000)
+    drows = (np.round(drows / 2.0) * 2.0).astype(np.float32)
+    tgt[0] = 1.5
+    ref = oracle.verify_accept_filtered(tgt, drows, tree["tokens"], tree["parent"], cfg.depth, 1.0,
+                                        seed=37, top_k=top_k, top_p=top_p,
+                                        draft_row=tree["draft_row"])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rs = torch.full((2, B, cfg.n, 2), float("nan"), device="cuda")
+    acc, path, emit = E.eagle_verify_accept(
+        _cuda(tgt), _cuda(drows), _cuda(tree["tokens"]), _cuda(tree["parent"]), cfg.depth, 1.0, 37,
+        draft_row=_cuda(tree["draft_row"]), row_stats=rs, dev_status=st, top_k=top_k, top_p=top_p)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and (ref["status"] == 0).all()
+    ft = oracle.filter_logits(tgt, 1.0, top_k, top_p)
+    fd = oracle.filter_logits(drows, 1.0, top_k, top_p)
+    dec, ties = compare_walks(ref, acc.cpu().numpy(), path.cpu().numpy(), emit.cpu().numpy(),
+                              rows=(ft, fd, tree["draft_row"], 1.0))
+    assert_tie_budget(dec, ties)
+    r = rs.cpu().numpy()
+    _, Z, _, _ = oracle.softmax_rows(ft, 1.0)
+    seen = ~np.isnan(r[0, :, :, 0])
+    assert seen[0].any() and seen.sum() >= 8
+    np.testing.assert_allclose(r[0][..., 1][seen], Z[seen], rtol=1e-5)
+    _, Zd, _, _ = oracle.softmax_rows(fd, 1.0)
+    rows = tree["draft_row"]
+    seen = ~np.isnan(r[1, :, :, 0])
+    b_i, n_i = np.nonzero(seen)
+    np.testing.assert_allclose(r[1, b_i, n_i, 1], Zd[b_i, rows[b_i, n_i]], rtol=1e-5)
+
+
 @pytest.mark.parametrize("B,quant", [(100, 0.0), (160, 0.5), (320, 0.0)])
 def test_filtered_walk_at_every_cluster_size(B, quant):
     """The walk's cluster shrinks as B grows (8 CTAs per sequence up to B = 76, then 4,

@@ -111,6 +111,35 @@ __device__ __forceinline__ bool topk_better(float v, int i, float w, int j) {
 // the segment's statistics and top-k go to the tree state.
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
+
+// The k best entries of the kTopkWarps warp lists in s_v / s_i (list w at w * kKMax, each
+// sorted best first, empty entries (-inf, 0x7fffffff)) into m_v / m_i in order, merged
+// by one warp: lane w < kTopkWarps holds the head of list w, a butterfly over those lanes
+// finds the best head (the order is strict, so every lane agrees), and its lane moves on.
+__device__ __forceinline__ void merge_warp_lists(const float* s_v, const int* s_i, int k, float* m_v,
+                                                 int* m_i) {
+    static_assert((kTopkWarps & (kTopkWarps - 1)) == 0 && kTopkWarps <= 32, "butterfly over the lists");
+    const int lane = threadIdx.x & 31;
+    int p = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff, bl = lane;
+        if (lane < kTopkWarps && p < k) {
+            bv = s_v[lane * kKMax + p];
+            bi = s_i[lane * kKMax + p];
+        }
+#pragma unroll
+        for (int o = kTopkWarps / 2; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+            if (topk_better(ov, oi, bv, bi)) { bv = ov; bi = oi; bl = ol; }
+        }
+        if (lane == bl && bi != 0x7fffffff) ++p;
+        if (lane == 0) { m_v[j] = bv; m_i[j] = bi; }
+    }
+}
+
 constexpr int kTopkUnroll = 8;                 // float4 loads in flight per thread
 constexpr int kSegMinElems = 8192;             // shortest segment worth its own CTA
 constexpr float kLog2e = 1.4426950408889634f;
@@ -168,6 +197,8 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
     __shared__ float s_red[kTopkWarps][2];
     __shared__ int s_bad[kTopkWarps];
     __shared__ float s_thr;                    // a lower bound on the block's k-th best
+    __shared__ float s_mv[kKMax];
+    __shared__ int s_mi[kKMax];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) s_thr = -INFINITY;
     volatile float* thr_p = &s_thr;
@@ -294,30 +325,17 @@ row_topk_kernel(const float* __restrict__ logits, int k_in, int R, int off, int 
     __syncthreads();
     SeqState st = seq_state(state, b, k, D);
     const int slot = s * kSegMax + seg;
-    // rank of every list entry among all of them (entries are distinct tokens,
-    // or empty slots that rank below every token)
-    if (tid < kTopkWarps * k) {
-        const int w = tid / k, j = tid % k;
-        const float v = s_v[w * kKMax + j];
-        const int i = s_i[w * kKMax + j];
-        int rank = 0;
-        for (int w2 = 0; w2 < kTopkWarps; ++w2)
-            for (int j2 = 0; j2 < k; ++j2)
-                rank += topk_better(s_v[w2 * kKMax + j2], s_i[w2 * kKMax + j2], v, i);
-        if (rank < k && i != 0x7fffffff) {
-            st.seg_val[slot * k + rank] = v;
-            st.seg_tok[slot * k + rank] = i;
+    if (warp == 0) {
+        // the segment's top-k in order; a segment shorter than k leaves empty entries
+        merge_warp_lists(s_v, s_i, k, s_mv, s_mi);
+        __syncwarp();
+        if (lane < k) {
+            const bool has = s_mi[lane] != 0x7fffffff;
+            st.seg_val[slot * k + lane] = has ? s_mv[lane] : -INFINITY;
+            st.seg_tok[slot * k + lane] = has ? s_mi[lane] : 0x7fffffff;
         }
     }
     if (tid == 0) {
-        // fewer than k entries can only happen for a segment shorter than k
-        int cnt = 0;
-        for (int w = 0; w < kTopkWarps; ++w)
-            for (int j = 0; j < k; ++j) cnt += s_i[w * kKMax + j] != 0x7fffffff;
-        for (int j = cnt; j < k; ++j) {
-            st.seg_val[slot * k + j] = -INFINITY;
-            st.seg_tok[slot * k + j] = 0x7fffffff;
-        }
         float M = -INFINITY, S = 0.f;
         int bd = 0;
         for (int w = 0; w < kTopkWarps; ++w) {
@@ -353,6 +371,8 @@ topk_merge_kernel(const float* __restrict__ part, const float* __restrict__ logi
     __shared__ int s_i[kTopkWarps * kKMax];
     __shared__ float s_red[kTopkWarps][2];
     __shared__ int s_bad[kTopkWarps];
+    __shared__ float s_mv[kKMax];
+    __shared__ int s_mi[kKMax];
     __shared__ float s_tau;
     __shared__ int s_nsel;
     __shared__ int s_sel[kMergeMaxTiles];
@@ -377,16 +397,6 @@ topk_merge_kernel(const float* __restrict__ part, const float* __restrict__ logi
                 ti = __shfl_sync(0xffffffffu, li, k - 1);
             }
         }
-    };
-    // rank of this warp-list entry among all warps' entries (block-wide)
-    auto block_rank = [&](int w, int j) {
-        const float v = s_v[w * kKMax + j];
-        const int i = s_i[w * kKMax + j];
-        int rank = 0;
-        for (int w2 = 0; w2 < kTopkWarps; ++w2)
-            for (int j2 = 0; j2 < k; ++j2)
-                rank += topk_better(s_v[w2 * kKMax + j2], s_i[w2 * kKMax + j2], v, i);
-        return rank;
     };
 
     // ---- pass 1: statistics, and the k largest tile maxima ----
@@ -426,16 +436,11 @@ topk_merge_kernel(const float* __restrict__ part, const float* __restrict__ logi
     if (lane == 0) { s_red[warp][0] = m; s_red[warp][1] = sum; s_bad[warp] = bad; }
     if (lane < k) { s_v[warp * kKMax + lane] = lv; s_i[warp * kKMax + lane] = li; }
     __syncthreads();
-    if (tid < kTopkWarps * k) {
-        const int w = tid / k, j = tid % k;
-        // the entry of rank k - 1 is the k-th largest tile maximum (fewer tiles: -inf)
-        if (block_rank(w, j) == k - 1 && s_i[w * kKMax + j] != 0x7fffffff) s_tau = s_v[w * kKMax + j];
-    }
-    if (tid == 0) {
-        int cnt = 0;
-        for (int w = 0; w < kTopkWarps; ++w)
-            for (int j = 0; j < k; ++j) cnt += s_i[w * kKMax + j] != 0x7fffffff;
-        if (cnt < k) s_tau = -INFINITY;
+    if (warp == 0) {
+        // the k-th largest tile maximum (fewer tiles: -inf)
+        merge_warp_lists(s_v, s_i, k, s_mv, s_mi);
+        __syncwarp();
+        if (lane == 0) s_tau = s_mi[k - 1] != 0x7fffffff ? s_mv[k - 1] : -INFINITY;
     }
     __syncthreads();
     const float tau = s_tau;
@@ -473,23 +478,17 @@ topk_merge_kernel(const float* __restrict__ part, const float* __restrict__ logi
     __syncthreads();
     SeqState st = seq_state(state, b, k, D);
     const int slot = s * kSegMax;
-    if (tid < kTopkWarps * k) {
-        const int w = tid / k, j = tid % k;
-        const int rank = block_rank(w, j);
-        const int i = s_i[w * kKMax + j];
-        if (rank < k && i != 0x7fffffff) {
-            st.seg_val[slot * k + rank] = s_v[w * kKMax + j];
-            st.seg_tok[slot * k + rank] = i;
+    if (warp == 0) {
+        // the row's top-k in order; missing entries (a row shorter than k) stay empty
+        merge_warp_lists(s_v, s_i, k, s_mv, s_mi);
+        __syncwarp();
+        if (lane < k) {
+            const bool has = s_mi[lane] != 0x7fffffff;
+            st.seg_val[slot * k + lane] = has ? s_mv[lane] : -INFINITY;
+            st.seg_tok[slot * k + lane] = has ? s_mi[lane] : 0x7fffffff;
         }
     }
     if (tid == 0) {
-        int cnt = 0;
-        for (int w = 0; w < kTopkWarps; ++w)
-            for (int j = 0; j < k; ++j) cnt += s_i[w * kKMax + j] != 0x7fffffff;
-        for (int j = cnt; j < k; ++j) {
-            st.seg_val[slot * k + j] = -INFINITY;
-            st.seg_tok[slot * k + j] = 0x7fffffff;
-        }
         float M = -INFINITY, S = 0.f;
         int bd = 0;
         for (int w = 0; w < kTopkWarps; ++w) {

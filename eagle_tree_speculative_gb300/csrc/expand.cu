@@ -540,15 +540,19 @@ select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t
         s_rowS[tid] = S;
     }
     __syncthreads();
-    // ---- each row's top-k: rank of every segment entry among the row's entries ----
+    // ---- each row's top-k: rank of every segment entry among the row's entries (one
+    // segment is already in rank order) ----
     for (int e = tid; e < k_in * nseg * k; e += kSelectThreads) {
         const int row = e / (nseg * k), r = e % (nseg * k);
         const int base = row * kSegMax * k;                 // first entry of the row
         const float v = st.seg_val[base + r];
         const int i = st.seg_tok[base + r];
-        int rank = 0;
-        for (int f = 0; f < nseg * k; ++f)
-            rank += topk_better(st.seg_val[base + f], st.seg_tok[base + f], v, i);
+        int rank = r;
+        if (nseg > 1) {
+            rank = 0;
+            for (int f = 0; f < nseg * k; ++f)
+                rank += topk_better(st.seg_val[base + f], st.seg_tok[base + f], v, i);
+        }
         if (rank < k) {
             s_tok[row * kKMax + rank] = i;
             s_conf[row * kKMax + rank] = exp2f((v - s_rowM[row]) * kLog2e) / s_rowS[row];
@@ -583,16 +587,31 @@ select_kernel(int level, int final, int k, int D, int nseg, void* state, int32_t
         s_id[e] = id;
     }
     __syncthreads();
-    // rank of each candidate in (V desc, id asc); the k best form the frontier
-    for (int e = tid; e < ncand; e += kSelectThreads) {
-        const float v = s_val[e];
-        const int id = s_id[e];
-        int rank = 0;
-        for (int f = 0; f < ncand; ++f) rank += topk_better(s_val[f], s_id[f], v, id);
-        if (rank < k) {
-            st.frontier[rank] = id;
-            if (level < D && !final) st.row[id] = 1 + (level - 1) * k + rank;
-            if (frontier_tokens) frontier_tokens[(int64_t)b * k + rank] = st.token[id];
+    // the k best candidates in (V desc, id asc) form the frontier.  Row s's candidates
+    // s * k .. s * k + k - 1 are already in that order (V = value[parent] * c with c
+    // non-increasing in j, ids increasing), so one warp merges the k_in rows: lane s holds
+    // the head of row s, a butterfly finds the best head, and its lane moves on.
+    static_assert(kKMax <= 16, "the merge spans 16 lanes");
+    if (tid < 32) {
+        const int lane = tid;
+        int p = 0;
+        for (int rank = 0; rank < k; ++rank) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff, bl = lane;
+            if (lane < k_in && p < k) { bv = s_val[lane * k + p]; bi = s_id[lane * k + p]; }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
+                if (topk_better(ov, oi, bv, bi)) { bv = ov; bi = oi; bl = ol; }
+            }
+            if (lane == bl && bi != 0x7fffffff) ++p;
+            if (lane == 0 && bi != 0x7fffffff) {
+                st.frontier[rank] = bi;
+                if (level < D && !final) st.row[bi] = 1 + (level - 1) * k + rank;
+                if (frontier_tokens) frontier_tokens[(int64_t)b * k + rank] = st.token[bi];
+            }
         }
     }
 }

@@ -26,13 +26,15 @@ bool ttt_map(CUtensorMap* map, const void* base, int S, int R1, int64_t slabs) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Every round of K or V as a 4-D tensor (128 dims, S positions, R1 rounds, slabs);
-// boxes of 64 dims x PB positions x RB rounds (the diagonal rows of one row tile).
-bool ttt_diag_map(CUtensorMap* map, const void* base, int S, int R1, int64_t slabs, int PB,
-                  int RB) {
+// Rounds 0 .. nrounds - 1 of K or V as a 4-D tensor (128 dims, S positions, rounds,
+// slabs; the slabs R1 rounds apart); boxes of 64 dims x PB positions x RB rounds, PB * RB
+// = 128 rows (the diagonal rows of one row tile).  Rounds from nrounds on and positions
+// from S on read as zeros.
+bool ttt_diag_map(CUtensorMap* map, const void* base, int S, int R1, int nrounds, int64_t slabs,
+                  int PB, int RB) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)S, (cuuint64_t)R1, (cuuint64_t)slabs};
+    cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)S, (cuuint64_t)nrounds, (cuuint64_t)slabs};
     cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)S * kHeadDim * 2,
                              (cuuint64_t)R1 * S * kHeadDim * 2};
     cuuint32_t box[4] = {64, (cuuint32_t)PB, (cuuint32_t)RB, 1};
@@ -64,14 +66,18 @@ extern "C" eagle_status eagle_ttt_attn(const void* q, const void* k, const void*
         (int64_t)R1 * S > 0x7fffffffLL)
         return EAGLE_ERR_SHAPE;
     // A row tile of 128 rows spans at most 127 / G + 1 positions, one more when G
-    // does not divide 128; the diagonal boxes cover that many positions and as many
-    // rounds as fit in 128 rows.
-    const int PB = 127 / G + 1 + (128 % G != 0 ? 1 : 0);
-    const int RB = std::max(1, std::min(128 / PB, std::max(1, R1 - 1)));
+    // does not divide 128.  A diagonal box holds RB rounds (a power of two) of PB =
+    // 128 / RB >= that many positions: exactly the 128 rows of a ring stage, so every row
+    // the MMAs read was written by the box.  Rounds above r read as zeros.
+    const int span = 127 / G + 1 + (128 % G != 0 ? 1 : 0);
+    int RB = 1;
+    while (2 * RB * span <= 128) RB *= 2;
+    const int PB = 128 / RB;
     const int ND = (r + RB - 1) / RB;
     CUtensorMap mk, mv, mkd, mvd;
     if (!ttt_map(&mk, k, S, R1, slabs) || !ttt_map(&mv, v, S, R1, slabs) ||
-        !ttt_diag_map(&mkd, k, S, R1, slabs, PB, RB) || !ttt_diag_map(&mvd, v, S, R1, slabs, PB, RB))
+        !ttt_diag_map(&mkd, k, S, R1, r + 1, slabs, PB, RB) ||
+        !ttt_diag_map(&mvd, v, S, R1, r + 1, slabs, PB, RB))
         return EAGLE_ERR_CUDA;
     ttt_tc::Args a;
     a.q = static_cast<const uint16_t*>(q);

@@ -15,25 +15,21 @@
 //     round 0 stream by TMA through two 3-stage rings; S = Q K^T and O += P V are
 //     tcgen05 MMAs with Q, S, P and O in TMEM; one thread per row runs the online
 //     softmax with the causal mask on the tiles that cross the diagonal.
-//   - Diagonal tiles follow the causal tiles through the same rings, so they load
-//     while the last causal tiles are computed.  The rows of rounds 1..r at the
-//     tile's positions are contiguous per round, so one 4-D TMA box (64 dims x PB
-//     positions x RB rounds) brings PB * RB <= 128 of them into a K stage, and the
-//     same box of V into the V stage.  After the last PV, each softmax thread takes
-//     O into registers and, per diagonal key of its position, the dot product with
-//     its query (read back from TMEM) on the CUDA cores, one more online-softmax
-//     step and the weighted value row; the four softmax warps then release the
-//     stage on `drel`.
+//   - Diagonal tiles follow the causal tiles through the same rings and the same
+//     MMAs, so they load while the last causal tiles are computed.  The rows of rounds
+//     1..r at the tile's positions are contiguous per round, so one 4-D TMA box (64
+//     dims x PB positions x RB rounds, PB * RB = 128) fills a K stage and the same box
+//     of V the V stage.  A row sees, of such a tile, only the keys of its own position
+//     in rounds up to r (at most RB of the 128): the softmax masks the rest, so the
+//     diagonal part costs ND = ceil(r / RB) more tiles of the same pipeline instead of
+//     per-position dot products on the CUDA cores after it.
 // The row tiles nearest the end of the sequence have the most keys, so the grid
 // runs them first.  Every wait is bounded.
 //
 // Barriers (each completes once per use; a waiter is never more than one
 // completion behind):
-//   k_full/v_full[s]     stage s landed (TMA): causal tiles -> MMA, diagonal tiles ->
-//                        softmax warps, which poll them only after the last PV, when
-//                        every earlier completion of the barrier has happened
-//   k_empty/v_empty[s]   causal tile in stage s consumed (MMA)  MMA -> producer
-//   drel[s]              diagonal tile in stage s consumed (4 softmax warps)
+//   k_full/v_full[s]     stage s landed (TMA)                   producer -> MMA
+//   k_empty/v_empty[s]   tile in stage s consumed (MMA)         MMA -> producer
 //   q_full, s_full/p_full/pv_done[tile % 2]  as in the tree-attention kernel.
 #pragma once
 
@@ -66,7 +62,7 @@ struct Args {
     uint16_t* out;            // [B, S, Hq, 128]
     int B, S, Hq, Hkv, G, R1, r;
     int PB;                   // positions per diagonal box (>= positions of any row tile)
-    int RB;                   // rounds per diagonal box (PB * RB <= 128)
+    int RB;                   // rounds per diagonal box (PB * RB = 128)
     int ND;                   // diagonal tiles: ceil(r / RB)
     int tiles;                // row tiles per (sequence, kv head)
     float scale_log2;
@@ -78,7 +74,6 @@ struct Bars {
     uint64_t k_empty[NSTAGES];
     uint64_t v_full[NSTAGES];
     uint64_t v_empty[NSTAGES];
-    uint64_t drel[NSTAGES];
     uint64_t s_full[NSBUF];
     uint64_t q_full;
     uint64_t p_full[NSBUF];
@@ -87,16 +82,6 @@ struct Bars {
     uint32_t tmem_slot;
     int abort_flag;
 };
-
-// 16 bytes (8 dims) of row `row` of a 64-dim half-box staged with the 128-byte
-// swizzle: chunk c of a 128-byte row sits at chunk c ^ (row % 8).
-__device__ __forceinline__ uint4 swz_chunk(const uint8_t* half_box, int row, int c) {
-    return *reinterpret_cast<const uint4*>(half_box + row * 128 + ((c ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ float2 bf2(uint32_t w) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-D
@@ -123,7 +108,6 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
     const int ke = (row_end - 1) / G + 1;                 // round-0 keys 0 .. ke-1 reach the tile
     const int T = (ke + TBN - 1) / TBN;                   // causal tiles
     const int ND = a.ND;                                  // diagonal tiles, loaded last
-    const bool has_diag = ND > 0;
 
     uint4 qrow[kHeadDim / 8];
     if (warp >= 4) {
@@ -144,7 +128,6 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
             mbar_init(s32(&bars->k_empty[s]), 1);
             mbar_init(s32(&bars->v_full[s]), 1);
             mbar_init(s32(&bars->v_empty[s]), 1);
-            mbar_init(s32(&bars->drel[s]), 4);
         }
         for (int p = 0; p < NSBUF; ++p) {
             mbar_init(s32(&bars->s_full[p]), 1);
@@ -193,10 +176,6 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
             uint8_t* ring = isK ? sK : sV;
             uint64_t* full = isK ? bars->k_full : bars->v_full;
             uint64_t* empty = isK ? bars->k_empty : bars->v_empty;
-            // first diagonal ring tile of each stage
-            const int d0s[NSTAGES] = {T + (NSTAGES - T % NSTAGES) % NSTAGES,
-                                      T + (NSTAGES + 1 - T % NSTAGES) % NSTAGES,
-                                      T + (NSTAGES + 2 - T % NSTAGES) % NSTAGES};
             for (int jp = NSTAGES; jp < min(T, NSTAGES + kPrefetch); ++jp) {
                 tma_prefetch_3d(map, 0, jp * TBN, kvz);
                 tma_prefetch_3d(map, 64, jp * TBN, kvz);
@@ -206,16 +185,10 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
             const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
             for (int t = 0; t < T + ND; ++t) {
                 const int st = t % NSTAGES;
-                if (t >= NSTAGES) {
-                    // wait until the stage's previous tile was consumed: a causal tile by
-                    // the MMA commit, a diagonal one by the softmax warps
-                    const int tp = t - NSTAGES;
-                    const bool okw =
-                        tp < T ? mbar_wait(s32(&empty[st]), (uint32_t)(tp / NSTAGES) & 1u, abort_flag)
-                               : mbar_wait(s32(&bars->drel[st]), (uint32_t)((tp - d0s[st]) / NSTAGES) & 1u,
-                                           abort_flag);
-                    if (!okw) break;
-                }
+                // wait until the MMAs consumed the stage's previous tile
+                if (t >= NSTAGES &&
+                    !mbar_wait(s32(&empty[st]), (uint32_t)((t - NSTAGES) / NSTAGES) & 1u, abort_flag))
+                    break;
                 const uint32_t fb = s32(&full[st]);
                 uint8_t* dst = ring + st * K_BYTES;
                 if (t < T) {
@@ -228,7 +201,7 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
                     tma_load_3d_hint(s32(dst), map, fb, 0, t * TBN, kvz, keep);
                     tma_load_3d_hint(s32(dst + KV_BOX_BYTES), map, fb, 64, t * TBN, kvz, keep);
                 } else {
-                    mbar_expect_tx(fb, (uint32_t)(2 * 128 * a.PB * a.RB));
+                    mbar_expect_tx(fb, K_BYTES);                  // PB * RB = 128 rows
                     const int u0 = 1 + (t - T) * a.RB;            // first round of the box
                     tma_load_4d_hint(s32(dst), dmap, fb, 0, imin, u0, kvz, once);
                     tma_load_4d_hint(s32(dst + KV_BOX_BYTES), dmap, fb, 64, imin, u0, kvz, once);
@@ -237,8 +210,8 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issuer: causal tiles (ring tiles 0 .. T-1) ----------------
-            attn_common::mma_issue_loop<NSTAGES>(bars, tmem, sK, sV, T, abort_flag);
+            // ---------------- MMA issuer: causal and diagonal tiles ----------------
+            attn_common::mma_issue_loop<NSTAGES>(bars, tmem, sK, sV, T + ND, abort_flag);
         }
     } else if (warp >= 4) {
         // ---------------- softmax: one thread per query row ----------------
@@ -249,11 +222,11 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
         const uint32_t s_addr0 = tmem + lane_base + S_COL0;
         const uint32_t o_addr = tmem + lane_base + O_COL0;
-        const uint32_t q_addr = tmem + lane_base + Q_COL0;
         const float sc = a.scale_log2;
+        const int pl = i - imin;                         // position within the diagonal boxes
         float mref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; ok && j < T; ++j) {
+        for (int j = 0; ok && j < T + ND; ++j) {
             bool got = mbar_wait(s32(&bars->s_full[j % NSBUF]), ((uint32_t)j / NSBUF) & 1u, abort_flag);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             tc_fence_after();
@@ -261,7 +234,20 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
             float x[TBN];
             attn_common::load_scores(s_addr, x);
             const int key0 = j * TBN;
-            if (key0 + TBN - 1 > imin || !valid) {
+            if (j >= T) {
+                // diagonal tile: key c = (round u0 + c / PB, position imin + c % PB); this
+                // row sees its own position in rounds up to r
+                const int nr = min(a.RB, a.r - (j - T) * a.RB);
+                uint64_t vis[2] = {0ull, 0ull};
+                if (valid)
+                    for (int ul = 0; ul < nr; ++ul) {
+                        const int c = ul * a.PB + pl;
+                        vis[c >> 6] |= 1ull << (c & 63);
+                    }
+#pragma unroll
+                for (int c = 0; c < TBN; ++c)
+                    if (!((vis[c >> 6] >> (c & 63)) & 1ull)) x[c] = -INFINITY;
+            } else if (key0 + TBN - 1 > imin || !valid) {
                 // causal mask: key k visible iff k <= i (keys past the sequence arrive as
                 // zeros from TMA and are masked too)
                 uint64_t vis[2];
@@ -279,122 +265,31 @@ ttt_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,    // round 0, 3-
                 break;
             }
         }
-        bool got = ok && T > 0 ? mbar_wait(s32(&bars->pv_done[(T - 1) % NSBUF]),
-                                           ((uint32_t)(T - 1) / NSBUF) & 1u, abort_flag)
-                               : false;
+        const int TT = T + ND;
+        bool got = ok && TT > 0 ? mbar_wait(s32(&bars->pv_done[(TT - 1) % NSBUF]),
+                                            ((uint32_t)(TT - 1) / NSBUF) & 1u, abort_flag)
+                                : false;
         got = __all_sync(0xffffffffu, got);
         tc_fence_after();
         const int h = kvh * G + (valid ? r % G : 0);
         uint16_t* dst0 = a.out + (((int64_t)b * S + i) * a.Hq + h) * kHeadDim;
-        if (!has_diag) {
-            const float inv = (got && l > 0.f) ? 1.f / l : 0.f;
-            for (int cc = 0; cc < kHeadDim / 32; ++cc) {
-                uint32_t o[32];
-                if (got) tmem_ld32(o_addr + cc * 32, o);
-                else
+        const float inv = (got && l > 0.f) ? 1.f / l : 0.f;
+        for (int cc = 0; cc < kHeadDim / 32; ++cc) {
+            uint32_t o[32];
+            if (got) tmem_ld32(o_addr + cc * 32, o);
+            else
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
-                if (!valid) continue;
-                uint16_t* dst = dst0 + cc * 32;
+                for (int e = 0; e < 32; ++e) o[e] = 0u;
+            if (!valid) continue;
+            uint16_t* dst = dst0 + cc * 32;
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                    const uint4 w = make_uint4(
-                        pack2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
-                        pack2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
-                        pack2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
-                        pack2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
-                    *reinterpret_cast<uint4*>(dst + e) = w;
-                }
-            }
-        } else {
-            // ---- diagonal: rounds 1..r at this position, folded into O last ----
-            // O comes into registers; each diagonal key is one more online-softmax step.
-            float oacc[kHeadDim];
-#pragma unroll
-            for (int cc = 0; cc < kHeadDim / 32; ++cc) {
-                uint32_t o[32];
-                if (got) tmem_ld32(o_addr + cc * 32, o);
-                else
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = 0u;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) oacc[32 * cc + e] = __uint_as_float(o[e]);
-            }
-            const int pl = i - imin;                     // position within the boxes
-            // The last PV has completed, so every causal tile's K and V landed and each
-            // stage's next full-barrier completion is the diagonal tile's.
-            for (int t = 0; got && t < ND; ++t) {
-                const int ring_t = T + t;
-                const int st = ring_t % NSTAGES;
-                const uint32_t par = ((uint32_t)ring_t / NSTAGES) & 1u;
-                const bool okw = mbar_wait(s32(&bars->k_full[st]), par, abort_flag) &&
-                                 mbar_wait(s32(&bars->v_full[st]), par, abort_flag);
-                if (!__all_sync(0xffffffffu, okw)) { got = false; break; }
-                const uint8_t* kst = sK + st * K_BYTES;
-                const uint8_t* vst = sV + st * K_BYTES;
-                // rounds of this box in use; the same for every lane, because the loop
-                // holds warp-collective TMEM loads (rows past the tile compute on row
-                // pl = 0 and are never written out)
-                const int nr = min(a.RB, a.r - t * a.RB);
-                for (int ub = 0; ub < nr; ++ub) {
-                    const int row = ub * a.PB + pl;
-                    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        // this row's query, dims 64hh .. 64hh+63, read back from TMEM
-                        uint32_t qa[32];
-                        tmem_ld32(q_addr + 32 * hh, qa);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 kw = swz_chunk(kst + hh * KV_BOX_BYTES, row, c);
-                            const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 kf = bf2(ka[e]), qf = bf2(qa[4 * c + e]);
-                                acc[2 * e] = fmaf(qf.x, kf.x, acc[2 * e]);
-                                acc[2 * e + 1] = fmaf(qf.y, kf.y, acc[2 * e + 1]);
-                            }
-                        }
-                    }
-                    const float sd = (((acc[0] + acc[1]) + (acc[2] + acc[3])) +
-                                      ((acc[4] + acc[5]) + (acc[6] + acc[7]))) * sc;
-                    if (sd > mref + kRescaleThreshold || mref == -INFINITY) {
-                        const float alpha = mref == -INFINITY ? 0.f : exp2f(mref - sd);
-#pragma unroll
-                        for (int e = 0; e < kHeadDim; ++e) oacc[e] *= alpha;
-                        l *= alpha;
-                        mref = sd;
-                    }
-                    const float p = ex2_approx(sd - mref);
-                    l += p;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 vw = swz_chunk(vst + hh * KV_BOX_BYTES, row, c);
-                            const uint32_t va[4] = {vw.x, vw.y, vw.z, vw.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 vf = bf2(va[e]);
-                                const int d0 = 64 * hh + 8 * c + 2 * e;
-                                oacc[d0] = fmaf(p, vf.x, oacc[d0]);
-                                oacc[d0 + 1] = fmaf(p, vf.y, oacc[d0 + 1]);
-                            }
-                        }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s32(&bars->drel[st]));
-            }
-            const float inv = (got && l > 0.f) ? 1.f / l : 0.f;
-            if (valid) {
-#pragma unroll
-                for (int e = 0; e < kHeadDim; e += 8) {
-                    const uint4 w = make_uint4(pack2(oacc[e] * inv, oacc[e + 1] * inv),
-                                               pack2(oacc[e + 2] * inv, oacc[e + 3] * inv),
-                                               pack2(oacc[e + 4] * inv, oacc[e + 5] * inv),
-                                               pack2(oacc[e + 6] * inv, oacc[e + 7] * inv));
-                    *reinterpret_cast<uint4*>(dst0 + e) = w;
-                }
+            for (int e = 0; e < 32; e += 8) {
+                const uint4 w = make_uint4(
+                    pack2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                    pack2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                    pack2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                    pack2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                *reinterpret_cast<uint4*>(dst + e) = w;
             }
         }
     }

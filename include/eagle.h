@@ -267,15 +267,18 @@ eagle_status eagle_kv_compact(void* k_cache, void* v_cache, int32_t* kv_len, con
  *   keys  = round-0 rows 0 .. i (the original tokens up to i) plus the rows of
  *           rounds 1 .. r at position i (its own chain, itself included);
  *   out   = softmax(scale * q . k) . v, fp32 accumulation, bf16 result.
- * The causal part runs on the tensor cores; the diagonal part (at most R1 - 1
- * keys per query) as per-position dot products, as the page suggests.
+ * Both parts run on the tensor cores: the diagonal part (at most R1 - 1 keys per
+ * query) as a few more 128-key tiles, each holding up to 128 / (positions per row
+ * tile) rounds of the tile's positions, with every key but a row's own masked (the
+ * page suggests per-position dot products; the result is the same).
  *   q    bf16 [B, S, Hq, head_dim]        (the queries of round r)
  *   k, v bf16 [B, Hkv, R1, S, head_dim]   (round 0 = original tokens; rounds
  *        1 .. R1-1 simulated; only rounds 0 .. r are read)
  *   out  bf16 [B, S, Hq, head_dim]
  * Sizes: S >= 1, 1 <= R1 <= 16, 0 <= r < R1, head_dim == 128, Hq % Hkv == 0,
- * B * Hkv * ceil(S * Hq / Hkv / 128) < 2^31.  Every row of round 0 must be finite (rows
- * past a query's position are read and masked).  All pointers 16-byte aligned.
+ * B * Hkv * ceil(S * Hq / Hkv / 128) < 2^31.  Every row of rounds 0 .. r must be finite
+ * (rows other than a query's own keys are read and masked; a zero weight does not
+ * cancel NaN).  All pointers 16-byte aligned.
  * Device errors: a wait that exceeds its limit sets EAGLE_DEV_TIMEOUT.
  * ------------------------------------------------------------------------- */
 eagle_status eagle_ttt_attn(const void* q, const void* k, const void* v, void* out, int B, int S,

@@ -3,7 +3,7 @@ double-precision oracle.
 
 Tolerance: per (sequence, position, head) row, max|O_gpu - O_ref| / max|O_ref| <= 1e-2,
 as for the tree attention (bf16 inputs and output, fp32 accumulation, P rounded to
-bf16 for the PV product of the causal part; the diagonal part stays in fp32).
+bf16 for the PV product, the diagonal keys included).
 """
 import numpy as np
 import pytest
@@ -44,6 +44,25 @@ def test_matches_oracle(B, S, Hq, Hkv, R1, r):
     ref = oracle.ttt_attn(q, k, v, r, scale)
     err = attn_row_rel_err(got, ref)
     assert err.max() <= TOL, (err.max(), np.unravel_index(err.argmax(), err.shape))
+
+
+@pytest.mark.parametrize("Hq,Hkv,R1,r", [(32, 8, 8, 3), (6, 2, 6, 2), (8, 8, 5, 1)])
+def test_rounds_after_r_are_never_read(Hq, Hkv, R1, r):
+    """Rounds r+1 .. R1-1 hold NaN and +inf (not yet simulated); the output must match
+    the oracle, which reads only rounds 0 .. r.  The diagonal boxes cover more rounds
+    than r needs (G = 4: 4 rounds per box, G = 3: 2, G = 1: 1)."""
+    B, S = 2, 150
+    q, k, v = W.ttt_inputs(B, S, Hq, Hkv, D, R1, seed=57 + r)
+    k, v = k.clone(), v.clone()
+    k[:, :, r + 1:] = float("nan")
+    v[:, :, r + 1:] = float("nan")
+    v[:, :, r + 1:, ::3] = float("inf")
+    scale = D ** -0.5
+    got, st = _run(q, k, v, r, scale)
+    assert st == 0
+    assert np.isfinite(got).all()
+    ref = oracle.ttt_attn(q, k, v, r, scale)
+    assert attn_row_rel_err(got, ref).max() <= TOL
 
 
 def test_full_size_rows_sampled():

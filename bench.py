@@ -32,9 +32,10 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "tree-verify steps/sec & accepted tokens/s at B=64; HBM GB/s vs roofline"
-# DRAM bytes (read + write) of one 640 x 4096 -> 128256 LM-head GEMM launch, from an
-# ncu capture of the current kernel: 1.0965e9 read + 0.3010e9 written.
-GEMM_LAUNCH_DRAM_BYTES = 1.3976e9
+# DRAM bytes (read + write) of one 640 x 4096 -> 128256 LM-head GEMM launch with its
+# per-tile partials (the step's form), from an ncu capture of the current kernel:
+# 1.0795e9 read + 0.3035e9 written.
+GEMM_LAUNCH_DRAM_BYTES = 1.3830e9
 CFG = W.CONFIGS["eagle3_b64"]
 SEED = 0
 
@@ -377,7 +378,8 @@ def run_ours(args, rank, world, dist):
                      "achieved": round(gemm_tflops, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / peak, 4), "traffic": GEMM_LAUNCH_DRAM_BYTES,
                      "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum of one "
-                                     "640-row launch (ncu); algorithmic 1.384e9",
+                                     "640-row launch with per-tile partials (ncu); "
+                                     "algorithmic 1.384e9",
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained",
                      "flops_per_launch": full_flops,
                      "ms_per_launch": round(full_ms, 4),

@@ -387,6 +387,14 @@ def run_ours(args, rank, world, dist):
                      "gemm_flops_per_step_all_levels": gemm_flops / eager_steps,
                      "timed": f"{eager_steps} eager steps, events around each launch"},
         "breakdown_ms": br,
+        "verify_step": {
+            "calls": "tree attention (1 layer) + verify-and-accept (T = 1) + KV compaction "
+                     "(32 layers), one after another; the draft expansion excluded",
+            "ms_median": br["verify_step"],
+            "steps_per_s": round(world * 1e3 / br["verify_step"], 1),
+            "accepted_tokens_per_s": round(world * st.B * br["verify_step_mean_accept_len_plus_1"]
+                                           * 1e3 / br["verify_step"], 1),
+            "timing": "median of 200 calls after 20 warm-up, one event pair per call"},
         "roofline_hbm": hbm_rooflines(br, peaks),
         "other_configs": other,
         "ttt_attn": ttt,
@@ -741,6 +749,18 @@ def breakdown(st, torch, reps=20):
         E.eagle_kv_compact(st.kc, st.vc, st.kv_len, st.path, st.accept_len, st.D)
         st.kv_len.copy_(st.kv_len0)
     res["kv_compact_32_layers"] = round(t(comp), 4)
+
+    # the verify step alone, the draft expansion excluded: attention (1 layer), the walk
+    # and the compaction (32 layers) one after another, 200 calls after 20 warm-up
+    def vstep():
+        E.eagle_tree_attn(st.q, st.kc[0], st.vc[0], st.kv_len0, st.parent, out=st.attn_out,
+                          workspace=st.attn_ws)
+        E.eagle_verify_accept(st.target, st.logits, st.tokens, st.parent, st.D, 1.0, 7,
+                              draft_row=st.draft_row, accept_len=st.accept_len, path=st.path,
+                              emit=st.emit)
+        comp()
+    res["verify_step"] = round(timed_ms(vstep, torch, reps=200, warm=20), 4)
+    res["verify_step_mean_accept_len_plus_1"] = round(float(st.accept_len.float().mean()) + 1, 4)
     # T = 1: the row statistics (max, sum) the walk needs; the argmax is the T = 0 output
     s = t(lambda: E.eagle_softmax_stats(st.target, 1.0, argmax=False))
     res["softmax_stats_all_rows_standalone"] = round(s, 4)

@@ -50,10 +50,6 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ float unit_closed_open(uint32_t w) {
     return (float)(w >> 8) * 0x1p-24f;
 }
-// Odd multiples of 2^-24 in (0, 1).
-__device__ __forceinline__ float unit_open(uint32_t w) {
-    return (float)(2u * (w >> 9) + 1u) * 0x1p-24f;
-}
 
 __device__ __forceinline__ float accept_uniform(uint64_t seed, uint32_t b, uint32_t node) {
     uint4 w = philox4x32_10(make_uint4(0u, node, b, kTagAccept), (uint32_t)seed,
@@ -67,27 +63,6 @@ __device__ __forceinline__ float accept_uniform(uint64_t seed, uint32_t b, uint3
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Online-softmax pair: (max, sum of exp(x - max)).  -inf max means "empty".
-struct MaxSum {
-    float m, s;
-};
-
-__device__ __forceinline__ MaxSum ms_combine(MaxSum a, MaxSum b) {
-    if (b.m == -INFINITY) return a;
-    if (a.m == -INFINITY) return b;
-    float m = fmaxf(a.m, b.m);
-    return MaxSum{m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
-}
-
-__device__ __forceinline__ MaxSum warp_ms(MaxSum v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        MaxSum w{__shfl_xor_sync(0xffffffffu, v.m, o), __shfl_xor_sync(0xffffffffu, v.s, o)};
-        v = ms_combine(v, w);
-    }
     return v;
 }
 
